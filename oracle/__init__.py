@@ -1,0 +1,157 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+This package checks the CUDA path; the library never imports it.  Only the
+tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg use it.
+
+``attn_fwd_oracle`` computes the plain two-pass definition of attention with a
+causal mask, grouped-query heads and packed variable-length sequences, in fp64,
+from the exact bf16 input values (see ``attn_oracle.c`` for the definition and
+the passages it follows: tang, sections 2.1-2.4 and 6; TileLang explainer,
+"FlashAttention, in tiles").
+
+Parity status: pinned.  The tests in ``tests/test_oracle.py`` check it against
+closed forms, invariants, an independent brute-force evaluation and the
+online-softmax merge of chunk states.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/liboracle.so`` with gcc and OpenMP."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = [
+            "gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+            "-o", _LIB, _SRC, "-lm",
+        ]
+        subprocess.run(cmd, check=True)
+    return _LIB
+
+
+def load_library(path: str):
+    """Open a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_attn_fwd.restype = ctypes.c_int
+    lib.oracle_attn_fwd.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q k v
+        ctypes.c_void_p, ctypes.c_void_p,                   # o lse
+        ctypes.c_int, i64p, i64p, i64p, i64p,               # nseq, starts/lens
+        ctypes.c_int, ctypes.c_int, ctypes.c_int,           # Hq Hkv d
+        ctypes.c_double, ctypes.c_int, ctypes.c_int,        # scale causal round_p
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,      # nsel sel nthreads
+    ]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = load_library(_LIB)
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor/array -> contiguous uint16 numpy array of its bits."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            assert x.dtype == torch.bfloat16, x.dtype
+            return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(x)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def attention_core(q, k, v, q_start, q_len, k_start, k_len, Hq, Hkv, d, scale,
+                   causal, round_p=False, sel=None, nthreads=0, lib=None):
+    """Direct call of the C oracle.
+
+    q: bf16 [rows_q, Hq, d]; k, v: bf16 [rows_k, Hkv, d] (torch bf16 tensors
+    or uint16 bit arrays).  Sequence s owns query rows q_start[s] ..
+    q_start[s]+q_len[s]-1 and keys k_start[s] .. k_start[s]+k_len[s]-1.
+
+    Returns (o, lse) in fp64: with sel=None, o is [rows_q, Hq, d] and lse
+    [rows_q, Hq] (rows outside every sequence stay NaN); with sel an int32
+    array of (s, h, i) triples, o is [n, d] and lse [n].
+    """
+    lib = _load() if lib is None else lib
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    rows_q = qb.size // (Hq * d)
+    nseq = len(q_len)
+    arr = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+    qs, ql, ks, kl = arr(q_start), arr(q_len), arr(k_start), arr(k_len)
+    for s in range(nseq):
+        assert qs[s] + ql[s] <= rows_q
+        assert ks[s] + kl[s] <= kb.size // (Hkv * d)
+    if sel is None:
+        o = np.full((rows_q, Hq, d), np.nan)
+        lse = np.full((rows_q, Hq), np.nan)
+        nsel, selp = -1, None
+    else:
+        sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 3))
+        o = np.full((sel.shape[0], d), np.nan)
+        lse = np.full((sel.shape[0],), np.nan)
+        nsel, selp = sel.shape[0], sel.ctypes.data
+    i64 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    rc = lib.oracle_attn_fwd(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, o.ctypes.data, lse.ctypes.data,
+        nseq, i64(qs), i64(ql), i64(ks), i64(kl), Hq, Hkv, d, float(scale),
+        int(bool(causal)), int(bool(round_p)), nsel, selp, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_fwd rejected its arguments (code {rc})")
+    return o, lse
+
+
+def attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
+                    round_p=False, rows=None, nthreads=0, lib=None):
+    """The oracle in the library's calling convention and layouts.
+
+    Fixed batch (cu_seqlens None): q, o are [B, N, Hq, d]; k, v [B, N, Hkv, d];
+    LSE is [B, Hq, N].  Packed (cu_seqlens = B+1 offsets): q, o [T, Hq, d];
+    k, v [T, Hkv, d]; LSE [Hq, T], T = cu_seqlens[B].
+
+    rows=None computes everything and returns (o, lse) in those layouts (fp64).
+    rows = array of (seq, h, i) triples computes only those rows and returns
+    (o [n, d], lse [n]).
+    """
+    if cu_seqlens is None:
+        starts = [b * N for b in range(B)]
+        lens = [N] * B
+        T = B * N
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64).reshape(-1)
+        assert cu.size == B + 1
+        starts = cu[:-1].tolist()
+        lens = (cu[1:] - cu[:-1]).tolist()
+        T = int(cu[-1])
+    o, lse = attention_core(q, k, v, starts, lens, starts, lens, Hq, Hkv, d, scale,
+                            causal, round_p=round_p, sel=rows, nthreads=nthreads,
+                            lib=lib)
+    if rows is not None:
+        return o, lse
+    if cu_seqlens is None:
+        o = o.reshape(B, N, Hq, d)
+        lse = lse.reshape(B, N, Hq).transpose(0, 2, 1).copy()
+    else:
+        o = o.reshape(T, Hq, d)
+        lse = lse.reshape(T, Hq).T.copy()
+    return o, lse

@@ -1,0 +1,223 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct fp64 CPU attention forward.  It exists to
+ * check the CUDA path; nothing in the library calls it, links it or shares
+ * code with it.  Only the tests, the package's smoke check and the benchmark's
+ * CPU-baseline leg load it.
+ *
+ * What it computes (the plain definition, no tiling, no online rescaling):
+ *
+ *   for every sequence s, query head h, query row i of s:
+ *     kv      = floor(h / (Hq / Hkv))                 grouped-query head map
+ *     valid   = { j : 0 <= j < Lk(s) }  and, if causal, j <= i
+ *     s_ij    = scale * sum_t q[i,h,t] * k[j,kv,t]     (fp64, inputs widened
+ *                                                       exactly from bf16)
+ *     m_i     = max_{j in valid} s_ij
+ *     l_i     = sum_{j in valid} exp(s_ij - m_i)
+ *     o[i,h,:]= sum_{j in valid} exp(s_ij - m_i) * v[j,kv,:] / l_i
+ *     lse[i,h]= m_i + ln(l_i)
+ *
+ * Sources:
+ *  - tang (muni.works/research/tang), section 2.2 "Comprehensions and
+ *    monoids" and section 2.3 "Rewrites" (stabilize_softmax): attention is
+ *    the score contraction followed by max, sum of exponentials and the
+ *    weighted value sum over the same scores; the fused online form is
+ *    equal to this two-pass form (section 6, the Lean theorem that online
+ *    softmax equals two-pass softmax).  So the oracle is the two-pass form.
+ *  - tang, section 2.1 "Views": grouped-query attention splits the query
+ *    head into (kv head, group); read here as contiguous groups.
+ *  - tang, section 2.4, Table 1 row "logsumexp": the per-row LSE output,
+ *    read here as the natural logarithm m + ln(l).
+ *  - tang, section 4 "Precision is a schedule": an f64 evaluator is the
+ *    reference; the optional round_p switch mimics its emulated mode for
+ *    one value only (P rounded to bf16, round-to-nearest-even, before the
+ *    P.V product), as a diagnostic.
+ *  - TileLang explainer (ai.thesatyajit.com/articles/tilelang), section
+ *    "FlashAttention, in tiles": the per-block loop casts P to the input
+ *    type before the P.V product; that is what round_p imitates.
+ *
+ * Rows with no valid key cannot occur when causal rows see themselves; if
+ * one is requested anyway it gets o = 0 and lse = -inf.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bits -> double, exactly (bf16 is the top half of an IEEE binary32). */
+static double bf16_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* double -> nearest bf16 value (ties to even), returned as a double.  Used
+ * only by the round_p diagnostic; inputs are finite and non-negative. */
+static double round_to_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/*
+ * One query row against the keys of its sequence.
+ *   qrow : pointer to q[i, h, 0]            (bf16 bits, d values)
+ *   kbase: pointer to k[k_start, kv, 0]     (row stride kstride elements)
+ *   vbase: pointer to v[k_start, kv, 0]
+ *   nvalid: number of visible keys (keys 0 .. nvalid-1)
+ *   scores: scratch of at least nvalid doubles
+ *   out: d doubles; *lse_out: one double
+ */
+static void one_row(const uint16_t *qrow, const uint16_t *kbase,
+                    const uint16_t *vbase, int64_t kstride, int64_t nvalid,
+                    int d, double scale, int round_p, double *scores,
+                    double *out, double *lse_out) {
+  for (int t = 0; t < d; ++t) out[t] = 0.0;
+  if (nvalid <= 0) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  /* pass 0: the score row */
+  for (int64_t j = 0; j < nvalid; ++j) {
+    const uint16_t *krow = kbase + j * kstride;
+    double acc = 0.0;
+    for (int t = 0; t < d; ++t) acc += bf16_to_double(qrow[t]) * bf16_to_double(krow[t]);
+    scores[j] = scale * acc;
+  }
+  /* pass 1: the row maximum */
+  double m = scores[0];
+  for (int64_t j = 1; j < nvalid; ++j)
+    if (scores[j] > m) m = scores[j];
+  /* pass 2: the sum of exponentials and the weighted value sum */
+  double l = 0.0;
+  for (int64_t j = 0; j < nvalid; ++j) {
+    double p = exp(scores[j] - m);
+    l += p;
+    double pw = round_p ? round_to_bf16(p) : p;
+    const uint16_t *vrow = vbase + j * kstride;
+    for (int t = 0; t < d; ++t) out[t] += pw * bf16_to_double(vrow[t]);
+  }
+  for (int t = 0; t < d; ++t) out[t] /= l;
+  *lse_out = m + log(l);
+}
+
+/*
+ * oracle_attn_fwd
+ *
+ * q: [*, Hq, d] bf16 bits; k, v: [*, Hkv, d] bf16 bits (token rows packed;
+ * row r of sequence s is token q_start[s] + r, resp. k_start[s] + r).
+ * nseq sequences; sequence s has q_len[s] query rows and k_len[s] keys.
+ * causal requires q_len[s] == k_len[s]; key j is visible from row i iff
+ * j <= i.
+ *
+ * If nsel < 0, every row is computed:
+ *   o  [(q_start[s] + i) * Hq + h) * d + t]
+ *   lse[(q_start[s] + i) * Hq + h]
+ * Otherwise sel holds nsel triples (s, h, i) and the results go to
+ *   o[n * d + t], lse[n]  for triple n.
+ *
+ * nthreads <= 0 uses the OpenMP default.  Returns 0, or a negative code on
+ * invalid arguments (nothing is written then).
+ */
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    double *o, double *lse, int nseq, const int64_t *q_start,
+                    const int64_t *q_len, const int64_t *k_start,
+                    const int64_t *k_len, int Hq, int Hkv, int d, double scale,
+                    int causal, int round_p, int64_t nsel, const int32_t *sel,
+                    int nthreads) {
+  if (nseq < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
+  int64_t kmax = 0;
+  for (int s = 0; s < nseq; ++s) {
+    if (q_len[s] < 0 || k_len[s] < 0) return -2;
+    if (causal && q_len[s] != k_len[s]) return -3;
+    if (k_len[s] > kmax) kmax = k_len[s];
+  }
+  const int group = Hq / Hkv;
+  const int64_t qstride = (int64_t)Hq * d;  /* elements between token rows */
+  const int64_t kstride = (int64_t)Hkv * d;
+
+  /* the list of (s, h, i) jobs */
+  int64_t njobs = 0;
+  int32_t *jobs = NULL;
+  if (nsel >= 0) {
+    njobs = nsel;
+    for (int64_t n = 0; n < nsel; ++n) {
+      int32_t s = sel[3 * n], h = sel[3 * n + 1], i = sel[3 * n + 2];
+      if (s < 0 || s >= nseq || h < 0 || h >= Hq || i < 0 || i >= q_len[s]) return -4;
+    }
+  } else {
+    for (int s = 0; s < nseq; ++s) njobs += q_len[s] * (int64_t)Hq;
+    jobs = (int32_t *)malloc(sizeof(int32_t) * 3 * (size_t)(njobs > 0 ? njobs : 1));
+    if (!jobs) return -5;
+    int64_t n = 0;
+    for (int s = 0; s < nseq; ++s)
+      for (int64_t i = 0; i < q_len[s]; ++i)
+        for (int h = 0; h < Hq; ++h) {
+          jobs[3 * n] = s;
+          jobs[3 * n + 1] = h;
+          jobs[3 * n + 2] = (int32_t)i;
+          ++n;
+        }
+  }
+  const int32_t *list = (nsel >= 0) ? sel : jobs;
+
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+
+  int failed = 0;
+#pragma omp parallel
+  {
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(kmax > 0 ? kmax : 1));
+    if (!scores) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t n = 0; n < njobs; ++n) {
+        int s = list[3 * n], h = list[3 * n + 1];
+        int64_t i = list[3 * n + 2];
+        int kv = h / group;
+        int64_t nvalid = causal ? (i + 1) : k_len[s];
+        if (nvalid > k_len[s]) nvalid = k_len[s];
+        const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;
+        const uint16_t *kb = k + k_start[s] * kstride + (int64_t)kv * d;
+        const uint16_t *vb = v + k_start[s] * kstride + (int64_t)kv * d;
+        double *orow;
+        double *lrow;
+        if (nsel >= 0) {
+          orow = o + n * d;
+          lrow = lse + n;
+        } else {
+          int64_t r = (q_start[s] + i) * Hq + h;
+          orow = o + r * d;
+          lrow = lse + r;
+        }
+        one_row(qrow, kb, vb, kstride, nvalid, d, scale, round_p, scores, orow, lrow);
+      }
+      free(scores);
+    }
+  }
+  free(jobs);
+  return failed ? -5 : 0;
+}
+
+/* The number of threads an OpenMP region would use (for reporting). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

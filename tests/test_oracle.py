@@ -1,0 +1,352 @@
+"""Pins for the fp64 oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something the pages or the mathematics
+fix: an exact brute-force evaluation, closed forms, invariants and the
+online-softmax monoid merge (tang, section 2.2 and Table 1; section 6: online
+softmax is a commutative semigroup equal to two-pass softmax, and softmax is
+shift invariant).  A plausible slip in the oracle -- a dropped scale, a
+wrong causal bound, a wrong group mapping, log2 for ln, a transposed
+operand, a missing max subtraction -- fails at least one of them.
+"""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import attention_core, attn_fwd_oracle
+
+
+def bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def rand_bf16(shape, seed, mult=1.0):
+    g = torch.Generator("cpu").manual_seed(seed)
+    return (torch.randn(shape, generator=g) * mult).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# (viii) brute force with exact summation, on tiny inputs
+# ---------------------------------------------------------------------------
+def brute_force(q, k, v, lens, Hq, Hkv, d, scale, causal):
+    """Exact-summation evaluation straight from the softmax definition."""
+    qf = q.float().tolist()
+    kf = k.float().tolist()
+    vf = v.float().tolist()
+    g = Hq // Hkv
+    T = sum(lens)
+    O = [[[0.0] * d for _ in range(Hq)] for _ in range(T)]
+    LSE = [[0.0] * Hq for _ in range(T)]
+    start = 0
+    for L in lens:
+        for i in range(L):
+            for h in range(Hq):
+                kvh = h // g
+                js = list(range(i + 1)) if causal else list(range(L))
+                sc = [scale * math.fsum(qf[start + i][h][t] * kf[start + j][kvh][t]
+                                        for t in range(d)) for j in js]
+                m = max(sc)
+                e = [math.exp(x - m) for x in sc]
+                l = math.fsum(e)
+                for t in range(d):
+                    O[start + i][h][t] = math.fsum(e[n] * vf[start + j][kvh][t]
+                                                   for n, j in enumerate(js)) / l
+                LSE[start + i][h] = m + math.log(l)
+        start += L
+    return np.array(O), np.array(LSE)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2), (6, 3), (4, 1)])
+def test_brute_force_fixed_batch(causal, Hq, Hkv):
+    B, N, d = 2, 9, 5
+    q = rand_bf16((B, N, Hq, d), 1)
+    k = rand_bf16((B, N, Hkv, d), 2)
+    v = rand_bf16((B, N, Hkv, d), 3)
+    scale = 0.37
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal)
+    Ob, Lb = brute_force(q.reshape(B * N, Hq, d), k.reshape(B * N, Hkv, d),
+                         v.reshape(B * N, Hkv, d), [N] * B, Hq, Hkv, d, scale, causal)
+    np.testing.assert_allclose(o.reshape(B * N, Hq, d), Ob, rtol=0, atol=1e-12)
+    # oracle LSE layout is [B, Hq, N]
+    np.testing.assert_allclose(lse.transpose(0, 2, 1).reshape(B * N, Hq), Lb, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_packed(causal):
+    lens = [5, 1, 7, 3, 0, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, Hq, Hkv, d = int(cu[-1]), 4, 2, 6
+    q = rand_bf16((T, Hq, d), 11, 2.0)
+    k = rand_bf16((T, Hkv, d), 12)
+    v = rand_bf16((T, Hkv, d), 13)
+    o, lse = attn_fwd_oracle(q, k, v, len(lens), Hq, Hkv, T, d, 0.5, causal, cu_seqlens=cu)
+    Ob, Lb = brute_force(q, k, v, lens, Hq, Hkv, d, 0.5, causal)
+    np.testing.assert_allclose(o, Ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, Lb.T, rtol=0, atol=1e-12)   # LSE is [Hq, T]
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+def test_hand_worked_example():
+    """q=[1,0]; keys [1,0],[0,1],[1,1]; values [1,0],[0,1],[2,3]; scale 1.
+    Scores 1,0,1; with x = e^-1 the weights are 1, x, 1 over 2+x, so
+    O = (3/(2+x), (x+3)/(2+x)) and LSE = 1 + ln(2+x)."""
+    q = bf16([[[1.0, 0.0]], [[0.0, 0.0]], [[0.0, 0.0]]])          # [3, 1, 2]; row 0 used
+    k = bf16([[[1.0, 0.0]], [[0.0, 1.0]], [[1.0, 1.0]]])
+    v = bf16([[[1.0, 0.0]], [[0.0, 1.0]], [[2.0, 3.0]]])
+    o, lse = attn_fwd_oracle(q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), 1, 1, 1, 3, 2,
+                             1.0, False)
+    x = math.exp(-1.0)
+    assert abs(o[0, 0, 0, 0] - 3 / (2 + x)) < 1e-15
+    assert abs(o[0, 0, 0, 1] - (x + 3) / (2 + x)) < 1e-15
+    assert abs(lse[0, 0, 0] - (1 + math.log(2 + x))) < 1e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_q_closed_form(causal):
+    """Q = 0: every visible score is 0, so LSE_i = ln |valid(i)| (natural log)
+    and O_i is the plain mean of V over the visible keys."""
+    B, N, Hq, Hkv, d = 2, 13, 4, 2, 8
+    q = torch.zeros((B, N, Hq, d), dtype=torch.bfloat16)
+    k = rand_bf16((B, N, Hkv, d), 21)
+    v = rand_bf16((B, N, Hkv, d), 22)
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, 0.125, causal)
+    vf = v.double().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(N):
+                n = i + 1 if causal else N
+                assert abs(lse[b, h, i] - math.log(n)) < 1e-14
+                mean = np.array([math.fsum(vf[b, :n, h // 2, t]) / n for t in range(d)])
+                np.testing.assert_allclose(o[b, i, h], mean, rtol=0, atol=1e-14)
+
+
+def test_causal_row0():
+    """A causal row 0 sees only key 0: O[0] = V[0] and LSE[0] = scale*q0.k0."""
+    B, N, Hq, Hkv, d = 3, 17, 6, 2, 16
+    q = rand_bf16((B, N, Hq, d), 31)
+    k = rand_bf16((B, N, Hkv, d), 32)
+    v = rand_bf16((B, N, Hkv, d), 33)
+    scale = 0.25
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, True)
+    qd, kd, vd = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_array_equal(o[b, 0, h], vd[b, 0, h // 3])
+            s00 = scale * math.fsum(qd[b, 0, h] * kd[b, 0, h // 3])
+            assert abs(lse[b, h, 0] - s00) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_sum_to_one(causal):
+    """With V = identity (d = N, V[j] = e_j) the output row IS the softmax row:
+    non-negative, zero on masked keys, summing to 1."""
+    N = 16
+    q = rand_bf16((1, N, 2, N), 41, 3.0)
+    k = rand_bf16((1, N, 1, N), 42)
+    v = torch.eye(N, dtype=torch.bfloat16).reshape(1, N, 1, N)
+    o, _ = attn_fwd_oracle(q, k, v, 1, 2, 1, N, N, 0.3, causal)
+    P = o[0]                       # [N, H, N]
+    assert (P >= 0).all()
+    np.testing.assert_allclose(P.sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+    if causal:
+        for i in range(N):
+            assert (P[i, :, i + 1:] == 0).all()
+            assert (P[i, :, : i + 1] > 0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v(causal):
+    """V = c everywhere gives O = c (weights sum to 1)."""
+    B, N, Hq, d = 2, 40, 4, 8
+    q = rand_bf16((B, N, Hq, d), 51, 4.0)
+    k = rand_bf16((B, N, Hq, d), 52)
+    v = torch.full((B, N, Hq, d), 0.75, dtype=torch.bfloat16)
+    o, _ = attn_fwd_oracle(q, k, v, B, Hq, Hq, N, d, 0.5, causal)
+    np.testing.assert_allclose(o, 0.75, rtol=0, atol=1e-14)
+
+
+def test_key_permutation_noncausal():
+    """Non-causal attention is a sum over keys: permuting K and V rows together
+    changes nothing (tang section 5: keys may be permuted because the reduction
+    is commutative and associative)."""
+    B, N, Hq, Hkv, d = 2, 33, 4, 4, 8
+    q = rand_bf16((B, N, Hq, d), 61)
+    k = rand_bf16((B, N, Hkv, d), 62)
+    v = rand_bf16((B, N, Hkv, d), 63)
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(64))
+    o1, l1 = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, 0.4, False)
+    o2, l2 = attn_fwd_oracle(q, k[:, perm], v[:, perm], B, Hq, Hkv, N, d, 0.4, False)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_shift_invariance(causal):
+    """Adding the same constant to every score of a row shifts LSE by it and
+    leaves O alone.  A spare feature t0 with q=1 and k=c adds scale*c to all
+    scores."""
+    B, N, Hq, d = 1, 24, 2, 8
+    q = rand_bf16((B, N, Hq, d), 71)
+    k = rand_bf16((B, N, Hq, d), 72)
+    v = rand_bf16((B, N, Hq, d), 73)
+    q[..., 0] = 1.0
+    k0 = k.clone()
+    k0[..., 0] = 0.0
+    kc = k.clone()
+    kc[..., 0] = 6.5
+    scale = 0.5
+    oa, la = attn_fwd_oracle(q, k0, v, B, Hq, Hq, N, d, scale, causal)
+    ob, lb = attn_fwd_oracle(q, kc, v, B, Hq, Hq, N, d, scale, causal)
+    np.testing.assert_allclose(ob, oa, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lb - la, scale * 6.5, rtol=0, atol=1e-12)
+
+
+def test_large_scores_stay_finite():
+    """Scores in the hundreds overflow exp() unless the row max is subtracted.
+    The result must be finite and agree with the library log-sum-exp."""
+    B, N, Hq, d = 1, 64, 2, 16
+    q = rand_bf16((B, N, Hq, d), 81, 30.0)
+    k = rand_bf16((B, N, Hq, d), 82, 30.0)
+    v = rand_bf16((B, N, Hq, d), 83)
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hq, N, d, 1.0, False)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    S = torch.einsum("bihd,bjhd->bhij", q.double(), k.double())
+    assert S.abs().max() > 800           # exp would overflow without the max
+    np.testing.assert_allclose(lse, torch.logsumexp(S, dim=-1).numpy(), rtol=1e-13, atol=1e-10)
+
+
+# ---------------------------------------------------------------------------
+# (i) merge of online-softmax chunk states in any order and tree shape
+# ---------------------------------------------------------------------------
+def combine(a, b):
+    """The online-softmax monoid on (m, l, o) with o carried unnormalised:
+    (tang, section 2.2 and Table 1 row "online softmax")."""
+    m1, l1, o1 = a
+    m2, l2, o2 = b
+    m = max(m1, m2)
+    w1, w2 = math.exp(m1 - m), math.exp(m2 - m)
+    return (m, l1 * w1 + l2 * w2, o1 * w1 + o2 * w2)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_merge_of_chunk_states_matches_two_pass(seed):
+    rng = random.Random(seed)
+    nq, nk, Hq, Hkv, d = 5, 37, 2, 1, 6
+    q = rand_bf16((nq, Hq, d), 100 + seed, 2.0)
+    k = rand_bf16((nk, Hkv, d), 200 + seed)
+    v = rand_bf16((nk, Hkv, d), 300 + seed)
+    scale = 0.45
+    o_full, l_full = attention_core(q, k, v, [0], [nq], [0], [nk], Hq, Hkv, d, scale, False)
+    # random chunking of the keys (chunks need not be contiguous)
+    keys = list(range(nk))
+    rng.shuffle(keys)
+    cuts = sorted(rng.sample(range(1, nk), rng.randint(1, 8)))
+    chunks = [keys[a:b] for a, b in zip([0] + cuts, cuts + [nk])]
+    states = []
+    for c in chunks:
+        idx = torch.tensor(c)
+        oc, lc = attention_core(q, k[idx], v[idx], [0], [nq], [0], [len(c)], Hq, Hkv, d,
+                                scale, False)
+        # a normalised chunk result (o, lse) is the state (lse, 1, o)
+        states.append([[(lc[i, h], 1.0, oc[i, h].copy()) for h in range(Hq)]
+                       for i in range(nq)])
+    for i in range(nq):
+        for h in range(Hq):
+            items = [s[i][h] for s in states]
+            # random merge tree: repeatedly merge two random neighbours or any pair
+            while len(items) > 1:
+                a = rng.randrange(len(items))
+                b = rng.randrange(len(items) - 1)
+                b = b + 1 if b >= a else b
+                x, y = items[a], items[b]
+                merged = combine(x, y) if rng.random() < 0.5 else combine(y, x)
+                items = [it for n, it in enumerate(items) if n not in (a, b)] + [merged]
+            m, l, o = items[0]
+            np.testing.assert_allclose(o / l, o_full[i, h], rtol=0, atol=1e-13)
+            assert abs((m + math.log(l)) - l_full[i, h]) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# (ix) library softmax cross-check, and the bf16-rounding diagnostic
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_torch_softmax_fp64(causal):
+    B, N, Hq, Hkv, d = 2, 70, 8, 2, 32
+    q = rand_bf16((B, N, Hq, d), 91, 2.0)
+    k = rand_bf16((B, N, Hkv, d), 92)
+    v = rand_bf16((B, N, Hkv, d), 93)
+    scale = d ** -0.5
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal)
+    kk = k.double().repeat_interleave(Hq // Hkv, dim=2)
+    vv = v.double().repeat_interleave(Hq // Hkv, dim=2)
+    S = torch.einsum("bihd,bjhd->bhij", q.double(), kk) * scale
+    if causal:
+        S = S.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    P = torch.softmax(S, dim=-1)
+    O = torch.einsum("bhij,bjhd->bihd", P, vv)
+    np.testing.assert_allclose(o, O.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(S, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_round_p_diagnostic_is_close_but_not_equal():
+    B, N, H, d = 1, 96, 2, 32
+    q = rand_bf16((B, N, H, d), 95)
+    k = rand_bf16((B, N, H, d), 96)
+    v = rand_bf16((B, N, H, d), 97)
+    o1, l1 = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.2, True)
+    o2, l2 = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.2, True, round_p=True)
+    np.testing.assert_array_equal(l1, l2)      # LSE uses unrounded weights
+    diff = np.abs(o1 - o2).max()
+    assert 0 < diff < 2e-2
+
+
+def test_row_selection_matches_full():
+    B, N, Hq, Hkv, d = 2, 50, 4, 2, 16
+    q = rand_bf16((B, N, Hq, d), 111)
+    k = rand_bf16((B, N, Hkv, d), 112)
+    v = rand_bf16((B, N, Hkv, d), 113)
+    o, lse = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, 0.3, True)
+    rows = [(1, 3, 49), (0, 0, 0), (1, 2, 17)]
+    os_, ls = attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, 0.3, True, rows=rows)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(os_[n], o[b, i, h])
+        assert ls[n] == lse[b, h, i]
+
+
+def test_rejects_bad_arguments():
+    q = rand_bf16((1, 4, 3, 8), 1)
+    k = rand_bf16((1, 4, 2, 8), 2)
+    with pytest.raises(ValueError):
+        attn_fwd_oracle(q, k, k, 1, 3, 2, 4, 8, 1.0, False)   # Hq % Hkv != 0
+    with pytest.raises(ValueError):   # causal needs equal query/key lengths
+        attention_core(q.reshape(4, 3, 8), k.reshape(4, 2, 8)[:, :1].contiguous(),
+                       k.reshape(4, 2, 8)[:, :1].contiguous(), [0], [4], [0], [3], 3, 1, 8,
+                       1.0, True)
+
+
+def test_threads_reported():
+    assert oracle.max_threads() >= 1
+
+
+def test_golden_regression_record():
+    import json
+    import os
+    import sys
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    sys.path.insert(0, here)
+    from make_golden import case
+    meta, q, k, v = case()
+    rec = json.load(open(os.path.join(here, "oracle_regression_small.json")))
+    o, lse = attn_fwd_oracle(q, k, v, meta["B"], meta["Hq"], meta["Hkv"], meta["N"], meta["d"],
+                             meta["scale"], meta["causal"])
+    np.testing.assert_allclose(o.reshape(-1), rec["o"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse.reshape(-1), rec["lse"], rtol=0, atol=1e-15)

@@ -1,0 +1,89 @@
+"""The oracle's pins must catch plausible slips.
+
+Each case compiles a copy of the oracle with one deliberate mistake (on the
+CPU, in a temporary directory) and checks that at least one pin from
+``test_oracle.py`` rejects it.  This guards the pins themselves: a pin set
+that a wrong oracle passes would prove nothing.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from test_oracle import brute_force, rand_bf16
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+MUTANTS = {
+    "causal bound off by one": ("nvalid = causal ? (i + 1)", "nvalid = causal ? (i)"),
+    "group mapping h % Hkv": ("int kv = h / group;", "int kv = h % Hkv;"),
+    "log2 instead of ln": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    "scale dropped": ("scores[j] = scale * acc;", "scores[j] = acc;"),
+    "value row fixed": ("const uint16_t *vrow = vbase + j * kstride;",
+                        "const uint16_t *vrow = vbase;"),
+    "key used as value": ("out[t] += pw * bf16_to_double(vrow[t]);",
+                          "out[t] += pw * bf16_to_double(kbase[j * kstride + t]);"),
+    "no max subtraction": ("double p = exp(scores[j] - m);", "double p = exp(scores[j]);"),
+    "max starts at zero": ("double m = scores[0];", "double m = 0.0;"),
+    "no normalisation": ("for (int t = 0; t < d; ++t) out[t] /= l;", ""),
+    "q row of the kv head": ("const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;",
+                             "const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)kv * d;"),
+}
+
+
+def _build_mutant(tmp_path, before, after):
+    src = open(SRC).read()
+    assert src.count(before) == 1, before
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(before, after))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                    "-o", str(so), str(path), "-lm"], check=True)
+    return oracle.load_library(str(so))
+
+
+def _pins_pass(lib) -> bool:
+    """A compact run of the pins; False as soon as one fails."""
+    # brute force, GQA, causal and not, packed sequences
+    for causal in (False, True):
+        lens = [7, 3, 9]
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T, Hq, Hkv, d = int(cu[-1]), 4, 2, 5
+        q = rand_bf16((T, Hq, d), 1, 2.0)
+        k = rand_bf16((T, Hkv, d), 2)
+        v = rand_bf16((T, Hkv, d), 3)
+        o, lse = oracle.attn_fwd_oracle(q, k, v, 3, Hq, Hkv, T, d, 0.5, causal,
+                                        cu_seqlens=cu, lib=lib)
+        Ob, Lb = brute_force(q, k, v, lens, Hq, Hkv, d, 0.5, causal)
+        if not (np.allclose(o, Ob, atol=1e-12, rtol=0) and np.allclose(lse, Lb.T, atol=1e-12, rtol=0)):
+            return False
+    # large scores stay finite and match the library log-sum-exp
+    q = rand_bf16((1, 64, 2, 16), 81, 30.0)
+    k = rand_bf16((1, 64, 2, 16), 82, 30.0)
+    v = rand_bf16((1, 64, 2, 16), 83)
+    o, lse = oracle.attn_fwd_oracle(q, k, v, 1, 2, 2, 64, 16, 1.0, False, lib=lib)
+    S = torch.einsum("bihd,bjhd->bhij", q.double(), k.double())
+    if not (np.isfinite(o).all() and np.allclose(lse, torch.logsumexp(S, -1).numpy(), rtol=1e-13)):
+        return False
+    # Q = 0 closed form
+    q = torch.zeros((1, 9, 2, 4), dtype=torch.bfloat16)
+    k = rand_bf16((1, 9, 2, 4), 5)
+    o, lse = oracle.attn_fwd_oracle(q, k, k, 1, 2, 2, 9, 4, 1.0, True, lib=lib)
+    if not all(abs(lse[0, h, i] - math.log(i + 1)) < 1e-14 for h in range(2) for i in range(9)):
+        return False
+    return True
+
+
+def test_unmutated_oracle_passes_compact_pins():
+    assert _pins_pass(oracle._load())
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    lib = _build_mutant(tmp_path, before, after)
+    assert not _pins_pass(lib), f"pins did not catch: {name}"
