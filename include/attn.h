@@ -1,0 +1,112 @@
+/*
+ * attn.h -- C ABI of libattn: fused attention forward for sm_103a (GB300).
+ *
+ * The operation
+ * -------------
+ * For every sequence, query head h and query row i:
+ *
+ *     kv     = h / (Hq / Hkv)                     (contiguous head groups)
+ *     s_ij   = scale * <q[i,h,:], k[j,kv,:]>      for visible keys j
+ *     o[i,h] = softmax_j(s_ij) . v[:,kv,:]
+ *     lse    = ln sum_j exp(s_ij)                 (natural logarithm)
+ *
+ * visible keys: all keys of the same sequence, or, when causal, keys j <= i.
+ * The score matrix is never written to memory: the kernel keeps a running
+ * row maximum and a rescaled running sum per row (the online-softmax monoid
+ * of tang, muni.works/research/tang, section 2.2 and Table 1 "online
+ * softmax" / "FlashAttention forward"; the per-block loop of the TileLang
+ * explainer, ai.thesatyajit.com/articles/tilelang, "FlashAttention, in
+ * tiles").  The grouped-query head split follows tang section 2.1 "Views";
+ * the logsumexp output is tang Table 1 "logsumexp".
+ *
+ * Arithmetic: bf16 inputs, fp32 accumulation on the tensor cores, fp32
+ * softmax with base-2 exponentials, probabilities rounded to bf16 before the
+ * P.V product, output rounded to bf16 (nearest even), LSE in fp32.
+ *
+ * Layouts (all row-major, contiguous, no padding)
+ * -----------------------------------------------
+ *   fixed batch (cu_seqlens == NULL):
+ *     q, o : [B, N, Hq,  d] bf16      k, v : [B, N, Hkv, d] bf16
+ *     lse  : [B, Hq, N] fp32
+ *   packed variable-length batch (cu_seqlens != NULL):
+ *     q, o : [T, Hq,  d] bf16         k, v : [T, Hkv, d] bf16
+ *     lse  : [Hq, T] fp32,  T = N = cu_seqlens[B]
+ *     sequence s owns token rows cu_seqlens[s] .. cu_seqlens[s+1]-1.
+ *
+ * Ownership: every pointer is caller-owned DEVICE memory on the current
+ * device.  The library allocates no memory and keeps no reference after the
+ * call returns.  Calls are asynchronous and ordered on `stream`.
+ */
+#ifndef LIBATTN_ATTN_H_
+#define LIBATTN_ATTN_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,        /* a size, flag or pointer is out of range    */
+  ATTN_ERR_ALIGNMENT = 2,          /* q/k/v/o not 16-byte aligned, lse not 4     */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  ATTN_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed           */
+  ATTN_ERR_TIMEOUT = 5,            /* a kernel pipeline wait ran out (device-side) */
+  ATTN_ERR_BAD_SEQLENS = 6         /* cu_seqlens inconsistent (device-side check)  */
+} attn_status;
+
+/*
+ * attn_fwd -- O = softmax(scale * Q K^T + mask) V and the per-row LSE.
+ *
+ *   q, k, v   : device bf16 inputs in the layouts above (16-byte aligned).
+ *   o         : device bf16 output (16-byte aligned).
+ *   lse       : device fp32 output (4-byte aligned).
+ *   B         : batch size, or number of packed sequences (>= 0).
+ *   Hq, Hkv   : query and key/value heads, Hq % Hkv == 0, both >= 1.
+ *   N         : fixed batch: tokens per sequence (>= 0);
+ *               packed: total tokens T = cu_seqlens[B].
+ *   d         : head dimension, one of 64, 128, 256.
+ *   scale     : score multiplier, finite and > 0 (usually 1/sqrt(d)).
+ *   causal    : nonzero masks keys after the query (j > i, per sequence).
+ *   cu_seqlens: NULL for a fixed batch, else device int32[B+1] with
+ *               cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = N.
+ *               The kernel checks this and reports ATTN_ERR_BAD_SEQLENS
+ *               through attn_get_status() (outputs then stay unwritten).
+ *   stream    : CUDA stream (0 = legacy default stream).
+ *
+ * Returns ATTN_OK once the kernel is enqueued (or when there is no work:
+ * B == 0 or N == 0).  Host-side argument errors return their code without
+ * launching anything.  Device-side errors (a pipeline wait that ran past
+ * its time limit, bad cu_seqlens) are recorded in a per-device status word
+ * read by attn_get_status().
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     const int *cu_seqlens, cudaStream_t stream);
+
+/*
+ * attn_get_status -- synchronises `stream`, then reads and clears the
+ * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
+ * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.
+ */
+attn_status attn_get_status(cudaStream_t stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+const char *attn_status_string(attn_status s);
+
+/*
+ * attn_selftest_timeout -- exercises the kernels' bounded-wait path without
+ * faulting the GPU: launches one block that waits on a pipeline barrier no
+ * one signals, with a time limit of `timeout_us` microseconds (1..1000000).
+ * The wait runs out, the kernel records ATTN_ERR_TIMEOUT in the status word
+ * and returns.  This call synchronises `stream` and returns what
+ * attn_get_status() then reports (ATTN_ERR_TIMEOUT when the path works).
+ */
+attn_status attn_selftest_timeout(int timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_ATTN_H_ */

@@ -1,0 +1,171 @@
+"""GB300 fused attention forward: Python binding of libattn's C ABI.
+
+The compute lives in ``csrc/attn_fwd.cu`` (sm_103a: TMA, mbarriers, tcgen05
+MMAs accumulating in tensor memory); ``include/attn.h`` documents the ABI.
+This module only marshals arguments: it passes device pointers, sizes and the
+current CUDA stream to the shared library and turns status codes into
+exceptions.  There is no fallback: if ``libattn.so`` is missing or the device
+is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+INCLUDE_DIR = os.path.join(_ROOT, "include")
+SOURCES = [os.path.join(_CSRC, "attn_fwd.cu")]
+DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(INCLUDE_DIR, "attn.h")]
+
+NVCC_FLAGS = [
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-O3", "-lineinfo", "-std=c++17",
+    "-Xcompiler", "-fPIC", "-shared",
+]
+
+# status codes (include/attn.h)
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_ALIGNMENT = 2
+ATTN_ERR_UNSUPPORTED_DEVICE = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_BAD_SEQLENS = 6
+
+EXPORTED = ["attn_fwd", "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {attn_status_string(code)} ({code})")
+        self.code = code
+
+
+def nvcc_path() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libattn.so in-tree for sm_103a (skipped when up to date)."""
+    if (not force and os.path.exists(LIB_PATH)
+            and os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(p) for p in DEPENDS)):
+        return LIB_PATH
+    tmp = LIB_PATH + ".tmp"
+    cmd = [nvcc_path(), *NVCC_FLAGS, "-o", tmp, *SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libattn.so is not built ({LIB_PATH}); run tensor_program_compilers_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd.restype = i
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, vp]
+        lib.attn_get_status.restype = i
+        lib.attn_get_status.argtypes = [vp]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_selftest_timeout.restype = i
+        lib.attn_selftest_timeout.argtypes = [i, vp]
+        _lib = lib
+    return _lib
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _load()
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_status_string(code: int) -> str:
+    return _load().attn_status_string(int(code)).decode()
+
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
+             stream=None, check=True) -> int:
+    """Call the C ``attn_fwd`` with device tensors (or raw device pointers).
+
+    Layouts and argument meaning are those of ``include/attn.h``.  Returns
+    the status code; with ``check`` a non-OK code raises AttnError.
+    """
+    rc = _load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                          int(Hkv), int(N), int(d), float(scale), int(bool(causal)),
+                          _ptr(cu_seqlens), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return rc
+
+
+def attn_get_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device status word."""
+    return _load().attn_get_status(_stream(stream))
+
+
+def attn_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
+    return _load().attn_selftest_timeout(int(timeout_us), _stream(stream))
+
+
+def attention(q, k, v, causal: bool, scale: Optional[float] = None, cu_seqlens=None,
+              out=None, lse=None, stream=None):
+    """Allocate outputs (torch, on q's device) and run ``attn_fwd``.
+
+    Fixed batch: q [B, N, Hq, d], k/v [B, N, Hkv, d] -> o like q, lse [B, Hq, N].
+    Packed: q [T, Hq, d], k/v [T, Hkv, d], cu_seqlens int32 [B+1] on the
+    device -> o like q, lse [Hq, T].
+    """
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    if cu_seqlens is None:
+        B, N, Hq, _ = q.shape
+        Hkv = k.shape[2]
+        lse_shape = (B, Hq, N)
+        n_arg = N
+    else:
+        T, Hq, _ = q.shape
+        Hkv = k.shape[1]
+        B = cu_seqlens.numel() - 1
+        lse_shape = (Hq, T)
+        n_arg = T
+    for t in (q, k, v):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, n_arg, d, scale, causal, cu_seqlens, stream)
+    return out, lse

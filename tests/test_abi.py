@@ -1,0 +1,81 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad host-side arguments before touching the GPU (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+import tensor_program_compilers_gb300 as pkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return pkg.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert names == sorted(pkg.EXPORTED), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (2, "ATTN_ERR_ALIGNMENT"),
+                       (3, "ATTN_ERR_UNSUPPORTED_DEVICE"), (4, "ATTN_ERR_CUDA"),
+                       (5, "ATTN_ERR_TIMEOUT"), (6, "ATTN_ERR_BAD_SEQLENS")]:
+        assert pkg.attn_status_string(code) == name
+    assert pkg.attn_status_string(99) == "ATTN_UNKNOWN_STATUS"
+
+
+def call(**kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=2, Hq=8, Hkv=2, N=256,
+                d=128, scale=0.088, causal=1, cu_seqlens=None, stream=0)
+    args.update(kw)
+    return pkg.attn_fwd(check=False, **args)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(d=96), dict(d=32), dict(d=512), dict(Hq=6, Hkv=4), dict(Hkv=0), dict(Hq=0),
+    dict(B=-1), dict(N=-5), dict(scale=0.0), dict(scale=-1.0), dict(scale=float("inf")),
+    dict(scale=float("nan")), dict(q=None), dict(lse=None), dict(o=None),
+    dict(N=1 << 30, B=4),          # more than 2^31 token rows
+])
+def test_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert call(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(q=0x1008), dict(k=0x2004), dict(v=0x3002),
+                                dict(o=0x4001), dict(lse=0x5002)])
+def test_misaligned_pointers_rejected(lib, kw):
+    assert call(**kw) == pkg.ATTN_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(N=0), dict(B=0, q=None, o=None)])
+def test_empty_problem_is_a_no_op(lib, kw):
+    assert call(**kw) == pkg.ATTN_OK
+
+
+def test_selftest_rejects_bad_limit(lib):
+    assert pkg.attn_selftest_timeout(0, stream=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert pkg.attn_selftest_timeout(2_000_000, stream=0) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(pkg, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        pkg.library()
