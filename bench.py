@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Attention-forward benchmark on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference]
+
+A step is one ``attn_fwd`` call (the whole fused forward: tile schedule,
+TMA loads, QK^T, masking, online softmax, rescale, PV, epilogue) over one
+batch of the workload's synthetic inputs, resident in HBM.  The metric is
+TFLOP/s under the convention 4*H*L^2*d per sequence, halved when causal.
+L2 is flushed (256 MB write) before every timed step; each step is timed
+with CUDA events on the launching stream.
+
+Default workload: the ragged packed batch (16 sequences, L ~ U[256, 8192],
+Hq 32, Hkv 8, d 128, causal, Q x4), the largest of the five workloads.  The
+other four are timed briefly and reported under "per_workload".
+
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+collective on the data path); value = FLOPs of all ranks / max rank time.
+
+--impl reference runs the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores; rank 0
+only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16) at 1 GB300; fraction of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK = 1900.0       # TFLOP/s, used only when MEASURED_PEAKS.json is absent
+FLUSH_BYTES = 256 << 20      # > 129 MB L2
+
+
+# ------------------------------------------------------------------ distributed
+def world() -> tuple:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, ws, _ = world()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, ws
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a float over ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_rate(units_all_ranks: float, max_seconds: float) -> float:
+    return units_all_ranks / max_seconds
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_program_compilers_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload_key)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        sm, mx, pw, reasons = [], [], [], set()
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ native arm
+def run_workload(pkg, W, wl, seed, steps, warmup, dev, flush, sample_clocks=False):
+    import torch
+    inp = W.make_inputs(wl, seed)
+    q, k, v = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    o = torch.empty_like(q)
+    lse_shape = (wl.Hq, inp.n_arg) if wl.varlen else (wl.B, wl.Hq, wl.N)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    flops = W.causal_flops(wl, inp.lens)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.attn_fwd(q, k, v, o, lse, wl.B, wl.Hq, wl.Hkv, inp.n_arg, wl.d, wl.scale,
+                     wl.causal, cu, stream=stream.cuda_stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"device status after warm-up: {pkg.attn_status_string(st)}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if sample_clocks else None
+    barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.__enter__()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {pkg.attn_status_string(st)}")
+    per_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return dict(inp=inp, flops=flops, per_ms=per_ms, total_ms=sum(per_ms), wall_s=wall,
+                clocks=sampler.summary() if sampler else None,
+                tensors=(q, k, v, o, lse, cu), step=step)
+
+
+def run_e2e(pkg, W, wl, inp, dev, steps):
+    """Same metric through the public C ABI with host buffers: every step
+    copies Q, K, V from pinned host memory, runs attn_fwd and reads O and LSE
+    back to pinned host memory."""
+    import torch
+    qh, kh, vh = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+    q, k, v = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    o = torch.empty_like(q)
+    lse_shape = (wl.Hq, inp.n_arg) if wl.varlen else (wl.B, wl.Hq, wl.N)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        pkg.attn_fwd(q, k, v, o, lse, wl.B, wl.Hq, wl.Hkv, inp.n_arg, wl.d, wl.scale,
+                     wl.causal, cu, stream=stream.cuda_stream)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    flops = W.causal_flops(wl, inp.lens)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return dict(ms=ms, steps=steps, flops=flops, h2d=h2d, d2h=d2h)
+
+
+def cpu_baseline(W, wl, inp, target_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded seeded row sample of the
+    same workload, timed on this host's cores."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+
+    def rows_flops(rows):
+        # 4*d per (query row, visible key) pair: the same convention as the GPU metric
+        n = 0
+        for (s, h, i) in rows:
+            L = inp.lens[s]
+            n += (i + 1) if wl.causal else L
+        return 4.0 * wl.d * n
+
+    def timed(rows):
+        t0 = time.perf_counter()
+        oracle.attn_fwd_oracle(inp.q, inp.k, inp.v, wl.B, wl.Hq, wl.Hkv, inp.n_arg, wl.d,
+                               wl.scale, wl.causal, cu_seqlens=cu, rows=rows, nthreads=cores)
+        return time.perf_counter() - t0
+
+    probe = W.sample_rows(wl, inp.lens, 4)
+    t = max(timed(probe), 1e-3)
+    per_head = max(4, min(int(4 * target_s / t), max(inp.lens) * len(inp.lens)))
+    rows = W.sample_rows(wl, inp.lens, per_head)
+    t = timed(rows)
+    f = rows_flops(rows)
+    return {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{per_head} seeded query rows per head x {wl.Hq} heads "
+                      f"({len(rows)} rows, {f:.3e} FLOPs) of workload '{wl.name}', fp64, "
+                      f"{t:.1f} s"}
+
+
+def native(args):
+    import torch
+    import tensor_program_compilers_gb300 as pkg
+    from tensor_program_compilers_gb300 import workloads as W
+
+    rank, ws, local = world()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl")
+    pkg.build()
+    wl = W.BY_KEY[args.workload]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    res = run_workload(pkg, W, wl, wl.seed + rank, args.steps, args.warmup, dev, flush,
+                       sample_clocks=(rank == 0))
+    max_s = reduce_max(res["total_ms"] / 1e3, dev)
+    flops_all = reduce_sum(res["flops"] * args.steps, dev)
+    value = whole_job_rate(flops_all, max_s) / 1e12
+    ms_per_step = max_s * 1e3 / args.steps
+
+    peaks = measured_peaks()
+    if "bf16_tflops" in peaks:
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured burst bf16 (MEASURED_PEAKS.json)"
+    else:
+        peak, peak_src = FALLBACK_PEAK, "fallback"
+    avg_launch_s = res["total_ms"] / 1e3 / args.steps
+    achieved = res["flops"] / avg_launch_s / 1e12
+    traffic = recorded_traffic(args.workload)
+
+    e2e = None
+    if not args.no_e2e:
+        r = run_e2e(pkg, W, wl, res["inp"], dev, args.e2e_steps)
+        e_max = reduce_max(r["ms"] / 1e3, dev)
+        e_flops = reduce_sum(r["flops"] * r["steps"], dev)
+        e2e = {"value": whole_job_rate(e_flops, e_max) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+               "steps": r["steps"], "ms_per_step": e_max * 1e3 / r["steps"]}
+
+    per_workload = {}
+    if not args.no_per_workload:
+        for key, other in W.BY_KEY.items():
+            if key == args.workload:
+                continue
+            rr = run_workload(pkg, W, other, other.seed + rank, min(args.steps, 20), 3, dev, flush)
+            ms = rr["total_ms"] / len(rr["per_ms"])
+            tf = rr["flops"] / (ms / 1e3) / 1e12
+            per_workload[key] = {"workload": other.name, "tflops": round(tf, 2),
+                                 "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peak, 4)}
+            del rr
+
+    base = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(W, wl, res["inp"], args.cpu_seconds)
+
+    if rank == 0:
+        inp = res["inp"]
+        out = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                       "d": wl.d, "causal": wl.causal, "tokens": inp.total_rows,
+                       "seq_lens": inp.lens if wl.varlen else wl.N,
+                       "flops_per_step": res["flops"],
+                       "l2": "flushed before every timed step (256 MB write)",
+                       "parallelism": f"{ws} replica(s), each rank its own batch"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "peak_source": peak_src, "unit": UNIT,
+                         "frac": round(achieved / peak, 4), "traffic": traffic},
+            "cpu_baseline": base, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": res["clocks"],
+            "kernel_ms": {"min": round(min(res["per_ms"]), 5),
+                          "median": round(statistics.median(res["per_ms"]), 5)},
+            "per_workload": per_workload,
+        }
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm
+def reference(args):
+    rank, ws, _ = world()
+    if rank != 0:
+        return            # rank 0 alone runs the CPU reference
+    import oracle
+    from tensor_program_compilers_gb300 import workloads as W
+    oracle.build()
+    wl = W.BY_KEY[args.workload]
+    inp = W.make_inputs(wl, wl.seed)
+    cores = len(os.sched_getaffinity(0))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+    per_head = args.ref_rows_per_head
+    rows = W.sample_rows(wl, inp.lens, per_head)
+    f = 4.0 * wl.d * sum(((i + 1) if wl.causal else inp.lens[s]) for (s, h, i) in rows)
+
+    def step():
+        oracle.attn_fwd_oracle(inp.q, inp.k, inp.v, wl.B, wl.Hq, wl.Hkv, inp.n_arg, wl.d,
+                               wl.scale, wl.causal, cu_seqlens=cu, rows=rows, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    value = f * args.steps / t / 1e12
+    sample = (f"{per_head} seeded query rows per head x {wl.Hq} heads ({len(rows)} rows, "
+              f"{f:.3e} FLOPs per step) of workload '{wl.name}', fp64")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": t * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                      "causal": wl.causal, "tokens": inp.total_rows},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=["ragged", "gqa", "d256", "block", "tiny"],
+                    default="ragged")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows-per-head", type=int, default=24)
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -167,13 +167,19 @@ def test_packed_bad_offsets_reported_and_outputs_untouched():
 
 # ----------------------------------------------------------------- invariants
 def test_constant_v_gives_constant_o():
+    """Weights sum to one, so V = c gives O = c.  P enters the P.V product
+    rounded to bf16 (relative error <= 2^-9 per weight) while l sums the
+    unrounded weights, and O is rounded to bf16 at the end: every output
+    is c or one of its bf16 neighbours (ulp 2^-8 at 0.75)."""
     B, N, Hq, d = 2, 700, 4, 128
     q = rand((B, N, Hq, d), 61, 3.0)
     k = rand((B, N, Hq, d), 62)
     v = torch.full((B, N, Hq, d), 0.75, dtype=torch.bfloat16)
     for causal in (False, True):
         o, lse = Run(q, k, v, B, Hq, Hq, N, d, d ** -0.5, causal)()
-        assert np.abs(o - 0.75).max() <= 2e-3
+        err = np.abs(o - 0.75)
+        assert err.max() <= 2.0 ** -8
+        assert err.mean() <= 2e-4
 
 
 def test_zero_q_closed_form():
