@@ -34,7 +34,7 @@ def build(force: bool = False) -> str:
             "gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
             "-o", _LIB, _SRC, "-lm",
         ]
-        subprocess.run(cmd, check=True)
+        subprocess.run(cmd, check=True, timeout=300)
     return _LIB
 
 

@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cmd = [nvcc_path(), *NVCC_FLAGS, "-o", tmp, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    subprocess.run(cmd, check=True, timeout=900)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -1,12 +1,13 @@
 // attn_fwd.cu -- fused attention forward for sm_103a (GB300) and its C ABI.
 //
-// One CTA computes one 128-row query tile of one (sequence, query head):
+// A CTA owns one 128-row query tile of one (sequence, query head) and walks
+// the key tiles of that sequence:
 //
 //   for each 128-key tile j (causal: only j <= the diagonal tile)
 //     S    = Q K_j^T                       tcgen05.mma, bf16 -> fp32 in TMEM
 //     m'   = max(m, rowmax S)              online-softmax monoid state (m, l)
 //     P    = 2^(S*c - m'*c), c = scale*log2(e), rounded to bf16 into TMEM
-//     l    = l * 2^((m - m')*c) + rowsum P
+//     l    = l * 2^((m - m')*c) + rowsum P      (of the rounded P)
 //     O    = O * 2^((m - m')*c) + P V_j    tcgen05.mma, P read from TMEM
 //   O / l -> bf16, LSE = m*scale + ln(l)
 //
@@ -16,22 +17,26 @@
 // explainer's loop (ai.thesatyajit.com/articles/tilelang, "FlashAttention,
 // in tiles").  Two liberties, both exact in real arithmetic:
 //  * the running max m is only moved when the tile max exceeds it by more
-//    than 8 (base-2 units): softmax is shift invariant (tang, section 6), so
+//    than 16 (base-2 units): softmax is shift invariant (tang, section 6), so
 //    any reference value works as long as O and l share it and the
-//    exponentials stay in range (they are <= 2^8 here);
+//    exponentials stay in range (they are <= 2^16 here);
 //  * masked keys read -inf, the identity of max (tang, section 2.1, guarded
 //    views), so fully masked tiles are skipped rather than computed.
 //
 // Warp roles (192 threads):
-//   warp 0     TMA producer: Q tile once, then K_0, K_1, V_0, K_2, V_1, ...
-//              into a ring of shared-memory slots (128-byte swizzle)
+//   warp 0     TMA producer: Q once, then K_0, K_1, V_0, K_2, V_1, ... into a
+//              ring of shared-memory slots (128-byte swizzle)
 //   warp 1     TMEM allocator and MMA issuer (one thread)
 //   warps 2-5  softmax warpgroup: thread t owns query row t (TMEM lane t)
 //
-// Tensor memory (512 columns x 128 lanes x 32 bit):
-//   [0,128)   S  (fp32 scores of the current tile)
-//   [128,192) P0 and [192,256) P1  (bf16 probabilities, two per column)
-//   [256,256+d) O (fp32 accumulator)
+// Tensor memory (512 columns x 128 lanes x 32 bit), SB = 2 score buffers for
+// d <= 128 and 1 for d = 256 (whose accumulator needs 256 columns):
+//   S_b   [128 b, 128 b + 128)      fp32 scores, b < SB
+//   P_b   [128 SB + 64 b, +64)      bf16 probabilities (two per column), b < 2
+//   O     [128 SB + 128, +d)        fp32 accumulator
+// The MMA issue order is QK_0, QK_1, PV_0, QK_2, PV_1, ...: the scores of the
+// next key tile are computed while the softmax warps work on this one.  With
+// two score buffers QK_{j+1} waits only for the softmax to have read S_{j-1}.
 //
 // Every pipeline wait is bounded: past a time limit it records
 // ATTN_ERR_TIMEOUT in a device status word and every role stops issuing,
@@ -52,42 +57,45 @@
 
 namespace attn {
 
-constexpr int BM = 128;            // query rows per tile
+constexpr int BM = 128;            // query rows per tile (one per TMEM lane)
 constexpr int BN = 128;            // keys per tile
-constexpr int NUM_THREADS = 192;
+constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0;
-constexpr uint32_t COL_P0 = 128;   // P buffer b at COL_P0 + 64*b
-constexpr uint32_t COL_O = 256;
-constexpr uint32_t CHUNK_BYTES = 128 * 128;   // 128 rows x 64 bf16
-constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units
+constexpr uint32_t CHUNK_BYTES = 128 * 128;   // 128 rows x 64 bf16, one swizzle column
+constexpr float RESCALE_THRESHOLD = 16.0f;    // log2 units: P <= 2^16 between moves
 
 template <int D>
 struct Cfg {
   static constexpr int CHUNKS = D / 64;
   static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;   // one Q, K or V tile
-  static constexpr int STAGES = D == 64 ? 8 : (D == 128 ? 5 : 2);
+  static constexpr int SB = D <= 128 ? 2 : 1;                     // score buffers
+  static constexpr int STAGES = D == 64 ? 10 : (D == 128 ? 6 : 2);  // K/V ring slots
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = TILE_BYTES;
   static constexpr uint32_t OFF_CTL = TILE_BYTES * (1 + STAGES);
-  static constexpr uint32_t CTL_BYTES = 512;
-  static constexpr uint32_t SMEM_BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment slack
+  static constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;   // control block + alignment
+  static constexpr uint32_t COL_P0 = 128 * SB;
+  static constexpr uint32_t COL_O = COL_P0 + 128;
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * (uint32_t)b; }
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
 };
 
-// Barrier slots in the control block.
+// Barrier slots of the control block, then the K/V ring (full[0..STAGES),
+// empty[0..STAGES)).
 enum : int {
   BAR_Q_FULL = 0,
-  BAR_S_FULL,
-  BAR_S_FREE,
-  BAR_P_FULL0,
+  BAR_S_FULL0,     // S_b written (MMA commit), b = 0, 1
+  BAR_S_FULL1,
+  BAR_S_FREE0,     // S_b read into registers (softmax warps)
+  BAR_S_FREE1,
+  BAR_P_FULL0,     // P_b written (softmax warps)
   BAR_P_FULL1,
-  BAR_PV_DONE0,
+  BAR_PV_DONE0,    // the PV reading P_b completed (MMA commit)
   BAR_PV_DONE1,
   BAR_DRAIN,
-  BAR_RING   // full[0..STAGES), then empty[0..STAGES)
+  BAR_RING
 };
 
 struct Params {
@@ -96,7 +104,8 @@ struct Params {
   const int *cu_seqlens;
   int B, Hq, Hkv, N, group;
   int causal;
-  int num_qt;           // fixed batch: ceil(N / BM)
+  int unit_rows;        // query rows per CTA work unit (one tile)
+  int num_units;        // fixed batch: ceil(N / unit_rows)
   float scale;          // score multiplier
   float scale_log2;     // scale * log2(e)
   unsigned long long timeout_ns;
@@ -106,12 +115,14 @@ __device__ int g_status;   // first device-side error since the last read
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_status, 0, code); }
 
-// Bounded wait on a barrier phase.  Returns false if the CTA is aborting or
-// the time limit passed (then it starts the abort).
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                          volatile uint32_t *abort_flag,
-                                          unsigned long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// ---------------------------------------------------------------- bounded waits
+// Bounded wait on a barrier phase, slow path (kept out of line: a call costs
+// a couple of hundred cycles, so the common already-complete case is tested
+// inline by wait_bounded below).  Returns false if the CTA is aborting or the
+// time limit passed (then it starts the abort).
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity,
+                                       volatile uint32_t *abort_flag,
+                                       unsigned long long timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -124,6 +135,12 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t *abort_flag,
+                                             unsigned long long timeout_ns) {
+  return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, timeout_ns);
 }
 
 // Warp-uniform bounded wait for the softmax warps: the tcgen05.ld/st that
@@ -145,57 +162,83 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- tile schedule
 struct Tile {
   int valid;
   int seq_start;   // token row of the sequence's first token
   int len;         // sequence length
-  int qt;          // query tile index within the sequence
+  int unit;        // work-unit index within the sequence (unit_rows query rows)
   int h;           // query head
   long long lse_base;   // LSE index of the sequence's row 0 for head h
 };
 
-// Packed batches: number of 128-row tiles of sequence s.
-__device__ __forceinline__ int seq_tiles(const int *cu, int s) {
+// Packed batches: number of work units of sequence s.
+__device__ __forceinline__ int seq_units(const int *cu, int s, int unit_rows) {
   int a = __ldg(cu + s), b = __ldg(cu + s + 1);
-  return b > a ? (b - a + BM - 1) / BM : 0;
+  return b > a ? (b - a + unit_rows - 1) / unit_rows : 0;
 }
 
-// Number of (sequence, query tile) pairs whose tile index is >= x.
-__device__ int pairs_at_or_above(const int *cu, int B, int x) {
+// Per-lane cache of the unit counts of sequences lane, lane+32, ... (up to
+// SEQ_CACHE per lane); larger batches read cu_seqlens again each time.
+constexpr int SEQ_CACHE = 4;
+
+struct SeqUnits {
+  int n[SEQ_CACHE];
+  bool cached;
+};
+
+// Number of (sequence, unit) pairs whose unit index is >= x (warp-wide).
+__device__ int units_at_or_above(const SeqUnits &su, const int *cu, int B, int x,
+                                 int unit_rows) {
   int c = 0;
-  for (int s = threadIdx.x & 31; s < B; s += 32) c += max(0, seq_tiles(cu, s) - x);
+  if (su.cached) {
+#pragma unroll
+    for (int i = 0; i < SEQ_CACHE; ++i) c += max(0, su.n[i] - x);
+  } else {
+    for (int s = threadIdx.x & 31; s < B; s += 32) c += max(0, seq_units(cu, s, unit_rows) - x);
+  }
   for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   return c;
 }
 
-// Map this CTA to its tile (all 32 lanes of one warp).  Tiles are ordered
-// longest first -- descending query-tile index, the number of causal key
-// tiles -- with heads fastest so that the query heads of one key/value head
-// run side by side.
+// Map this CTA to its work unit (all 32 lanes of one warp).  Units are
+// ordered longest first -- descending unit index, i.e. descending number of
+// causal key tiles -- with heads fastest so that the query heads of one
+// key/value head run side by side.
 __device__ Tile decode_tile(const Params &p) {
   Tile t{};
   const int lane = threadIdx.x & 31;
   const long long idx = blockIdx.x;
+  const int U = p.unit_rows;
   if (p.cu_seqlens == nullptr) {
     const long long per = (long long)p.B * p.Hq;
     const int lvl = (int)(idx / per);
     const int rem = (int)(idx % per);
     const int b = rem / p.Hq;
     t.h = rem % p.Hq;
-    t.qt = p.num_qt - 1 - lvl;
+    t.unit = p.num_units - 1 - lvl;
     t.seq_start = b * p.N;
     t.len = p.N;
     t.lse_base = ((long long)b * p.Hq + t.h) * p.N;
-    t.valid = t.qt >= 0;
+    t.valid = t.unit >= 0;
     return t;
   }
   const int *cu = p.cu_seqlens;
-  // validate the offsets and find the total and largest tile counts
+  // validate the offsets and find the total and largest unit counts
+  SeqUnits su;
+  su.cached = p.B <= 32 * SEQ_CACHE;
+#pragma unroll
+  for (int i = 0; i < SEQ_CACHE; ++i) su.n[i] = 0;
   int bad = 0, nmax = 0, ntot = 0;
-  for (int s = lane; s < p.B; s += 32) {
+  for (int s = lane, i = 0; s < p.B; s += 32, ++i) {
     int a = __ldg(cu + s), b = __ldg(cu + s + 1);
     bad |= (b < a);
-    int n = b > a ? (b - a + BM - 1) / BM : 0;
+    int n = b > a ? (b - a + U - 1) / U : 0;
+    if (su.cached) {
+#pragma unroll
+      for (int k = 0; k < SEQ_CACHE; ++k)
+        if (k == i) su.n[k] = n;
+    }
     nmax = max(nmax, n);
     ntot += n;
   }
@@ -210,24 +253,32 @@ __device__ Tile decode_tile(const Params &p) {
     t.valid = 0;
     return t;
   }
-  const int u = (int)(idx / p.Hq);   // pair index
+  const int u = (int)(idx / p.Hq);   // (sequence, unit) pair index
   t.h = (int)(idx % p.Hq);
   if (u >= ntot) {
     t.valid = 0;
     return t;
   }
-  // largest x with pairs_at_or_above(x) > u: pair u sits at tile level x
+  // largest x with units_at_or_above(x) > u: pair u sits at unit level x
   int lo = 0, hi = nmax;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
-    if (pairs_at_or_above(cu, p.B, mid) > u) lo = mid; else hi = mid;
+    if (units_at_or_above(su, cu, p.B, mid, U) > u) lo = mid; else hi = mid;
   }
   const int x = lo;
-  int r = u - pairs_at_or_above(cu, p.B, x + 1);   // rank among sequences with > x tiles
+  int r = u - units_at_or_above(su, cu, p.B, x + 1, U);   // rank among sequences with > x units
   int seq = -1;
-  for (int base = 0; base < p.B; base += 32) {
+  for (int base = 0, i = 0; base < p.B; base += 32, ++i) {
     const int s = base + lane;
-    const bool has = s < p.B && seq_tiles(cu, s) > x;
+    int n = 0;
+    if (su.cached) {
+#pragma unroll
+      for (int k = 0; k < SEQ_CACHE; ++k)
+        if (k == i) n = su.n[k];
+    } else if (s < p.B) {
+      n = seq_units(cu, s, U);
+    }
+    const bool has = s < p.B && n > x;
     const unsigned m = __ballot_sync(0xffffffffu, has);
     const int cnt = __popc(m);
     if (r < cnt) {
@@ -242,95 +293,365 @@ __device__ Tile decode_tile(const Params &p) {
   }
   t.seq_start = __ldg(cu + seq);
   t.len = __ldg(cu + seq + 1) - t.seq_start;
-  t.qt = x;
+  t.unit = x;
   t.lse_base = (long long)t.h * p.N + t.seq_start;
   t.valid = 1;
   return t;
 }
 
+// Warp 0 decodes, lane 0 publishes the tile in the control block.
+__device__ __forceinline__ void publish_tile(const Params &p, int *info) {
+  Tile t = decode_tile(p);
+  if ((threadIdx.x & 31) == 0) {
+    info[0] = t.valid;
+    info[1] = t.seq_start;
+    info[2] = t.len;
+    info[3] = t.unit;
+    info[4] = t.h;
+    *reinterpret_cast<long long *>(info + 6) = t.lse_base;
+  }
+}
+
+// ---------------------------------------------------------------- softmax pieces
+// This thread's 128 fp32 scores (TMEM columns col..col+127 of its lane).
+__device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[BN]) {
+  uint32_t a[32], b[32], c[32], d[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld32(taddr + 64, c);
+  tmem_ld32(taddr + 96, d);
+  tmem_wait_ld();
+  reg_fence32(a);
+  reg_fence32(b);
+  reg_fence32(c);
+  reg_fence32(d);
+#pragma unroll
+  for (int x = 0; x < 32; ++x) {
+    s[x] = __uint_as_float(a[x]);
+    s[32 + x] = __uint_as_float(b[x]);
+    s[64 + x] = __uint_as_float(c[x]);
+    s[96 + x] = __uint_as_float(d[x]);
+  }
+}
+
+// Keys kv0 + x >= lim are invisible: they read -inf, the identity of max.
+__device__ __forceinline__ void mask_scores(float (&s)[BN], int kv0, int lim) {
+#pragma unroll
+  for (int x = 0; x < BN; ++x)
+    if (kv0 + x >= lim) s[x] = -INFINITY;
+}
+
+// Row maximum as eight independent chains of 3-input max (short dependency
+// chains: one warp per sub-partition has to hide the latency itself).
+__device__ __forceinline__ float row_max(const float (&s)[BN]) {
+  float mk[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float m = max3f(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+    for (int i = 3; i + 1 < 16; i += 2) m = max3f(m, s[k + 8 * i], s[k + 8 * (i + 1)]);
+    mk[k] = fmaxf(m, s[k + 8 * 15]);
+  }
+  return fmaxf(max3f(mk[0], mk[1], mk[2]), max3f(mk[3], mk[4], max3f(mk[5], mk[6], mk[7])));
+}
+
+// Online-softmax state of one row: reference max (raw score units), the
+// running sum of 2^((s - m) * c) (for the LSE) and the running sum of the
+// same weights rounded to bf16 as the P.V product uses them (for O / l: a
+// row dominated by one key then returns that key's value exactly).
+struct RowState {
+  float m;
+  float l;
+  float lr;
+};
+
+// Folds a tile maximum into the state.  Returns the factor the row's O
+// accumulator must be multiplied by (1 when the reference max stays).
+__device__ __forceinline__ float fold_max(RowState &st, float tile_max, float c, bool &moved) {
+  const float m_new = fmaxf(st.m, tile_max);
+  moved = (st.m == -INFINITY) ? (m_new != -INFINITY)
+                              : ((m_new - st.m) * c > RESCALE_THRESHOLD);
+  float alpha = 1.f;
+  if (moved) {
+    alpha = (st.m == -INFINITY) ? 0.f : ex2_approx((st.m - m_new) * c);
+    st.m = m_new;
+    st.l *= alpha;
+    st.lr *= alpha;
+  }
+  return alpha;
+}
+
+// p = 2^(s*c - m*c) for 64 scores s[BASE..BASE+63]: bf16 pairs into pk,
+// fp32 sums into acc (four packed accumulators).
+template <int BASE>
+__device__ __forceinline__ void exp_chunk(const float (&s)[BN], uint64_t c2, uint64_t nm2,
+                                          uint32_t (&pk)[32], uint64_t (&acc)[4],
+                                          uint64_t (&accr)[4]) {
+#pragma unroll
+  for (int x = 0; x < 64; x += 2) {
+    const uint64_t a = f2_fma(f2_pack(s[BASE + x], s[BASE + x + 1]), c2, nm2);
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+    const uint32_t w = pack_bf16x2(e0, e1);
+    pk[x >> 1] = w;
+    acc[(x >> 1) & 3] = f2_add(acc[(x >> 1) & 3], f2_pack(e0, e1));
+    // the rounded values too: the P.V product sees exactly these weights
+    accr[(x >> 1) & 3] = f2_add(accr[(x >> 1) & 3], bf16x2_widen(w));
+  }
+}
+
+// exp_chunk that also tracks the running maximum of the raw scores (four
+// partial maxima, combined by the caller).
+template <int BASE>
+__device__ __forceinline__ void exp_chunk_track(const float (&s)[BN], uint64_t c2, uint64_t nm2,
+                                                uint32_t (&pk)[32], uint64_t (&acc)[4],
+                                                uint64_t (&accr)[4], float (&mx)[4]) {
+#pragma unroll
+  for (int x = 0; x < 64; x += 2) {
+    const uint64_t a = f2_fma(f2_pack(s[BASE + x], s[BASE + x + 1]), c2, nm2);
+    float a0, a1;
+    f2_unpack(a, a0, a1);
+    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+    const uint32_t w = pack_bf16x2(e0, e1);
+    pk[x >> 1] = w;
+    acc[(x >> 1) & 3] = f2_add(acc[(x >> 1) & 3], f2_pack(e0, e1));
+    accr[(x >> 1) & 3] = f2_add(accr[(x >> 1) & 3], bf16x2_widen(w));
+    mx[(x >> 1) & 3] = max3f(mx[(x >> 1) & 3], s[BASE + x], s[BASE + x + 1]);
+  }
+}
+
+__device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]);
+
+// One key tile of this thread's row (warp-collective: TMEM stores).  Writes
+// P = 2^(s*c - m*c) as bf16 pairs to TMEM columns p_addr .. p_addr+63,
+// folds the tile into the row state and returns the factor the row's O must
+// be multiplied by (1 unless the reference max moved; `moved` says which).
+//
+// Once a row has a reference max, the exponentials are taken against it in
+// the same pass that finds the tile maximum; the tile is redone with a new
+// reference only when its maximum passes the old one by more than the
+// threshold (for some lane of the warp).  Rows without a reference (the first
+// tile) take the maximum first.  Either way the stored P and the sum share one
+// reference, which is all that shift invariance requires.
+__device__ __forceinline__ float softmax_tile(const float (&s)[BN], RowState &st, float c,
+                                              uint32_t p_addr, bool &moved) {
+  const uint64_t c2 = f2_pack(c, c);
+  uint64_t acc[4] = {0, 0, 0, 0}, accr[4] = {0, 0, 0, 0};
+  uint32_t pk[32];
+  float alpha = 1.f;
+  moved = false;
+  const bool have_ref = __all_sync(0xffffffffu, st.m != -INFINITY);
+  bool redo = !have_ref;
+  if (have_ref) {
+    const float neg_mc = -st.m * c;
+    const uint64_t nm2 = f2_pack(neg_mc, neg_mc);
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    exp_chunk_track<0>(s, c2, nm2, pk, acc, accr, mx);
+    tmem_st32(p_addr, pk);
+    exp_chunk_track<64>(s, c2, nm2, pk, acc, accr, mx);
+    tmem_st32(p_addr + 32, pk);
+    alpha = fold_max(st, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), c, moved);
+    redo = __any_sync(0xffffffffu, moved);
+  } else {
+    alpha = fold_max(st, row_max(s), c, moved);
+  }
+  if (redo) {   // first tile, or the reference moved: P against the final reference
+    const float neg_mc = (st.m == -INFINITY) ? 0.f : -st.m * c;
+    const uint64_t nm2 = f2_pack(neg_mc, neg_mc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = accr[i] = 0;
+    exp_chunk<0>(s, c2, nm2, pk, acc, accr);
+    tmem_st32(p_addr, pk);
+    exp_chunk<64>(s, c2, nm2, pk, acc, accr);
+    tmem_st32(p_addr + 32, pk);
+  }
+  st.l += sum_acc(acc);
+  st.lr += sum_acc(accr);
+  return alpha;
+}
+
+__device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]) {
+  float a, b;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a, b);
+  return a + b;
+}
+
+// O row *= alpha (TMEM columns taddr .. taddr+D-1 of this lane).  The caller
+// issues tcgen05.wait::st before publishing.
 template <int D>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+#pragma unroll
+    for (int x = 0; x < 32; x += 2) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[x]), __uint_as_float(o[x + 1])), a2), lo, hi);
+      o[x] = __float_as_uint(lo);
+      o[x + 1] = __float_as_uint(hi);
+    }
+    tmem_st32(taddr + cc, o);
+  }
+}
+
+// Epilogue of one row: O / l -> bf16, 16-byte stores of the row (if live).
+template <int D>
+__device__ __forceinline__ void store_row(uint32_t taddr, float inv_l, __nv_bfloat16 *orow,
+                                          bool live) {
+  const uint64_t s2 = f2_pack(inv_l, inv_l);
+#pragma unroll 1
+  for (int cc = 0; cc < D; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+    uint32_t w[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1])), s2),
+                lo, hi);
+      w[x] = pack_bf16x2(lo, hi);
+    }
+    if (live) {
+      uint4 *dst = reinterpret_cast<uint4 *>(orow + cc);
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+        dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ float row_lse(const RowState &st, float scale) {
+  const float m_use = (st.m == -INFINITY) ? 0.f : st.m;
+  return st.l > 0.f ? m_use * scale + logf(st.l) : -INFINITY;
+}
+
+// One 128x128x(16*K_STEPS) QK^T into TMEM: A = Q tile, B = K tile, both
+// K-major in 64-column swizzle chunks.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_s, uint32_t k_s) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BN, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    // 16 head-dim columns per step = 32 bytes inside a 128-byte swizzle row;
+    // 64-column chunks are CHUNK_BYTES apart; 8-row groups 1024 bytes apart.
+    const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc_sw128(q_s + koff, 16, 1024), smem_desc_sw128(k_s + koff, 16, 1024),
+           IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V_j: A = P from TMEM (bf16 pairs), B = V tile with keys as K and
+// the head dim as N (N contiguous: 64-wide swizzle atoms CHUNK_BYTES apart,
+// 8-key groups 1024 bytes apart, 16 keys = 2048 bytes per step).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_s,
+                                         bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_s + kk * 2048, CHUNK_BYTES, 1024), IDESC,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ---------------------------------------------------------------- control block
+struct Ctl {
+  uint64_t *bars;
+  uint32_t *words;   // [0] TMEM base, [1] abort flag, [2..] tile info
+  __device__ uint32_t bar(int i) const { return smem_u32(bars + i); }
+};
+
+template <int STAGES>
+__device__ __forceinline__ void init_barriers(const Ctl &c) {
+  mbar_init(c.bar(BAR_Q_FULL), 1);
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(c.bar(BAR_S_FULL0 + b), 1);
+    mbar_init(c.bar(BAR_S_FREE0 + b), 4 * 32);
+    mbar_init(c.bar(BAR_P_FULL0 + b), 4 * 32);
+    mbar_init(c.bar(BAR_PV_DONE0 + b), 1);
+  }
+  mbar_init(c.bar(BAR_DRAIN), 1);
+  for (int s = 0; s < STAGES; ++s) {
+    mbar_init(c.bar(BAR_RING + s), 1);
+    mbar_init(c.bar(BAR_RING + STAGES + s), 1);
+  }
+  c.words[1] = 0u;
+  mbar_init_fence();
+}
+
+// Producer-side drain after an abort: wait for the copies already issued.
+template <int STAGES>
+__device__ void drain_loads(const Ctl &c, int issued, unsigned long long timeout_ns) {
+  wait_drain(c.bar(BAR_Q_FULL), 0, timeout_ns);
+  for (int s = 0; s < STAGES && s < issued; ++s) {
+    const int last = s + STAGES * ((issued - 1 - s) / STAGES);
+    wait_drain(c.bar(BAR_RING + s), (uint32_t)(last / STAGES) & 1u, timeout_ns);
+  }
+}
+
+// ================================================================ kernel
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D>;
+  constexpr int SB = C::SB;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_s = smem_u32(smem_raw);
-  uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t base_s = smem_u32(smem);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  Ctl ctl{reinterpret_cast<uint64_t *>(smem + C::OFF_CTL), nullptr};
+  ctl.words = reinterpret_cast<uint32_t *>(ctl.bars + BAR_RING + 2 * C::STAGES);
+  volatile uint32_t *abort_flag = ctl.words + 1;
+  int *info = reinterpret_cast<int *>(ctl.words + 2);
+  auto bar_full = [&](int s) { return ctl.bar(BAR_RING + s); };
+  auto bar_empty = [&](int s) { return ctl.bar(BAR_RING + C::STAGES + s); };
 
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_CTL);
-  uint32_t *ctl = reinterpret_cast<uint32_t *>(bars + BAR_RING + 2 * C::STAGES);
-  volatile uint32_t *abort_flag = ctl + 1;
-  int *tile_info = reinterpret_cast<int *>(ctl + 2);
-  auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
-  auto bar_full = [&](int s) -> uint32_t { return bar(BAR_RING + s); };
-  auto bar_empty = [&](int s) -> uint32_t { return bar(BAR_RING + C::STAGES + s); };
-
-  // ---- set-up: tile decode (warp 0), barriers (warp 1) ----
   if (warp == 0) {
-    Tile t = decode_tile(p);
+    publish_tile(p, info);
     if (lane == 0) {
-      tile_info[0] = t.valid;
-      tile_info[1] = t.seq_start;
-      tile_info[2] = t.len;
-      tile_info[3] = t.qt;
-      tile_info[4] = t.h;
-      *reinterpret_cast<long long *>(tile_info + 6) = t.lse_base;
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
     }
   } else if (warp == 1 && lane == 0) {
-    mbar_init(bar(BAR_Q_FULL), 1);
-    mbar_init(bar(BAR_S_FULL), 1);
-    mbar_init(bar(BAR_S_FREE), 4 * 32);
-    mbar_init(bar(BAR_P_FULL0), 4 * 32);
-    mbar_init(bar(BAR_P_FULL1), 4 * 32);
-    mbar_init(bar(BAR_PV_DONE0), 1);
-    mbar_init(bar(BAR_PV_DONE1), 1);
-    mbar_init(bar(BAR_DRAIN), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
-    }
-    *abort_flag = 0u;
-    mbar_init_fence();
+    init_barriers<C::STAGES>(ctl);
   }
   __syncthreads();
-  if (!tile_info[0]) return;   // no tile for this CTA (uniform)
+  if (!info[0]) return;   // no tile for this CTA (uniform)
 
-  const int seq_start = tile_info[1];
-  const int len = tile_info[2];
-  const int qt = tile_info[3];
-  const int h = tile_info[4];
-  const long long lse_base = *reinterpret_cast<long long *>(tile_info + 6);
+  const int seq_start = info[1], len = info[2], qt = info[3], h = info[4];
+  const long long lse_base = *reinterpret_cast<long long *>(info + 6);
   const int kvh = h / p.group;
-  const int kv_tiles_total = (len + BN - 1) / BN;
-  const int n_kv = p.causal ? min(qt + 1, kv_tiles_total) : kv_tiles_total;
+  const int kv_tiles = (len + BN - 1) / BN;
+  const int n_kv = p.causal ? min(qt + 1, kv_tiles) : kv_tiles;
 
   if (warp == 1) {
-    tmem_alloc(smem_u32(ctl), TMEM_COLS);
+    tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl[0];
-
+  const uint32_t tmem = ctl.words[0];
   const uint32_t q_s = base_s + C::OFF_Q;
   const uint32_t kv_s = base_s + C::OFF_KV;
 
   if (warp == 0) {
-    // =========================== TMA producer ===========================
+    // ---------------- TMA producer: Q, then K0, K1, V0, K2, V1, ..., V_{n-1}
     if (lane == 0) {
-      const int row0 = seq_start + qt * BM;
-      mbar_arrive_expect_tx(bar(BAR_Q_FULL), C::TILE_BYTES);
+      mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), C::TILE_BYTES);
       for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(q_s + c * CHUNK_BYTES, &tm_q, bar(BAR_Q_FULL), c * 64, h, row0);
+        tma_load_3d(q_s + c * CHUNK_BYTES, &tm_q, ctl.bar(BAR_Q_FULL), c * 64, h,
+                    seq_start + qt * BM);
       int it = 0;
       bool ok = true;
       auto load = [&](const CUtensorMap *tm, int j) -> bool {
@@ -344,225 +665,111 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++it;
         return true;
       };
-      // consumption order of the MMA issuer: K0, K1, V0, K2, V1, ..., V_{n-1}
       for (int j = 0; ok && j < n_kv; ++j) {
         ok = load(&tm_k, j);
         if (ok && j >= 1) ok = load(&tm_v, j - 1);
       }
       if (ok) ok = load(&tm_v, n_kv - 1);
-      if (!ok) {
-        // drain: wait for the copies this thread issued
-        wait_drain(bar(BAR_Q_FULL), 0, p.timeout_ns);
-        for (int s = 0; s < C::STAGES && s < it; ++s) {
-          const int last = s + C::STAGES * ((it - 1 - s) / C::STAGES);
-          wait_drain(bar_full(s), (uint32_t)(last / C::STAGES) & 1u, p.timeout_ns);
-        }
-      }
+      if (!ok) drain_loads<C::STAGES>(ctl, it, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // =========================== MMA issuer =============================
+    // ---------------- MMA issuer: QK_0, QK_1, PV_0, QK_2, PV_1, ...
     if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BN, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
       int it = 0;
-      bool ok = wait_bounded(bar(BAR_Q_FULL), 0, abort_flag, p.timeout_ns);
+      bool ok = wait_bounded(ctl.bar(BAR_Q_FULL), 0, abort_flag, p.timeout_ns);
       auto pv = [&](int i) -> bool {
-        if (!wait_bounded(bar(BAR_P_FULL0 + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag,
+        if (!wait_bounded(ctl.bar(BAR_P_FULL0 + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag,
                           p.timeout_ns))
           return false;
         const int slot = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!wait_bounded(bar_full(slot), ph, abort_flag, p.timeout_ns)) return false;
+        if (!wait_bounded(bar_full(slot), (uint32_t)(it / C::STAGES) & 1u, abort_flag,
+                          p.timeout_ns))
+          return false;
         tc_fence_after();
-        const uint32_t v_s = kv_s + slot * C::TILE_BYTES;
-        const uint32_t p_t = tmem + COL_P0 + 64u * (uint32_t)(i & 1);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // V tile: keys are K (16 per step = 2048 bytes), d is N (64-wide
-          // swizzle atoms CHUNK_BYTES apart), 8-key groups 1024 bytes apart.
-          const uint64_t bdesc = smem_desc_sw128(v_s + kk * 2048, CHUNK_BYTES, 1024);
-          mma_ts(tmem + COL_O, p_t + kk * 8, bdesc, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(BAR_PV_DONE0 + (i & 1)));
+        issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)(i & 1),
+                    kv_s + slot * C::TILE_BYTES, i > 0);
+        tc_commit(ctl.bar(BAR_PV_DONE0 + (i & 1)));
         tc_commit(bar_empty(slot));
         ++it;
         return true;
       };
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j > 0) ok = wait_bounded(bar(BAR_S_FREE), (uint32_t)(j - 1) & 1u, abort_flag,
-                                     p.timeout_ns);
+        const int b = j % SB;
+        // S_b last held the scores of key tile j - SB: wait until they were read
+        if (j >= SB)
+          ok = wait_bounded(ctl.bar(BAR_S_FREE0 + b), (uint32_t)(j / SB - 1) & 1u, abort_flag,
+                            p.timeout_ns);
         if (!ok) break;
         const int slot = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        ok = wait_bounded(bar_full(slot), ph, abort_flag, p.timeout_ns);
+        ok = wait_bounded(bar_full(slot), (uint32_t)(it / C::STAGES) & 1u, abort_flag,
+                          p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t k_s = kv_s + slot * C::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // Q and K tiles: rows are M / N, head dim is K (16 per step = 32
-          // bytes inside a 128-byte swizzle row; 64-wide chunks apart).
-          const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-          const uint64_t adesc = smem_desc_sw128(q_s + koff, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(k_s + koff, 16, 1024);
-          mma_ss(tmem + COL_S, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(BAR_S_FULL));
+        issue_qk<D>(tmem + C::col_s(b), q_s, kv_s + slot * C::TILE_BYTES);
+        tc_commit(ctl.bar(BAR_S_FULL0 + b));
         tc_commit(bar_empty(slot));
         ++it;
         if (j > 0) ok = pv(j - 1);
       }
       if (ok) ok = pv(n_kv - 1);
-      // no MMA may be in flight when the tensor memory is released
-      tc_commit(bar(BAR_DRAIN));
-      wait_drain(bar(BAR_DRAIN), 0, p.timeout_ns);
+      tc_commit(ctl.bar(BAR_DRAIN));   // no MMA may be in flight at teardown
+      wait_drain(ctl.bar(BAR_DRAIN), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
-    // =========================== softmax warpgroup ======================
-    const int wq = warp & 3;                      // TMEM lane quarter of this warp
+    // ---------------- softmax warpgroup
+    const int wq = warp & 3;                        // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int q_idx = qt * BM + row;              // row within the sequence
+    const int q_idx = qt * BM + row;                // row within the sequence
     const float c = p.scale_log2;
-    float m_ref = -INFINITY;                      // running max, raw score units
-    float l = 0.f;                                // running sum (relative to m_ref)
+    RowState st{-INFINITY, 0.f, 0.f};
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = wait_warp(bar(BAR_S_FULL), (uint32_t)j & 1u, abort_flag, p.timeout_ns);
+      const int b = j % SB;
+      ok = wait_warp(ctl.bar(BAR_S_FULL0 + b), (uint32_t)(j / SB) & 1u, abort_flag, p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(tmem + lane_off + COL_S + 0, s0);
-      tmem_ld32(tmem + lane_off + COL_S + 32, s1);
-      tmem_ld32(tmem + lane_off + COL_S + 64, s2);
-      tmem_ld32(tmem + lane_off + COL_S + 96, s3);
-      tmem_wait_ld();
-      reg_fence32(s0);
-      reg_fence32(s1);
-      reg_fence32(s2);
-      reg_fence32(s3);
-      tc_fence_before();
-      mbar_arrive(bar(BAR_S_FREE));   // S may now be overwritten by the next QK^T
-
       float s[BN];
-#pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        s[x] = __uint_as_float(s0[x]);
-        s[32 + x] = __uint_as_float(s1[x]);
-        s[64 + x] = __uint_as_float(s2[x]);
-        s[96 + x] = __uint_as_float(s3[x]);
-      }
-      // masking: causal diagonal tile and the sequence tail only
+      load_scores(tmem + lane_off + C::col_s(b), s);
+      tc_fence_before();
+      mbar_arrive(ctl.bar(BAR_S_FREE0 + b));   // S_b may now take the scores of tile j + SB
       const int kv0 = j * BN;
-      const bool need_mask = (kv0 + BN > len) || (p.causal && kv0 + BN - 1 > qt * BM);
-      if (need_mask) {
-        const int lim = p.causal ? min(len, q_idx + 1) : len;   // keys < lim are visible
-#pragma unroll
-        for (int x = 0; x < BN; ++x)
-          if (kv0 + x >= lim) s[x] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int x = 1; x < BN; ++x) mx = fmaxf(mx, s[x]);
-      // move the reference max only when the tile max passes it by > threshold
-      const float m_new = fmaxf(m_ref, mx);
-      const bool rescale = (m_ref == -INFINITY) ? (m_new != -INFINITY)
-                                                : ((m_new - m_ref) * c > RESCALE_THRESHOLD);
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx((m_ref - m_new) * c);
-        m_ref = m_new;
-        l *= alpha;
-      }
-      const float neg_mc = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
-      uint32_t pk[BN / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int x = 0; x < BN; x += 2) {
-        const float e0 = ex2_approx(fmaf(s[x], c, neg_mc));
-        const float e1 = ex2_approx(fmaf(s[x + 1], c, neg_mc));
-        rs += e0 + e1;
-        pk[x / 2] = pack_bf16x2(e0, e1);
-      }
-      l += rs;
-
-      // P buffer j&1 was last read by PV_{j-2}
-      if (j >= 2) {
-        ok = wait_warp(bar(BAR_PV_DONE0 + (j & 1)), (uint32_t)((j - 2) >> 1) & 1u,
-                          abort_flag, p.timeout_ns);
-        if (!ok) break;
-      }
-      // rescale the O rows of this warp (after PV_{j-1} has landed)
-      if (__any_sync(0xffffffffu, rescale && j > 0)) {
-        ok = wait_warp(bar(BAR_PV_DONE0 + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u,
-                          abort_flag, p.timeout_ns);
+      if ((kv0 + BN > len) || (p.causal && kv0 + BN - 1 > qt * BM))
+        mask_scores(s, kv0, p.causal ? min(len, q_idx + 1) : len);
+      if (j >= 2) {   // P buffer j&1 was last read by PV_{j-2}
+        ok = wait_warp(ctl.bar(BAR_PV_DONE0 + (j & 1)), (uint32_t)((j - 2) >> 1) & 1u,
+                       abort_flag, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + COL_O + cc, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tmem_st32(tmem + lane_off + COL_O + cc, o);
-        }
       }
-      const uint32_t p_col = COL_P0 + 64u * (uint32_t)(j & 1);
-      {
-        uint32_t a[32], b[32];
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          a[x] = pk[x];
-          b[x] = pk[32 + x];
-        }
-        tmem_st32(tmem + lane_off + p_col, a);
-        tmem_st32(tmem + lane_off + p_col + 32, b);
+      bool moved;
+      const float alpha =
+          softmax_tile(s, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)(j & 1), moved);
+      if (__any_sync(0xffffffffu, moved && j > 0)) {   // rescale O after PV_{j-1} landed
+        ok = wait_warp(ctl.bar(BAR_PV_DONE0 + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u,
+                       abort_flag, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        rescale_o<D>(tmem + lane_off + C::COL_O, alpha);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(BAR_P_FULL0 + (j & 1)));
+      mbar_arrive(ctl.bar(BAR_P_FULL0 + (j & 1)));
     }
-
-    // ---- epilogue: O / l -> bf16, LSE ----
     if (ok)
-      ok = wait_warp(bar(BAR_PV_DONE0 + ((n_kv - 1) & 1)), (uint32_t)((n_kv - 1) >> 1) & 1u,
-                        abort_flag, p.timeout_ns);
+      ok = wait_warp(ctl.bar(BAR_PV_DONE0 + ((n_kv - 1) & 1)), (uint32_t)((n_kv - 1) >> 1) & 1u,
+                     abort_flag, p.timeout_ns);
     if (ok) {
       tc_fence_after();
       const bool live = q_idx < len;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow =
-          p.o + ((long long)(seq_start + q_idx) * p.Hq + h) * (long long)D;
-#pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + COL_O + cc, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv_l,
-                             __uint_as_float(o[2 * x + 1]) * inv_l);
-        if (live) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc);
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-        }
-      }
-      if (live) {
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        p.lse[lse_base + q_idx] = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
-      }
+      store_row<D>(tmem + lane_off + C::COL_O, st.lr > 0.f ? 1.f / st.lr : 0.f,
+                   p.o + ((long long)(seq_start + q_idx) * p.Hq + h) * (long long)D, live);
+      if (live) p.lse[lse_base + q_idx] = row_lse(st, p.scale);
     }
   }
 
-  // ---- teardown ----
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -621,8 +828,14 @@ static bool make_map(EncodeTiledFn enc, CUtensorMap *m, const void *base, int he
 
 constexpr int MAX_DEVICES = 64;
 
+template <typename K>
+static bool opt_in_smem(K kernel, uint32_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+         cudaSuccess;
+}
+
 // Per device: compute capability check and the shared-memory opt-in of the
-// three kernel instantiations, done once.
+// kernel instantiations, done once.
 static attn_status prepare_device(int dev) {
   static std::mutex mu;
   static signed char state[MAX_DEVICES];   // 0 unknown, 1 ready, -1 unsupported
@@ -638,12 +851,9 @@ static attn_status prepare_device(int dev) {
     state[dev] = -1;
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
-  if (cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<64>::SMEM_BYTES) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::SMEM_BYTES) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_fwd_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<256>::SMEM_BYTES) != cudaSuccess)
+  if (!opt_in_smem(attn_fwd_kernel<64>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256>, Cfg<256>::SMEM_BYTES))
     return ATTN_ERR_CUDA;
   state[dev] = 1;
   return ATTN_OK;
@@ -659,13 +869,6 @@ static unsigned long long wait_timeout_ns() {
   return t;
 }
 
-template <int D>
-static attn_status launch(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          const Params &p, long long grid, cudaStream_t stream) {
-  attn_fwd_kernel<D><<<(unsigned)grid, NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 }  // namespace attn
 
 extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -677,7 +880,9 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  auto misaligned = [](const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+  auto misaligned = [](const void *ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
   if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
       misaligned(lse, 4))
     return ATTN_ERR_ALIGNMENT;
@@ -706,22 +911,32 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
   p.N = N;
   p.group = Hq / Hkv;
   p.causal = causal ? 1 : 0;
-  p.num_qt = (N + BM - 1) / BM;
+  p.unit_rows = BM;
+  p.num_units = (N + p.unit_rows - 1) / p.unit_rows;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
 
-  // fixed batch: exactly the tiles; packed: an upper bound on them
-  // (sum_s ceil(L_s/128) <= T/128 + B), surplus CTAs exit at once.
-  const long long pairs = cu_seqlens ? (long long)(N + BM - 1) / BM + B : (long long)p.num_qt * B;
-  const long long grid = pairs * Hq;
+  // fixed batch: exactly the units; packed: an upper bound on them
+  // (sum_s ceil(L_s/U) <= T/U + B), surplus CTAs exit at once.
+  const long long units = cu_seqlens ? (long long)p.num_units + B : (long long)p.num_units * B;
+  const long long grid = units * Hq;
   if (grid > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
 
   switch (d) {
-    case 64: return launch<64>(mq, mk, mv, p, grid, stream);
-    case 128: return launch<128>(mq, mk, mv, p, grid, stream);
-    default: return launch<256>(mq, mk, mv, p, grid, stream);
+    case 64:
+      attn_fwd_kernel<64><<<(unsigned)grid, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+      break;
+    case 128:
+      attn_fwd_kernel<128><<<(unsigned)grid, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv,
+                                                                                    p);
+      break;
+    default:
+      attn_fwd_kernel<256><<<(unsigned)grid, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv,
+                                                                                    p);
+      break;
   }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 extern "C" attn_status attn_get_status(cudaStream_t stream) {
