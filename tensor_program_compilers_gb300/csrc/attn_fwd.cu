@@ -23,21 +23,23 @@
 //  * masked keys read -inf, the identity of max (tang, section 2.1, guarded
 //    views), so fully masked tiles are skipped rather than computed.
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warp 0     TMA producer: Q once, then K_0, K_1, V_0, K_2, V_1, ... into a
 //              ring of shared-memory slots (128-byte swizzle)
-//   warp 1     TMEM allocator and MMA issuer (one thread)
+//   warp 1     TMEM allocator and QK^T issuer (one thread); at d = 256 also
+//              the PV issuer, keeping the order QK_{j+1}, PV_j
 //   warps 2-5  softmax warpgroup: thread t owns query row t (TMEM lane t)
+//   warp 6     PV issuer (one thread), d <= 128
+// Each issuing thread shares its SM sub-partition with a busy softmax warp,
+// so the issue loops keep their instruction counts small.
 //
-// Tensor memory (512 columns x 128 lanes x 32 bit), SB = 2 score buffers for
-// d <= 128 and 1 for d = 256 (whose accumulator needs 256 columns):
-//   S_b   [128 b, 128 b + 128)      fp32 scores, b < SB
-//   P_b   [128 SB + 64 b, +64)      bf16 probabilities (two per column), b < 2
-//   O     [128 SB + 128, +d)        fp32 accumulator
-// The MMA issue order is QK_0, QK_1, PV_0, QK_2, PV_1, ...: the scores of the
-// next key tile are computed while the softmax warps work on this one.  With
-// two score buffers QK_{j+1} waits only for the softmax to have read S_{j-1}.
-//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   S     [0, 128)          fp32 scores of the current key tile
+//   P_b   [128 + 64 b, +64) bf16 probabilities (two per column), b < 2
+//   O     [256, 256 + d)    fp32 accumulator
+// QK_{j+1} is issued as soon as the softmax warps have read S_j into
+// registers, so it runs while they compute P_j.
+
 // Every pipeline wait is bounded: past a time limit it records
 // ATTN_ERR_TIMEOUT in a device status word and every role stops issuing,
 // waits (bounded) for its copies and MMAs in flight, and the CTA releases
@@ -59,7 +61,7 @@ namespace attn {
 
 constexpr int BM = 128;            // query rows per tile (one per TMEM lane)
 constexpr int BN = 128;            // keys per tile
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t CHUNK_BYTES = 128 * 128;   // 128 rows x 64 bf16, one swizzle column
 constexpr float RESCALE_THRESHOLD = 16.0f;    // log2 units: P <= 2^16 between moves
@@ -68,15 +70,18 @@ template <int D>
 struct Cfg {
   static constexpr int CHUNKS = D / 64;
   static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;   // one Q, K or V tile
-  static constexpr int SB = D <= 128 ? 2 : 1;                     // score buffers
   static constexpr int STAGES = D == 64 ? 10 : (D == 128 ? 6 : 2);  // K/V ring slots
+  // Separate QK^T and PV issuing threads when the ring is deep enough; with
+  // two slots (d = 256) one thread keeps the order QK_{j+1}, PV_j so that the
+  // load of V_j overlaps QK_{j+1}.
+  static constexpr bool SPLIT_ISSUE = STAGES >= 4;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = TILE_BYTES;
-  static constexpr uint32_t OFF_CTL = TILE_BYTES * (1 + STAGES);
+  static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
   static constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;   // control block + alignment
-  static constexpr uint32_t COL_P0 = 128 * SB;
-  static constexpr uint32_t COL_O = COL_P0 + 128;
-  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * (uint32_t)b; }
+  static constexpr uint32_t COL_S = 0;
+  static constexpr uint32_t COL_P0 = 128;
+  static constexpr uint32_t COL_O = 256;
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
@@ -86,19 +91,19 @@ struct Cfg {
 // empty[0..STAGES)).
 enum : int {
   BAR_Q_FULL = 0,
-  BAR_S_FULL0,     // S_b written (MMA commit), b = 0, 1
-  BAR_S_FULL1,
-  BAR_S_FREE0,     // S_b read into registers (softmax warps)
-  BAR_S_FREE1,
-  BAR_P_FULL0,     // P_b written (softmax warps)
+  BAR_S_FULL,      // S written (QK issuer commit)
+  BAR_S_FREE,      // S read into registers (softmax warps)
+  BAR_P_FULL0,     // P_b written (softmax warps), b = 0, 1
   BAR_P_FULL1,
-  BAR_PV_DONE0,    // the PV reading P_b completed (MMA commit)
+  BAR_PV_DONE0,    // the PV reading P_b completed (PV issuer commit)
   BAR_PV_DONE1,
-  BAR_DRAIN,
+  BAR_DRAIN_QK,    // abort drain of each issuer
+  BAR_DRAIN_PV,
   BAR_RING
 };
 
 struct Params {
+  const __nv_bfloat16 *q;
   __nv_bfloat16 *o;
   float *lse;
   const int *cu_seqlens;
@@ -532,31 +537,30 @@ __device__ __forceinline__ float row_lse(const RowState &st, float scale) {
   return st.l > 0.f ? m_use * scale + logf(st.l) : -INFINITY;
 }
 
-// One 128x128x(16*K_STEPS) QK^T into TMEM: A = Q tile, B = K tile, both
-// K-major in 64-column swizzle chunks.
+// One 128x128xd QK^T into TMEM: A = Q tile (qdesc), B = K tile (kdesc), both
+// K-major in 64-column swizzle chunks.  Per step of 16 head-dim columns the
+// operands advance 32 bytes inside a 128-byte swizzle row, and CHUNK_BYTES
+// from one 64-column chunk to the next.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_s, uint32_t k_s) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BN, 0);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    // 16 head-dim columns per step = 32 bytes inside a 128-byte swizzle row;
-    // 64-column chunks are CHUNK_BYTES apart; 8-row groups 1024 bytes apart.
     const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(q_s + koff, 16, 1024), smem_desc_sw128(k_s + koff, 16, 1024),
-           IDESC, kk > 0 ? 1u : 0u);
+    mma_ss(d_tmem, desc_add(qdesc, koff), desc_add(kdesc, koff), IDESC, kk > 0 ? 1u : 0u);
   }
 }
 
-// O (+)= P V_j: A = P from TMEM (bf16 pairs), B = V tile with keys as K and
-// the head dim as N (N contiguous: 64-wide swizzle atoms CHUNK_BYTES apart,
-// 8-key groups 1024 bytes apart, 16 keys = 2048 bytes per step).
+// O (+)= P V_j: A = P from TMEM (bf16 pairs), B = V tile (vdesc) with keys as
+// K and the head dim as N (N contiguous: 64-wide swizzle atoms CHUNK_BYTES
+// apart, 8-key groups 1024 bytes apart, 16 keys = 2048 bytes per step).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_s,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
                                          bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
-    mma_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(v_s + kk * 2048, CHUNK_BYTES, 1024), IDESC,
+    mma_ts(d_tmem, p_tmem + kk * 8, desc_add(vdesc, kk * 2048), IDESC,
            (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -570,13 +574,14 @@ struct Ctl {
 template <int STAGES>
 __device__ __forceinline__ void init_barriers(const Ctl &c) {
   mbar_init(c.bar(BAR_Q_FULL), 1);
+  mbar_init(c.bar(BAR_S_FULL), 1);
+  mbar_init(c.bar(BAR_S_FREE), 4 * 32);
   for (int b = 0; b < 2; ++b) {
-    mbar_init(c.bar(BAR_S_FULL0 + b), 1);
-    mbar_init(c.bar(BAR_S_FREE0 + b), 4 * 32);
     mbar_init(c.bar(BAR_P_FULL0 + b), 4 * 32);
     mbar_init(c.bar(BAR_PV_DONE0 + b), 1);
   }
-  mbar_init(c.bar(BAR_DRAIN), 1);
+  mbar_init(c.bar(BAR_DRAIN_QK), 1);
+  mbar_init(c.bar(BAR_DRAIN_PV), 1);
   for (int s = 0; s < STAGES; ++s) {
     mbar_init(c.bar(BAR_RING + s), 1);
     mbar_init(c.bar(BAR_RING + STAGES + s), 1);
@@ -595,6 +600,30 @@ __device__ void drain_loads(const Ctl &c, int issued, unsigned long long timeout
   }
 }
 
+// O (+)= P_i V_i: waits for P_i (softmax warps) and V_i (ring position
+// 2i + 2, the last one 2n - 1), issues the MMAs, commits PV_DONE and the
+// slot release.
+template <int D>
+__device__ __forceinline__ bool pv_step(const Ctl &ctl, uint32_t tmem, uint32_t kv_s, int i,
+                                        int n_kv, volatile uint32_t *abort_flag,
+                                        unsigned long long timeout_ns) {
+  using C = Cfg<D>;
+  const uint32_t bar0 = ctl.bar(0);
+  const int pos = i == n_kv - 1 ? 2 * n_kv - 1 : 2 * i + 2;
+  const int slot = pos % C::STAGES;
+  if (!wait_bounded(bar0 + 8u * (BAR_P_FULL0 + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag,
+                    timeout_ns) ||
+      !wait_bounded(bar0 + 8u * (BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u, abort_flag,
+                    timeout_ns))
+    return false;
+  tc_fence_after();
+  issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)(i & 1),
+              desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES), i > 0);
+  tc_commit(bar0 + 8u * (BAR_PV_DONE0 + (i & 1)));
+  tc_commit(bar0 + 8u * (BAR_RING + C::STAGES + slot));
+  return true;
+}
+
 // ================================================================ kernel
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -602,7 +631,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D>;
-  constexpr int SB = C::SB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t base_s = smem_u32(smem);
@@ -674,50 +702,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer: QK_0, QK_1, PV_0, QK_2, PV_1, ...
+    // ---------------- QK^T issuer: S = Q K_j^T once the softmax warps have
+    // read S_{j-1}.  K_j sits at ring position 0 (j = 0) or 2j - 1, V_i at
+    // 2i + 2 (the last one at 2n - 1).  Without a separate PV issuer this
+    // thread also issues PV_{j-1} after QK_j.
     if (lane == 0) {
-      int it = 0;
-      bool ok = wait_bounded(ctl.bar(BAR_Q_FULL), 0, abort_flag, p.timeout_ns);
-      auto pv = [&](int i) -> bool {
-        if (!wait_bounded(ctl.bar(BAR_P_FULL0 + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag,
-                          p.timeout_ns))
-          return false;
-        const int slot = it % C::STAGES;
-        if (!wait_bounded(bar_full(slot), (uint32_t)(it / C::STAGES) & 1u, abort_flag,
-                          p.timeout_ns))
-          return false;
-        tc_fence_after();
-        issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)(i & 1),
-                    kv_s + slot * C::TILE_BYTES, i > 0);
-        tc_commit(ctl.bar(BAR_PV_DONE0 + (i & 1)));
-        tc_commit(bar_empty(slot));
-        ++it;
-        return true;
-      };
+      const uint32_t bar0 = ctl.bar(0);
+      const uint64_t kdesc0 = smem_desc_sw128(kv_s, 16, 1024);
+      const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
+      bool ok = wait_bounded(bar0 + 8u * BAR_Q_FULL, 0, abort_flag, p.timeout_ns);
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int b = j % SB;
-        // S_b last held the scores of key tile j - SB: wait until they were read
-        if (j >= SB)
-          ok = wait_bounded(ctl.bar(BAR_S_FREE0 + b), (uint32_t)(j / SB - 1) & 1u, abort_flag,
-                            p.timeout_ns);
-        if (!ok) break;
-        const int slot = it % C::STAGES;
-        ok = wait_bounded(bar_full(slot), (uint32_t)(it / C::STAGES) & 1u, abort_flag,
-                          p.timeout_ns);
-        if (!ok) break;
+        const int pos = j == 0 ? 0 : 2 * j - 1;
+        const int slot = pos % C::STAGES;
+        if (j > 0 && !(ok = wait_bounded(bar0 + 8u * BAR_S_FREE, (uint32_t)(j - 1) & 1u,
+                                         abort_flag, p.timeout_ns)))
+          break;
+        if (!(ok = wait_bounded(bar0 + 8u * (BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u,
+                                abort_flag, p.timeout_ns)))
+          break;
         tc_fence_after();
-        issue_qk<D>(tmem + C::col_s(b), q_s, kv_s + slot * C::TILE_BYTES);
-        tc_commit(ctl.bar(BAR_S_FULL0 + b));
-        tc_commit(bar_empty(slot));
-        ++it;
-        if (j > 0) ok = pv(j - 1);
+        issue_qk<D>(tmem + C::COL_S, qdesc, desc_add(kdesc0, slot * C::TILE_BYTES));
+        tc_commit(bar0 + 8u * BAR_S_FULL);
+        tc_commit(bar0 + 8u * (BAR_RING + C::STAGES + slot));
+        if (!C::SPLIT_ISSUE && j > 0) ok = pv_step<D>(ctl, tmem, kv_s, j - 1, n_kv, abort_flag,
+                                                      p.timeout_ns);
       }
-      if (ok) ok = pv(n_kv - 1);
-      tc_commit(ctl.bar(BAR_DRAIN));   // no MMA may be in flight at teardown
-      wait_drain(ctl.bar(BAR_DRAIN), 0, p.timeout_ns);
+      if (!C::SPLIT_ISSUE && ok)
+        ok = pv_step<D>(ctl, tmem, kv_s, n_kv - 1, n_kv, abort_flag, p.timeout_ns);
+      tc_commit(bar0 + 8u * BAR_DRAIN_QK);   // no MMA may be in flight at teardown
+      wait_drain(bar0 + 8u * BAR_DRAIN_QK, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp == 6) {
+    // ---------------- PV issuer: O (+)= P_i V_i once the softmax warps have
+    // written P_i.
+    if (C::SPLIT_ISSUE && lane == 0) {
+      const uint32_t bar0 = ctl.bar(0);
+      bool ok = true;
+      for (int i = 0; ok && i < n_kv; ++i)
+        ok = pv_step<D>(ctl, tmem, kv_s, i, n_kv, abort_flag, p.timeout_ns);
+      tc_commit(bar0 + 8u * BAR_DRAIN_PV);
+      wait_drain(bar0 + 8u * BAR_DRAIN_PV, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
     // ---------------- softmax warpgroup
     const int wq = warp & 3;                        // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;
@@ -727,14 +755,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     RowState st{-INFINITY, 0.f, 0.f};
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int b = j % SB;
-      ok = wait_warp(ctl.bar(BAR_S_FULL0 + b), (uint32_t)(j / SB) & 1u, abort_flag, p.timeout_ns);
+      ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)j & 1u, abort_flag, p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
       float s[BN];
-      load_scores(tmem + lane_off + C::col_s(b), s);
+      load_scores(tmem + lane_off + C::COL_S, s);
       tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_S_FREE0 + b));   // S_b may now take the scores of tile j + SB
+      mbar_arrive(ctl.bar(BAR_S_FREE));   // S may now take the scores of tile j + 1
       const int kv0 = j * BN;
       if ((kv0 + BN > len) || (p.causal && kv0 + BN - 1 > qt * BM))
         mask_scores(s, kv0, p.causal ? min(len, q_idx + 1) : len);
@@ -902,6 +929,7 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
     return ATTN_ERR_INVALID_ARG;
 
   Params p{};
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
   p.o = reinterpret_cast<__nv_bfloat16 *>(o);
   p.lse = lse;
   p.cu_seqlens = cu_seqlens;

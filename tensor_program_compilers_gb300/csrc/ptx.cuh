@@ -125,6 +125,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Descriptor plus a byte offset (a multiple of 16) added to its start
+// address field; valid while the field does not carry out (shared addresses
+// below 256 KB), so only the low word changes.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  uint64_t r;
+  asm("{\n\t.reg .b32 lo, hi;\n\t"
+      "mov.b64 {lo, hi}, %1;\n\t"
+      "add.u32 lo, lo, %2;\n\t"
+      "mov.b64 %0, {lo, hi};\n\t}\n"
+      : "=l"(r)
+      : "l"(desc), "r"(byte_off >> 4));
+  return r;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 D, M = 128.
 // b_mn_major: B operand stored with N contiguous (else K contiguous).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t n, uint32_t b_mn_major) {
