@@ -50,6 +50,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
@@ -70,15 +71,17 @@ template <int D>
 struct Cfg {
   static constexpr int CHUNKS = D / 64;
   static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;   // one Q, K or V tile
-  static constexpr int STAGES = D == 64 ? 10 : (D == 128 ? 6 : 2);  // K/V ring slots
+  static constexpr int QB = D == 256 ? 1 : 2;                       // Q buffers
+  static constexpr int STAGES = D == 64 ? 10 : (D == 128 ? 5 : 2);  // K/V ring slots
   // Separate QK^T and PV issuing threads when the ring is deep enough; with
   // two slots (d = 256) one thread keeps the order QK_{j+1}, PV_j so that the
   // load of V_j overlaps QK_{j+1}.
   static constexpr bool SPLIT_ISSUE = STAGES >= 4;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_KV = TILE_BYTES;
+  static constexpr uint32_t OFF_KV = TILE_BYTES * QB;
   static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
-  static constexpr uint32_t SMEM_BYTES = OFF_CTL + 512 + 1024;   // control block + alignment
+  static constexpr uint32_t CTL_BYTES = 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_P0 = 128;
   static constexpr uint32_t COL_O = 256;
@@ -90,17 +93,25 @@ struct Cfg {
 // Barrier slots of the control block, then the K/V ring (full[0..STAGES),
 // empty[0..STAGES)).
 enum : int {
-  BAR_Q_FULL = 0,
-  BAR_S_FULL,      // S written (QK issuer commit)
-  BAR_S_FREE,      // S read into registers (softmax warps)
-  BAR_P_FULL0,     // P_b written (softmax warps), b = 0, 1
+  BAR_Q_FULL0 = 0,   // Q buffer b loaded (TMA), b < 2
+  BAR_Q_FULL1,
+  BAR_Q_EMPTY0,      // Q buffer b no longer read (QK issuer commit)
+  BAR_Q_EMPTY1,
+  BAR_S_FULL,        // S written (QK issuer commit)
+  BAR_S_FREE,        // S read into registers (softmax warps)
+  BAR_P_FULL0,       // P_b written (softmax warps), b < 2
   BAR_P_FULL1,
-  BAR_PV_DONE0,    // the PV reading P_b completed (PV issuer commit)
+  BAR_PV_DONE0,      // the PV reading P_b completed (PV issuer commit)
   BAR_PV_DONE1,
-  BAR_DRAIN_QK,    // abort drain of each issuer
+  BAR_O_FREE,        // O read by the epilogue (softmax warps)
+  BAR_INFO_FULL0,    // tile-info entry e written (producer), e < INFO_SLOTS
+  BAR_INFO_EMPTY0 = BAR_INFO_FULL0 + 4,   // tile-info entry e consumed
+  BAR_DRAIN_QK = BAR_INFO_EMPTY0 + 4,     // abort drain of each issuer
   BAR_DRAIN_PV,
-  BAR_RING
+  BAR_RING           // K/V ring: full[0..STAGES), then empty[0..STAGES)
 };
+constexpr int INFO_SLOTS = 4;
+constexpr int INFO_INTS = 8;
 
 struct Params {
   const __nv_bfloat16 *q;
@@ -210,10 +221,9 @@ __device__ int units_at_or_above(const SeqUnits &su, const int *cu, int B, int x
 // ordered longest first -- descending unit index, i.e. descending number of
 // causal key tiles -- with heads fastest so that the query heads of one
 // key/value head run side by side.
-__device__ Tile decode_tile(const Params &p) {
+__device__ Tile decode_tile(const Params &p, long long idx) {
   Tile t{};
   const int lane = threadIdx.x & 31;
-  const long long idx = blockIdx.x;
   const int U = p.unit_rows;
   if (p.cu_seqlens == nullptr) {
     const long long per = (long long)p.B * p.Hq;
@@ -225,7 +235,7 @@ __device__ Tile decode_tile(const Params &p) {
     t.seq_start = b * p.N;
     t.len = p.N;
     t.lse_base = ((long long)b * p.Hq + t.h) * p.N;
-    t.valid = t.unit >= 0;
+    t.valid = t.unit >= 0 && idx < (long long)p.num_units * per;
     return t;
   }
   const int *cu = p.cu_seqlens;
@@ -302,19 +312,6 @@ __device__ Tile decode_tile(const Params &p) {
   t.lse_base = (long long)t.h * p.N + t.seq_start;
   t.valid = 1;
   return t;
-}
-
-// Warp 0 decodes, lane 0 publishes the tile in the control block.
-__device__ __forceinline__ void publish_tile(const Params &p, int *info) {
-  Tile t = decode_tile(p);
-  if ((threadIdx.x & 31) == 0) {
-    info[0] = t.valid;
-    info[1] = t.seq_start;
-    info[2] = t.len;
-    info[3] = t.unit;
-    info[4] = t.h;
-    *reinterpret_cast<long long *>(info + 6) = t.lse_base;
-  }
 }
 
 // ---------------------------------------------------------------- softmax pieces
@@ -566,19 +563,26 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 
 // ---------------------------------------------------------------- control block
 struct Ctl {
-  uint64_t *bars;
-  uint32_t *words;   // [0] TMEM base, [1] abort flag, [2..] tile info
-  __device__ uint32_t bar(int i) const { return smem_u32(bars + i); }
+  uint32_t bar0;       // shared address of barrier 0 (barriers are 8 bytes apart)
+  uint32_t *words;     // [0] TMEM base, [1] abort flag
+  int *info;           // INFO_SLOTS entries of INFO_INTS ints
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
 template <int STAGES>
-__device__ __forceinline__ void init_barriers(const Ctl &c) {
-  mbar_init(c.bar(BAR_Q_FULL), 1);
-  mbar_init(c.bar(BAR_S_FULL), 1);
-  mbar_init(c.bar(BAR_S_FREE), 4 * 32);
+__device__ __forceinline__ void init_barriers(const Ctl &c, uint32_t info_consumers) {
   for (int b = 0; b < 2; ++b) {
+    mbar_init(c.bar(BAR_Q_FULL0 + b), 1);
+    mbar_init(c.bar(BAR_Q_EMPTY0 + b), 1);
     mbar_init(c.bar(BAR_P_FULL0 + b), 4 * 32);
     mbar_init(c.bar(BAR_PV_DONE0 + b), 1);
+  }
+  mbar_init(c.bar(BAR_S_FULL), 1);
+  mbar_init(c.bar(BAR_S_FREE), 4 * 32);
+  mbar_init(c.bar(BAR_O_FREE), 4 * 32);
+  for (int e = 0; e < INFO_SLOTS; ++e) {
+    mbar_init(c.bar(BAR_INFO_FULL0 + e), 1);
+    mbar_init(c.bar(BAR_INFO_EMPTY0 + e), info_consumers);
   }
   mbar_init(c.bar(BAR_DRAIN_QK), 1);
   mbar_init(c.bar(BAR_DRAIN_PV), 1);
@@ -590,41 +594,68 @@ __device__ __forceinline__ void init_barriers(const Ctl &c) {
   mbar_init_fence();
 }
 
-// Producer-side drain after an abort: wait for the copies already issued.
-template <int STAGES>
-__device__ void drain_loads(const Ctl &c, int issued, unsigned long long timeout_ns) {
-  wait_drain(c.bar(BAR_Q_FULL), 0, timeout_ns);
-  for (int s = 0; s < STAGES && s < issued; ++s) {
-    const int last = s + STAGES * ((issued - 1 - s) / STAGES);
-    wait_drain(c.bar(BAR_RING + s), (uint32_t)(last / STAGES) & 1u, timeout_ns);
-  }
-}
+// A decoded work tile as the roles use it.
+struct TileInfo {
+  int valid, seq_start, len, qt, h;
+  long long lse_base;
+  int n_kv;   // key tiles to visit
+};
 
-// O (+)= P_i V_i: waits for P_i (softmax warps) and V_i (ring position
-// 2i + 2, the last one 2n - 1), issues the MMAs, commits PV_DONE and the
-// slot release.
-template <int D>
-__device__ __forceinline__ bool pv_step(const Ctl &ctl, uint32_t tmem, uint32_t kv_s, int i,
-                                        int n_kv, volatile uint32_t *abort_flag,
-                                        unsigned long long timeout_ns) {
-  using C = Cfg<D>;
-  const uint32_t bar0 = ctl.bar(0);
-  const int pos = i == n_kv - 1 ? 2 * n_kv - 1 : 2 * i + 2;
-  const int slot = pos % C::STAGES;
-  if (!wait_bounded(bar0 + 8u * (BAR_P_FULL0 + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag,
-                    timeout_ns) ||
-      !wait_bounded(bar0 + 8u * (BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u, abort_flag,
+// Consumer side of the tile-info ring: entry k % INFO_SLOTS (warp-uniform).
+__device__ __forceinline__ bool read_tile(const Ctl &c, int k, TileInfo &t,
+                                          volatile uint32_t *abort_flag,
+                                          unsigned long long timeout_ns, bool arrive) {
+  const int e = k % INFO_SLOTS;
+  if (!wait_bounded(c.bar(BAR_INFO_FULL0 + e), (uint32_t)(k / INFO_SLOTS) & 1u, abort_flag,
                     timeout_ns))
     return false;
-  tc_fence_after();
-  issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)(i & 1),
-              desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES), i > 0);
-  tc_commit(bar0 + 8u * (BAR_PV_DONE0 + (i & 1)));
-  tc_commit(bar0 + 8u * (BAR_RING + C::STAGES + slot));
+  const volatile int *src = c.info + e * INFO_INTS;
+  t.valid = src[0];
+  t.seq_start = src[1];
+  t.len = src[2];
+  t.qt = src[3];
+  t.h = src[4];
+  t.n_kv = src[5];
+  t.lse_base = (long long)(unsigned)src[6] | ((long long)src[7] << 32);
+  if (arrive) mbar_arrive(c.bar(BAR_INFO_EMPTY0 + e));
   return true;
 }
 
+// O (+)= P_g V_i for global key step g (local step i of the tile): waits for
+// P_g (softmax warps) and V_i at ring position pos, issues the MMAs, commits
+// PV_DONE and the slot release.  The first step of a tile overwrites O.
+template <int D>
+__device__ __forceinline__ bool pv_step(const Ctl &ctl, uint32_t tmem, uint32_t kv_s, long long g,
+                                        int i, long long pos, volatile uint32_t *abort_flag,
+                                        unsigned long long timeout_ns) {
+  using C = Cfg<D>;
+  const int slot = (int)(pos % C::STAGES);
+  const int pb = (int)(g & 1);
+  if (!wait_bounded(ctl.bar(BAR_P_FULL0 + pb), (uint32_t)(g >> 1) & 1u, abort_flag, timeout_ns) ||
+      !wait_bounded(ctl.bar(BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u, abort_flag,
+                    timeout_ns))
+    return false;
+  tc_fence_after();
+  issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)pb,
+              desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES), i > 0);
+  tc_commit(ctl.bar(BAR_PV_DONE0 + pb));
+  tc_commit(ctl.bar(BAR_RING + C::STAGES + slot));
+  return true;
+}
+
+// Ring positions of a tile's loads, in the producer's order K_0, K_1, V_0,
+// K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1} (2n items from `base`).
+__device__ __forceinline__ long long pos_k(long long base, int j) {
+  return base + (j == 0 ? 0 : 2 * j - 1);
+}
+__device__ __forceinline__ long long pos_v(long long base, int i, int n) {
+  return base + (i == n - 1 ? 2 * n - 1 : 2 * i + 2);
+}
+
 // ================================================================ kernel
+// Persistent: with G = gridDim.x CTAs, CTA b processes one tile of each
+// round of G tiles of the longest-first list -- tile b of even rounds, tile
+// G-1-b of odd rounds -- until the producer publishes an invalid tile.
 template <int D>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -636,164 +667,246 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t base_s = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  Ctl ctl{reinterpret_cast<uint64_t *>(smem + C::OFF_CTL), nullptr};
-  ctl.words = reinterpret_cast<uint32_t *>(ctl.bars + BAR_RING + 2 * C::STAGES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_CTL);
+  Ctl ctl;
+  ctl.bar0 = smem_u32(bars);
+  ctl.words = reinterpret_cast<uint32_t *>(bars + BAR_RING + 2 * C::STAGES);
+  ctl.info = reinterpret_cast<int *>(ctl.words + 4);
   volatile uint32_t *abort_flag = ctl.words + 1;
-  int *info = reinterpret_cast<int *>(ctl.words + 2);
-  auto bar_full = [&](int s) { return ctl.bar(BAR_RING + s); };
-  auto bar_empty = [&](int s) { return ctl.bar(BAR_RING + C::STAGES + s); };
-
-  if (warp == 0) {
-    publish_tile(p, info);
-    if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-    }
-  } else if (warp == 1 && lane == 0) {
-    init_barriers<C::STAGES>(ctl);
-  }
-  __syncthreads();
-  if (!info[0]) return;   // no tile for this CTA (uniform)
-
-  const int seq_start = info[1], len = info[2], qt = info[3], h = info[4];
-  const long long lse_base = *reinterpret_cast<long long *>(info + 6);
-  const int kvh = h / p.group;
-  const int kv_tiles = (len + BN - 1) / BN;
-  const int n_kv = p.causal ? min(qt + 1, kv_tiles) : kv_tiles;
+  const uint32_t q_s = base_s + C::OFF_Q;
+  const uint32_t kv_s = base_s + C::OFF_KV;
+  // consumers of each tile-info entry: QK issuer, PV issuer, 4 softmax warps
+  constexpr uint32_t INFO_CONSUMERS = C::SPLIT_ISSUE ? 6 : 5;
 
   if (warp == 1) {
+    if (lane == 0) init_barriers<C::STAGES>(ctl, INFO_CONSUMERS);
+    __syncwarp();
     tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
     tmem_relinquish();
+  } else if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.words[0];
-  const uint32_t q_s = base_s + C::OFF_Q;
-  const uint32_t kv_s = base_s + C::OFF_KV;
 
   if (warp == 0) {
-    // ---------------- TMA producer: Q, then K0, K1, V0, K2, V1, ..., V_{n-1}
-    if (lane == 0) {
-      mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL), C::TILE_BYTES);
-      for (int c = 0; c < C::CHUNKS; ++c)
-        tma_load_3d(q_s + c * CHUNK_BYTES, &tm_q, ctl.bar(BAR_Q_FULL), c * 64, h,
-                    seq_start + qt * BM);
-      int it = 0;
-      bool ok = true;
-      auto load = [&](const CUtensorMap *tm, int j) -> bool {
-        const int slot = it % C::STAGES;
-        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!wait_bounded(bar_empty(slot), ph ^ 1u, abort_flag, p.timeout_ns)) return false;
-        mbar_arrive_expect_tx(bar_full(slot), C::TILE_BYTES);
-        const uint32_t dst = kv_s + slot * C::TILE_BYTES;
-        for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_3d(dst + c * CHUNK_BYTES, tm, bar_full(slot), c * 64, kvh, seq_start + j * BN);
-        ++it;
-        return true;
-      };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        ok = load(&tm_k, j);
-        if (ok && j >= 1) ok = load(&tm_v, j - 1);
+    // ---------------- producer: decode tiles, publish them, load Q and K/V
+    long long pos = 0;   // global ring position
+    int q_loads = 0;     // Q tiles loaded so far (buffer q_loads % QB next)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      // round k covers tiles [k G, (k+1) G); odd rounds run backwards so that
+      // the CTA given the longest tile of a round gets the shortest next
+      const long long G = gridDim.x;
+      const Tile t = decode_tile(p, (long long)k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x));
+      const int kv_tiles = (t.len + BN - 1) / BN;
+      const int n = t.valid ? (p.causal ? min(t.unit + 1, kv_tiles) : kv_tiles) : 0;
+      if (lane == 0) {
+        const int e = k % INFO_SLOTS;
+        ok = wait_bounded(ctl.bar(BAR_INFO_EMPTY0 + e), ((uint32_t)(k / INFO_SLOTS) & 1u) ^ 1u,
+                          abort_flag, p.timeout_ns);
+        if (ok) {
+          int *dst = ctl.info + e * INFO_INTS;
+          dst[0] = t.valid;
+          dst[1] = t.seq_start;
+          dst[2] = t.len;
+          dst[3] = t.unit;
+          dst[4] = t.h;
+          dst[5] = n;
+          dst[6] = (int)(unsigned)(t.lse_base & 0xFFFFFFFFll);
+          dst[7] = (int)(t.lse_base >> 32);
+          mbar_arrive(ctl.bar(BAR_INFO_FULL0 + e));   // release: the entry is visible
+        }
+        if (ok && t.valid) {
+          const int kvh = t.h / p.group;
+          const int qb = k % C::QB;
+          // Q buffer qb last served tile k - QB
+          if (k >= C::QB)
+            ok = wait_bounded(ctl.bar(BAR_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
+                              abort_flag, p.timeout_ns);
+          if (ok) {
+            ++q_loads;
+            mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL0 + qb), C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(q_s + qb * C::TILE_BYTES + c * CHUNK_BYTES, &tm_q,
+                          ctl.bar(BAR_Q_FULL0 + qb), c * 64, t.h, t.seq_start + t.unit * BM);
+          }
+          // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
+          for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
+            const int slot = (int)(pos % C::STAGES);
+            if (!(ok = wait_bounded(ctl.bar(BAR_RING + C::STAGES + slot),
+                                    ((uint32_t)(pos / C::STAGES) & 1u) ^ 1u, abort_flag,
+                                    p.timeout_ns)))
+              break;
+            // item 0: K_0; last item: V_{n-1}; odd: K_{(item+1)/2}; even: V_{item/2-1}
+            const bool last = item == 2 * n - 1;
+            const bool is_v = last || (item > 0 && (item & 1) == 0);
+            const int kt = last ? n - 1 : (item == 0 ? 0 : (is_v ? item / 2 - 1 : (item + 1) / 2));
+            mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
+            const uint32_t dst = kv_s + slot * C::TILE_BYTES;
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
+                          c * 64, kvh, t.seq_start + kt * BN);
+          }
+        }
       }
-      if (ok) ok = load(&tm_v, n_kv - 1);
-      if (!ok) drain_loads<C::STAGES>(ctl, it, p.timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && t.valid;
+    }
+    if (lane == 0 && *abort_flag) {
+      // drain: wait (bounded) for the copies this thread issued
+      for (int b = 0; b < C::QB && b < q_loads; ++b) {
+        const int last = b + C::QB * ((q_loads - 1 - b) / C::QB);
+        wait_drain(ctl.bar(BAR_Q_FULL0 + b), (uint32_t)(last / C::QB) & 1u, p.timeout_ns);
+      }
+      for (int s = 0; s < C::STAGES && s < pos; ++s) {
+        const long long last = s + C::STAGES * ((pos - 1 - s) / C::STAGES);
+        wait_drain(ctl.bar(BAR_RING + s), (uint32_t)(last / C::STAGES) & 1u, p.timeout_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- QK^T issuer: S = Q K_j^T once the softmax warps have
-    // read S_{j-1}.  K_j sits at ring position 0 (j = 0) or 2j - 1, V_i at
-    // 2i + 2 (the last one at 2n - 1).  Without a separate PV issuer this
-    // thread also issues PV_{j-1} after QK_j.
+    // read the previous S.  Without a separate PV issuer this thread also
+    // issues PV_{j-1} right after QK_j.
     if (lane == 0) {
-      const uint32_t bar0 = ctl.bar(0);
       const uint64_t kdesc0 = smem_desc_sw128(kv_s, 16, 1024);
-      const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
-      bool ok = wait_bounded(bar0 + 8u * BAR_Q_FULL, 0, abort_flag, p.timeout_ns);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int pos = j == 0 ? 0 : 2 * j - 1;
-        const int slot = pos % C::STAGES;
-        if (j > 0 && !(ok = wait_bounded(bar0 + 8u * BAR_S_FREE, (uint32_t)(j - 1) & 1u,
-                                         abort_flag, p.timeout_ns)))
-          break;
-        if (!(ok = wait_bounded(bar0 + 8u * (BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u,
+      long long g = 0, base = 0;   // global key step, ring position of the tile's first load
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        TileInfo t;
+        if (!(ok = read_tile(ctl, k, t, abort_flag, p.timeout_ns, true)) || !t.valid) break;
+        const int qb = k % C::QB;
+        const uint64_t qdesc = smem_desc_sw128(q_s + qb * C::TILE_BYTES, 16, 1024);
+        if (!(ok = wait_bounded(ctl.bar(BAR_Q_FULL0 + qb), (uint32_t)(k / C::QB) & 1u,
                                 abort_flag, p.timeout_ns)))
           break;
-        tc_fence_after();
-        issue_qk<D>(tmem + C::COL_S, qdesc, desc_add(kdesc0, slot * C::TILE_BYTES));
-        tc_commit(bar0 + 8u * BAR_S_FULL);
-        tc_commit(bar0 + 8u * (BAR_RING + C::STAGES + slot));
-        if (!C::SPLIT_ISSUE && j > 0) ok = pv_step<D>(ctl, tmem, kv_s, j - 1, n_kv, abort_flag,
-                                                      p.timeout_ns);
+        for (int j = 0; ok && j < t.n_kv; ++j, ++g) {
+          const long long pos = pos_k(base, j);
+          const int slot = (int)(pos % C::STAGES);
+          if (g > 0 && !(ok = wait_bounded(ctl.bar(BAR_S_FREE), (uint32_t)(g - 1) & 1u,
+                                           abort_flag, p.timeout_ns)))
+            break;
+          if (!(ok = wait_bounded(ctl.bar(BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u,
+                                  abort_flag, p.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_qk<D>(tmem + C::COL_S, qdesc, desc_add(kdesc0, slot * C::TILE_BYTES));
+          tc_commit(ctl.bar(BAR_S_FULL));
+          tc_commit(ctl.bar(BAR_RING + C::STAGES + slot));
+          if (j == t.n_kv - 1) tc_commit(ctl.bar(BAR_Q_EMPTY0 + qb));   // Q buffer free
+          if (!C::SPLIT_ISSUE && j > 0) {
+            if (j == 1 && k > 0 &&   // the tile's first PV overwrites O
+                !(ok = wait_bounded(ctl.bar(BAR_O_FREE), (uint32_t)(k - 1) & 1u, abort_flag,
+                                    p.timeout_ns)))
+              break;
+            ok = pv_step<D>(ctl, tmem, kv_s, g - 1, j - 1, pos_v(base, j - 1, t.n_kv),
+                            abort_flag, p.timeout_ns);
+          }
+        }
+        if (!C::SPLIT_ISSUE && ok) {
+          if (t.n_kv == 1 && k > 0)
+            ok = wait_bounded(ctl.bar(BAR_O_FREE), (uint32_t)(k - 1) & 1u, abort_flag,
+                              p.timeout_ns);
+          if (ok)
+            ok = pv_step<D>(ctl, tmem, kv_s, g - 1, t.n_kv - 1, pos_v(base, t.n_kv - 1, t.n_kv),
+                            abort_flag, p.timeout_ns);
+        }
+        base += 2 * t.n_kv;
       }
-      if (!C::SPLIT_ISSUE && ok)
-        ok = pv_step<D>(ctl, tmem, kv_s, n_kv - 1, n_kv, abort_flag, p.timeout_ns);
-      tc_commit(bar0 + 8u * BAR_DRAIN_QK);   // no MMA may be in flight at teardown
-      wait_drain(bar0 + 8u * BAR_DRAIN_QK, 0, p.timeout_ns);
+      tc_commit(ctl.bar(BAR_DRAIN_QK));   // no MMA may be in flight at teardown
+      wait_drain(ctl.bar(BAR_DRAIN_QK), 0, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 6) {
     // ---------------- PV issuer: O (+)= P_i V_i once the softmax warps have
-    // written P_i.
+    // written P_i; a tile's first PV also waits until the epilogue of the
+    // previous tile has read O.
     if (C::SPLIT_ISSUE && lane == 0) {
-      const uint32_t bar0 = ctl.bar(0);
+      long long g = 0, base = 0;
       bool ok = true;
-      for (int i = 0; ok && i < n_kv; ++i)
-        ok = pv_step<D>(ctl, tmem, kv_s, i, n_kv, abort_flag, p.timeout_ns);
-      tc_commit(bar0 + 8u * BAR_DRAIN_PV);
-      wait_drain(bar0 + 8u * BAR_DRAIN_PV, 0, p.timeout_ns);
+      for (int k = 0; ok; ++k) {
+        TileInfo t;
+        if (!(ok = read_tile(ctl, k, t, abort_flag, p.timeout_ns, true)) || !t.valid) break;
+        for (int i = 0; ok && i < t.n_kv; ++i, ++g) {
+          if (i == 0 && k > 0 &&
+              !(ok = wait_bounded(ctl.bar(BAR_O_FREE), (uint32_t)(k - 1) & 1u, abort_flag,
+                                  p.timeout_ns)))
+            break;
+          ok = pv_step<D>(ctl, tmem, kv_s, g, i, pos_v(base, i, t.n_kv), abort_flag,
+                          p.timeout_ns);
+        }
+        base += 2 * t.n_kv;
+      }
+      tc_commit(ctl.bar(BAR_DRAIN_PV));
+      wait_drain(ctl.bar(BAR_DRAIN_PV), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ---------------- softmax warpgroup
+  } else {
+    // ---------------- softmax warpgroup (warps 2-5)
     const int wq = warp & 3;                        // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int q_idx = qt * BM + row;                // row within the sequence
     const float c = p.scale_log2;
-    RowState st{-INFINITY, 0.f, 0.f};
+    long long g = 0;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)j & 1u, abort_flag, p.timeout_ns);
+    for (int k = 0; ok; ++k) {
+      TileInfo t;
+      ok = __all_sync(0xffffffffu, read_tile(ctl, k, t, abort_flag, p.timeout_ns, false));
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(BAR_INFO_EMPTY0 + k % INFO_SLOTS));
+      if (!t.valid) break;
+      const int q_idx = t.qt * BM + row;            // row within the sequence
+      RowState st{-INFINITY, 0.f, 0.f};
+      for (int j = 0; j < t.n_kv; ++j, ++g) {
+        ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)g & 1u, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        float s[BN];
+        load_scores(tmem + lane_off + C::COL_S, s);
+        tc_fence_before();
+        mbar_arrive(ctl.bar(BAR_S_FREE));   // S may now take the next scores
+        const int kv0 = j * BN;
+        if ((kv0 + BN > t.len) || (p.causal && kv0 + BN - 1 > t.qt * BM))
+          mask_scores(s, kv0, p.causal ? min(t.len, q_idx + 1) : t.len);
+        const int pb = (int)(g & 1);
+        if (g >= 2) {   // P buffer pb was last read by PV_{g-2}
+          ok = wait_warp(ctl.bar(BAR_PV_DONE0 + pb), (uint32_t)((g - 2) >> 1) & 1u, abort_flag,
+                         p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        bool moved;
+        const float alpha =
+            softmax_tile(s, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)pb, moved);
+        if (__any_sync(0xffffffffu, moved && j > 0)) {   // rescale O after PV_{g-1} landed
+          ok = wait_warp(ctl.bar(BAR_PV_DONE0 + (pb ^ 1)), (uint32_t)((g - 1) >> 1) & 1u,
+                         abort_flag, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          rescale_o<D>(tmem + lane_off + C::COL_O, alpha);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ctl.bar(BAR_P_FULL0 + pb));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, LSE; then O is free for the next tile
+      const long long gl = g - 1;   // the tile's last key step
+      ok = wait_warp(ctl.bar(BAR_PV_DONE0 + (int)(gl & 1)), (uint32_t)(gl >> 1) & 1u, abort_flag,
+                     p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
-      float s[BN];
-      load_scores(tmem + lane_off + C::COL_S, s);
-      tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_S_FREE));   // S may now take the scores of tile j + 1
-      const int kv0 = j * BN;
-      if ((kv0 + BN > len) || (p.causal && kv0 + BN - 1 > qt * BM))
-        mask_scores(s, kv0, p.causal ? min(len, q_idx + 1) : len);
-      if (j >= 2) {   // P buffer j&1 was last read by PV_{j-2}
-        ok = wait_warp(ctl.bar(BAR_PV_DONE0 + (j & 1)), (uint32_t)((j - 2) >> 1) & 1u,
-                       abort_flag, p.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      bool moved;
-      const float alpha =
-          softmax_tile(s, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)(j & 1), moved);
-      if (__any_sync(0xffffffffu, moved && j > 0)) {   // rescale O after PV_{j-1} landed
-        ok = wait_warp(ctl.bar(BAR_PV_DONE0 + ((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1u,
-                       abort_flag, p.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-        rescale_o<D>(tmem + lane_off + C::COL_O, alpha);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_P_FULL0 + (j & 1)));
-    }
-    if (ok)
-      ok = wait_warp(ctl.bar(BAR_PV_DONE0 + ((n_kv - 1) & 1)), (uint32_t)((n_kv - 1) >> 1) & 1u,
-                     abort_flag, p.timeout_ns);
-    if (ok) {
-      tc_fence_after();
-      const bool live = q_idx < len;
+      const bool live = q_idx < t.len;
       store_row<D>(tmem + lane_off + C::COL_O, st.lr > 0.f ? 1.f / st.lr : 0.f,
-                   p.o + ((long long)(seq_start + q_idx) * p.Hq + h) * (long long)D, live);
-      if (live) p.lse[lse_base + q_idx] = row_lse(st, p.scale);
+                   p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D, live);
+      if (live) p.lse[t.lse_base + q_idx] = row_lse(st, p.scale);
+      tc_fence_before();
+      mbar_arrive(ctl.bar(BAR_O_FREE));
     }
   }
 
@@ -863,6 +976,8 @@ static bool opt_in_smem(K kernel, uint32_t bytes) {
 
 // Per device: compute capability check and the shared-memory opt-in of the
 // kernel instantiations, done once.
+static int g_sm_count[MAX_DEVICES];
+
 static attn_status prepare_device(int dev) {
   static std::mutex mu;
   static signed char state[MAX_DEVICES];   // 0 unknown, 1 ready, -1 unsupported
@@ -878,6 +993,10 @@ static attn_status prepare_device(int dev) {
     state[dev] = -1;
     return ATTN_ERR_UNSUPPORTED_DEVICE;
   }
+  if (cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess ||
+      g_sm_count[dev] < 1)
+    return ATTN_ERR_CUDA;
   if (!opt_in_smem(attn_fwd_kernel<64>, Cfg<64>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<128>, Cfg<128>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<256>, Cfg<256>::SMEM_BYTES))
@@ -945,11 +1064,16 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
 
-  // fixed batch: exactly the units; packed: an upper bound on them
-  // (sum_s ceil(L_s/U) <= T/U + B), surplus CTAs exit at once.
-  const long long units = cu_seqlens ? (long long)p.num_units + B : (long long)p.num_units * B;
-  const long long grid = units * Hq;
-  if (grid > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  // Persistent grid: one CTA per SM (at most one per work unit).  Fixed
+  // batch: exactly num_units * B * Hq units; packed: an upper bound
+  // (sum_s ceil(L_s/U) <= T/U + B, times Hq) -- the tile decoder marks the
+  // surplus invalid.
+  const long long units =
+      (cu_seqlens ? (long long)p.num_units + B : (long long)p.num_units * B) * Hq;
+  if (units > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  // One CTA per tile when there are at most two tiles per SM (the hardware
+  // scheduler balances small grids better than fixed rounds).
+  const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
 
   switch (d) {
     case 64:
