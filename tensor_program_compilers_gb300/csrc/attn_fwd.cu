@@ -16,10 +16,10 @@
 // softmax" and "FlashAttention forward"), in the block order of the TileLang
 // explainer's loop (ai.thesatyajit.com/articles/tilelang, "FlashAttention,
 // in tiles").  Two liberties, both exact in real arithmetic:
-//  * the running max m is only moved when the tile max exceeds it by more
-//    than 16 (base-2 units): softmax is shift invariant (tang, section 6), so
-//    any reference value works as long as O and l share it and the
-//    exponentials stay in range (they are <= 2^16 here);
+//  * the running max m is only moved when the exponentials against it would
+//    leave range (a half-row sum above 2^16): softmax is shift invariant
+//    (tang, section 6), so any reference value works as long as O and l share
+//    it and the exponentials stay in range (each P <= 2^16 here);
 //  * masked keys read -inf, the identity of max (tang, section 2.1, guarded
 //    views), so fully masked tiles are skipped rather than computed.
 //
@@ -60,12 +60,40 @@
 
 namespace attn {
 
+// Diagnostic timeline (compiled in only with -DATTN_TRACE): clock() stamps of
+// pipeline events of up to four chosen CTAs, read back with
+// attn_trace_read().  Without the macro the hooks compile to nothing.
+#ifdef ATTN_TRACE
+constexpr int TRACE_CTAS = 4, TRACE_ROLES = 5, TRACE_STEPS = 64, TRACE_EVENTS = 4;
+__device__ unsigned g_trace[TRACE_CTAS][TRACE_ROLES][TRACE_STEPS][TRACE_EVENTS];
+__device__ int g_trace_cta[TRACE_CTAS] = {-1, -1, -1, -1};
+__device__ __forceinline__ int trace_slot() {
+  for (int i = 0; i < TRACE_CTAS; ++i)
+    if ((int)blockIdx.x == g_trace_cta[i]) return i;
+  return -1;
+}
+__device__ __forceinline__ void trace_ev(int slot, int role, long long step, int ev) {
+  if (slot >= 0 && step >= 0 && step < TRACE_STEPS) {
+    unsigned c;
+    asm volatile("mov.u32 %0, %%clock;" : "=r"(c));
+    g_trace[slot][role][step][ev] = c;
+  }
+}
+#define ATTN_TRACE_SLOT() trace_slot()
+#define ATTN_TRACE_EV(role, step, ev) trace_ev(tslot, role, step, ev)
+#else
+#define ATTN_TRACE_SLOT() (-1)
+#define ATTN_TRACE_EV(role, step, ev) ((void)tslot)
+#endif
+
 constexpr int BM = 128;            // query rows per tile (one per TMEM lane)
 constexpr int BN = 128;            // keys per tile
-constexpr int THREADS = 224;
+constexpr int THREADS = 352;   // 11 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t CHUNK_BYTES = 128 * 128;   // 128 rows x 64 bf16, one swizzle column
-constexpr float RESCALE_THRESHOLD = 16.0f;    // log2 units: P <= 2^16 between moves
+// The reference max of a row moves only when a half-row's sum of P exceeds
+// this (so every stored P is <= 2^16) or is not finite.
+constexpr float P_SUM_LIMIT = 65536.0f;
 
 template <int D>
 struct Cfg {
@@ -80,7 +108,7 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = TILE_BYTES * QB;
   static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
-  static constexpr uint32_t CTL_BYTES = 1024;
+  static constexpr uint32_t CTL_BYTES = 2048;
   static constexpr uint32_t SMEM_BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_P0 = 128;
@@ -108,10 +136,14 @@ enum : int {
   BAR_INFO_EMPTY0 = BAR_INFO_FULL0 + 4,   // tile-info entry e consumed
   BAR_DRAIN_QK = BAR_INFO_EMPTY0 + 4,     // abort drain of each issuer
   BAR_DRAIN_PV,
-  BAR_RING           // K/V ring: full[0..STAGES), then empty[0..STAGES)
+  BAR_PAIR0,         // softmax pair of TMEM lane quarter q, q < 4
+  BAR_PAIR_END = BAR_PAIR0 + 4,
+  BAR_RING = BAR_PAIR_END   // K/V ring: full[0..STAGES), then empty[0..STAGES)
 };
 constexpr int INFO_SLOTS = 4;
 constexpr int INFO_INTS = 8;
+constexpr int SOFTMAX_WARP0 = 2, SOFTMAX_WARPS = 8;
+constexpr int WARP_PV = SOFTMAX_WARP0 + SOFTMAX_WARPS;   // 10
 
 struct Params {
   const __nv_bfloat16 *q;
@@ -157,6 +189,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile uint32_t *abort_flag,
                                              unsigned long long timeout_ns) {
   return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, timeout_ns);
+}
+
+// One arrival per warp (count barriers in warps): after every lane's prior
+// work (each lane fenced its tcgen05 operations before this point).
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // Warp-uniform bounded wait for the softmax warps: the tcgen05.ld/st that
@@ -315,83 +354,55 @@ __device__ Tile decode_tile(const Params &p, long long idx) {
 }
 
 // ---------------------------------------------------------------- softmax pieces
-// This thread's 128 fp32 scores (TMEM columns col..col+127 of its lane).
-__device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[BN]) {
-  uint32_t a[32], b[32], c[32], d[32];
+// Two softmax warps share each TMEM lane quarter: for a query row, the thread
+// of the first warp handles keys 0..63 of the key tile and the thread of the
+// second keys 64..127 ("halves").  They keep one reference max per row.
+constexpr int HB = BN / 2;   // keys per softmax thread
+
+// This thread's 64 scores (TMEM columns col..col+63 of its lane).
+__device__ __forceinline__ void load_half(uint32_t taddr, float (&h)[HB]) {
+  uint32_t a[32], b[32];
   tmem_ld32(taddr, a);
   tmem_ld32(taddr + 32, b);
-  tmem_ld32(taddr + 64, c);
-  tmem_ld32(taddr + 96, d);
   tmem_wait_ld();
   reg_fence32(a);
   reg_fence32(b);
-  reg_fence32(c);
-  reg_fence32(d);
 #pragma unroll
   for (int x = 0; x < 32; ++x) {
-    s[x] = __uint_as_float(a[x]);
-    s[32 + x] = __uint_as_float(b[x]);
-    s[64 + x] = __uint_as_float(c[x]);
-    s[96 + x] = __uint_as_float(d[x]);
+    h[x] = __uint_as_float(a[x]);
+    h[32 + x] = __uint_as_float(b[x]);
   }
 }
 
-// Keys kv0 + x >= lim are invisible: they read -inf, the identity of max.
-__device__ __forceinline__ void mask_scores(float (&s)[BN], int kv0, int lim) {
+// Keys key0 + x >= lim are invisible: they read -inf, the identity of max.
+__device__ __forceinline__ void mask_half(float (&h)[HB], int key0, int lim) {
 #pragma unroll
-  for (int x = 0; x < BN; ++x)
-    if (kv0 + x >= lim) s[x] = -INFINITY;
+  for (int x = 0; x < HB; ++x)
+    if (key0 + x >= lim) h[x] = -INFINITY;
 }
 
-// Row maximum as eight independent chains of 3-input max (short dependency
-// chains: one warp per sub-partition has to hide the latency itself).
-__device__ __forceinline__ float row_max(const float (&s)[BN]) {
-  float mk[8];
+// Maximum of 64 scores: four independent chains of 3-input max.
+__device__ __forceinline__ float max_half(const float (&h)[HB]) {
+  float mk[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float m = max3f(s[k], s[k + 8], s[k + 16]);
+  for (int k = 0; k < 4; ++k) {
+    float m = max3f(h[k], h[k + 4], h[k + 8]);
 #pragma unroll
-    for (int i = 3; i + 1 < 16; i += 2) m = max3f(m, s[k + 8 * i], s[k + 8 * (i + 1)]);
-    mk[k] = fmaxf(m, s[k + 8 * 15]);
+    for (int i = 3; i + 1 < 16; i += 2) m = max3f(m, h[k + 4 * i], h[k + 4 * (i + 1)]);
+    mk[k] = fmaxf(m, h[k + 4 * 15]);
   }
-  return fmaxf(max3f(mk[0], mk[1], mk[2]), max3f(mk[3], mk[4], max3f(mk[5], mk[6], mk[7])));
+  return fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
 }
 
-// Online-softmax state of one row: reference max (raw score units), the
-// running sum of 2^((s - m) * c) (for the LSE) and the running sum of the
-// same weights rounded to bf16 as the P.V product uses them (for O / l: a
-// row dominated by one key then returns that key's value exactly).
-struct RowState {
-  float m;
-  float l;
-  float lr;
-};
-
-// Folds a tile maximum into the state.  Returns the factor the row's O
-// accumulator must be multiplied by (1 when the reference max stays).
-__device__ __forceinline__ float fold_max(RowState &st, float tile_max, float c, bool &moved) {
-  const float m_new = fmaxf(st.m, tile_max);
-  moved = (st.m == -INFINITY) ? (m_new != -INFINITY)
-                              : ((m_new - st.m) * c > RESCALE_THRESHOLD);
-  float alpha = 1.f;
-  if (moved) {
-    alpha = (st.m == -INFINITY) ? 0.f : ex2_approx((st.m - m_new) * c);
-    st.m = m_new;
-    st.l *= alpha;
-    st.lr *= alpha;
-  }
-  return alpha;
-}
-
-// p = 2^(s*c - m*c) for 64 scores s[BASE..BASE+63]: bf16 pairs into pk,
-// fp32 sums into acc (four packed accumulators).
-template <int BASE>
-__device__ __forceinline__ void exp_chunk(const float (&s)[BN], uint64_t c2, uint64_t nm2,
-                                          uint32_t (&pk)[32], uint64_t (&acc)[4],
-                                          uint64_t (&accr)[4]) {
+// p = 2^(h*c - m*c) for 64 scores: bf16 pairs into pk; sums of the fp32
+// values into acc and of the bf16-rounded values into accr (four packed
+// accumulators each).
+__device__ __forceinline__ void exp_half(const float (&h)[HB], uint64_t c2, uint64_t nm2,
+                                         uint32_t (&pk)[HB / 2], uint64_t (&acc)[4],
+                                         uint64_t (&accr)[4]) {
 #pragma unroll
-  for (int x = 0; x < 64; x += 2) {
-    const uint64_t a = f2_fma(f2_pack(s[BASE + x], s[BASE + x + 1]), c2, nm2);
+  for (int x = 0; x < HB; x += 2) {
+    const uint64_t a = f2_fma(f2_pack(h[x], h[x + 1]), c2, nm2);
     float a0, a1;
     f2_unpack(a, a0, a1);
     const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
@@ -403,89 +414,166 @@ __device__ __forceinline__ void exp_chunk(const float (&s)[BN], uint64_t c2, uin
   }
 }
 
-// exp_chunk that also tracks the running maximum of the raw scores (four
-// partial maxima, combined by the caller).
-template <int BASE>
-__device__ __forceinline__ void exp_chunk_track(const float (&s)[BN], uint64_t c2, uint64_t nm2,
-                                                uint32_t (&pk)[32], uint64_t (&acc)[4],
-                                                uint64_t (&accr)[4], float (&mx)[4]) {
-#pragma unroll
-  for (int x = 0; x < 64; x += 2) {
-    const uint64_t a = f2_fma(f2_pack(s[BASE + x], s[BASE + x + 1]), c2, nm2);
-    float a0, a1;
-    f2_unpack(a, a0, a1);
-    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
-    const uint32_t w = pack_bf16x2(e0, e1);
-    pk[x >> 1] = w;
-    acc[(x >> 1) & 3] = f2_add(acc[(x >> 1) & 3], f2_pack(e0, e1));
-    accr[(x >> 1) & 3] = f2_add(accr[(x >> 1) & 3], bf16x2_widen(w));
-    mx[(x >> 1) & 3] = max3f(mx[(x >> 1) & 3], s[BASE + x], s[BASE + x + 1]);
-  }
-}
-
-__device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]);
-
-// One key tile of this thread's row (warp-collective: TMEM stores).  Writes
-// P = 2^(s*c - m*c) as bf16 pairs to TMEM columns p_addr .. p_addr+63,
-// folds the tile into the row state and returns the factor the row's O must
-// be multiplied by (1 unless the reference max moved; `moved` says which).
-//
-// Once a row has a reference max, the exponentials are taken against it in
-// the same pass that finds the tile maximum; the tile is redone with a new
-// reference only when its maximum passes the old one by more than the
-// threshold (for some lane of the warp).  Rows without a reference (the first
-// tile) take the maximum first.  Either way the stored P and the sum share one
-// reference, which is all that shift invariance requires.
-__device__ __forceinline__ float softmax_tile(const float (&s)[BN], RowState &st, float c,
-                                              uint32_t p_addr, bool &moved) {
-  const uint64_t c2 = f2_pack(c, c);
-  uint64_t acc[4] = {0, 0, 0, 0}, accr[4] = {0, 0, 0, 0};
-  uint32_t pk[32];
-  float alpha = 1.f;
-  moved = false;
-  const bool have_ref = __all_sync(0xffffffffu, st.m != -INFINITY);
-  bool redo = !have_ref;
-  if (have_ref) {
-    const float neg_mc = -st.m * c;
-    const uint64_t nm2 = f2_pack(neg_mc, neg_mc);
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    exp_chunk_track<0>(s, c2, nm2, pk, acc, accr, mx);
-    tmem_st32(p_addr, pk);
-    exp_chunk_track<64>(s, c2, nm2, pk, acc, accr, mx);
-    tmem_st32(p_addr + 32, pk);
-    alpha = fold_max(st, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), c, moved);
-    redo = __any_sync(0xffffffffu, moved);
-  } else {
-    alpha = fold_max(st, row_max(s), c, moved);
-  }
-  if (redo) {   // first tile, or the reference moved: P against the final reference
-    const float neg_mc = (st.m == -INFINITY) ? 0.f : -st.m * c;
-    const uint64_t nm2 = f2_pack(neg_mc, neg_mc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = accr[i] = 0;
-    exp_chunk<0>(s, c2, nm2, pk, acc, accr);
-    tmem_st32(p_addr, pk);
-    exp_chunk<64>(s, c2, nm2, pk, acc, accr);
-    tmem_st32(p_addr + 32, pk);
-  }
-  st.l += sum_acc(acc);
-  st.lr += sum_acc(accr);
-  return alpha;
-}
-
 __device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]) {
   float a, b;
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a, b);
   return a + b;
 }
 
-// O row *= alpha (TMEM columns taddr .. taddr+D-1 of this lane).  The caller
-// issues tcgen05.wait::st before publishing.
-template <int D>
+// Online-softmax state of one half-row: the row's reference max (raw score
+// units, shared by both halves), the running sum of 2^((s - m) * c) over this
+// half's keys (for the LSE) and the running sum of the same weights rounded
+// to bf16 as the P.V product uses them (for O / l: a row dominated by one key
+// then returns that key's value exactly).
+struct RowState {
+  float m;
+  float l;
+  float lr;
+};
+
+// The pair of softmax warps that share a TMEM lane quarter synchronise on an
+// mbarrier of their own (one arrival per warp per round, bounded waits) and exchange
+// values through shared memory.  Both warps run the same sequence of rounds,
+// so `round` counts identically on both sides.
+struct Pair {
+  int wq, half, lane;
+  uint32_t bar;          // this pair's mbarrier
+  volatile float *xv;    // [4 quarters][2 halves][32 lanes] row values
+  volatile int *xf;      // [2 buffers][4 quarters][2 halves] per-warp flags
+  uint32_t round;
+  volatile uint32_t *abort_flag;
+  unsigned long long timeout_ns;
+  __device__ bool sync() {
+    warp_arrive(bar);
+    const bool ok = wait_bounded(bar, round & 1u, abort_flag, timeout_ns);
+    ++round;
+    return __all_sync(0xffffffffu, ok);
+  }
+  // The partner's value of v for this row (two rounds: the slot is reused).
+  __device__ bool exchange(float v, float &o) {
+    xv[(wq * 2 + half) * 32 + lane] = v;
+    if (!sync()) return false;
+    o = xv[(wq * 2 + (half ^ 1)) * 32 + lane];
+    return sync();
+  }
+  // OR of a warp-uniform flag over the pair, in one round split in two so
+  // that other work can overlap the round trip: post() publishes the flag and
+  // arrives, collect() waits and reads the partner's.  Flags are
+  // double-buffered by round parity; a buffer is rewritten only after the
+  // partner has finished the next round, i.e. has read it.
+  __device__ void post(bool f) {
+    if (lane == 0) xf[((round & 1u) * 4 + wq) * 2 + half] = f ? 1 : 0;
+    warp_arrive(bar);
+  }
+  __device__ bool collect(bool f, bool &any) {
+    const bool ok =
+        __all_sync(0xffffffffu, wait_bounded(bar, round & 1u, abort_flag, timeout_ns));
+    any = f || xf[((round & 1u) * 4 + wq) * 2 + (half ^ 1)] != 0;
+    ++round;
+    return ok;
+  }
+};
+
+template <int NCOLS>
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha);
+
+// Barrier addresses and parities one softmax step needs.
+struct StepBars {
+  uint32_t p_full;       // P_b written (this step)
+  uint32_t pbuf_done;    // PV that last read P_b (step g-2) completed
+  uint32_t pbuf_parity;
+  uint32_t prev_done;    // PV of step g-1 completed (before rescaling O)
+  uint32_t prev_parity;
+  uint32_t s_full;       // S of the next step written
+  uint32_t s_next_parity;
+};
+
+// One key tile of this thread's half-row, after its scores h are in
+// registers (warp-collective: TMEM stores).  Writes P = 2^(s*c - m*c) as
+// bf16 pairs to TMEM columns p_addr .. +31, rescales this half's O columns
+// when the reference moves, and publishes P (P_FULL).  Returns false on a
+// failed wait.  s_next_ready: a non-blocking early test of the next step's
+// scores, to be used by the caller (valid if test_next).
+//
+// With a reference in place, the exponentials are taken against it straight
+// away and stored; the pair moves the reference -- to the row maximum over
+// both halves -- and redoes the tile only if some half-row's sum exceeds
+// P_SUM_LIMIT (so every stored P is <= 2^16) or is not finite.  The first
+// tile of a row takes the maximum first.  Either way P and both running sums
+// share one reference, which is all that shift invariance requires.  The
+// waits whose conditions usually hold already are tested early and collected
+// late, so their shared-memory round trips overlap other work.
+template <int OC>
+__device__ __forceinline__ bool softmax_step(const float (&h)[HB], RowState &st, float c,
+                                             uint32_t p_addr, uint32_t o_addr, Pair &pr,
+                                             const StepBars &sb, bool check_pbuf, bool rescale_ok,
+                                             bool test_next, bool &s_next_ready,
+                                             volatile uint32_t *abort_flag,
+                                             unsigned long long timeout_ns) {
+  const bool pbuf_early = !check_pbuf || mbar_test_wait(sb.pbuf_done, sb.pbuf_parity);
+  const uint64_t c2 = f2_pack(c, c);
+  uint64_t acc[4] = {0, 0, 0, 0}, accr[4] = {0, 0, 0, 0};
+  uint32_t pk[HB / 2];
+  // identical across the pair (same rows, same reference) and voted warp-wide
+  const bool have_ref = __all_sync(0xffffffffu, st.m != -INFINITY);
+  float sum = 0.f;
+  if (have_ref) {
+    const float neg_mc = -st.m * c;
+    exp_half(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
+    sum = sum_acc(acc);
+  }
+  const bool want = __any_sync(0xffffffffu, !have_ref || !(sum <= P_SUM_LIMIT));
+  pr.post(want);
+  // the P buffer must be free (its previous PV done) before it is written
+  if (!__all_sync(0xffffffffu, pbuf_early) &&
+      !wait_warp(sb.pbuf_done, sb.pbuf_parity, abort_flag, timeout_ns))
+    return false;
+  tc_fence_after();
+  if (have_ref) tmem_st32(p_addr, pk);   // optimistic; rewritten on a redo
+  s_next_ready = test_next && mbar_test_wait(sb.s_full, sb.s_next_parity);
+  bool redo;
+  if (!pr.collect(want, redo)) return false;
+  float alpha = 1.f;
+  bool moved = false;
+  if (redo) {   // first tile, or the reference must move: take the row maximum
+    const float hmax = max_half(h);
+    float other;
+    if (!pr.exchange(hmax, other)) return false;
+    const float m_new = fmaxf(st.m, fmaxf(hmax, other));
+    if (m_new != st.m) {
+      alpha = (st.m == -INFINITY) ? 0.f : ex2_approx((st.m - m_new) * c);
+      st.m = m_new;
+      st.l *= alpha;
+      st.lr *= alpha;
+      moved = true;
+    }
+    const float neg_mc = (st.m == -INFINITY) ? 0.f : -st.m * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = accr[i] = 0;
+    exp_half(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
+    tmem_st32(p_addr, pk);
+    sum = sum_acc(acc);
+  }
+  st.l += sum;
+  st.lr += sum_acc(accr);
+  if (__any_sync(0xffffffffu, moved && rescale_ok)) {   // rescale O after PV_{g-1} landed
+    if (!wait_warp(sb.prev_done, sb.prev_parity, abort_flag, timeout_ns)) return false;
+    tc_fence_after();
+    rescale_o<OC>(o_addr, alpha);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  warp_arrive(sb.p_full);
+  return true;
+}
+
+// O[cols] *= alpha for NCOLS columns of this lane starting at taddr.  The
+// caller issues tcgen05.wait::st before publishing.
+template <int NCOLS>
 __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
   const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-  for (int cc = 0; cc < D; cc += 32) {
+  for (int cc = 0; cc < NCOLS; cc += 32) {
     uint32_t o[32];
     tmem_ld32(taddr + cc, o);
     tmem_wait_ld();
@@ -501,13 +589,14 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha) {
   }
 }
 
-// Epilogue of one row: O / l -> bf16, 16-byte stores of the row (if live).
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t taddr, float inv_l, __nv_bfloat16 *orow,
-                                          bool live) {
+// Epilogue of NCOLS columns of one row: O / l -> bf16, 16-byte stores to orow
+// (if live).
+template <int NCOLS>
+__device__ __forceinline__ void store_cols(uint32_t taddr, float inv_l, __nv_bfloat16 *orow,
+                                           bool live) {
   const uint64_t s2 = f2_pack(inv_l, inv_l);
 #pragma unroll 1
-  for (int cc = 0; cc < D; cc += 32) {
+  for (int cc = 0; cc < NCOLS; cc += 32) {
     uint32_t o[32];
     tmem_ld32(taddr + cc, o);
     tmem_wait_ld();
@@ -527,11 +616,6 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float inv_l, __nv_bflo
         dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
     }
   }
-}
-
-__device__ __forceinline__ float row_lse(const RowState &st, float scale) {
-  const float m_use = (st.m == -INFINITY) ? 0.f : st.m;
-  return st.l > 0.f ? m_use * scale + logf(st.l) : -INFINITY;
 }
 
 // One 128x128xd QK^T into TMEM: A = Q tile (qdesc), B = K tile (kdesc), both
@@ -566,6 +650,8 @@ struct Ctl {
   uint32_t bar0;       // shared address of barrier 0 (barriers are 8 bytes apart)
   uint32_t *words;     // [0] TMEM base, [1] abort flag
   int *info;           // INFO_SLOTS entries of INFO_INTS ints
+  float *xv;           // softmax pair exchange: 4 x 2 x 32 floats
+  int *xf;             // softmax pair flags: 2 x 4 x 2 ints
   __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
 };
 
@@ -574,18 +660,19 @@ __device__ __forceinline__ void init_barriers(const Ctl &c, uint32_t info_consum
   for (int b = 0; b < 2; ++b) {
     mbar_init(c.bar(BAR_Q_FULL0 + b), 1);
     mbar_init(c.bar(BAR_Q_EMPTY0 + b), 1);
-    mbar_init(c.bar(BAR_P_FULL0 + b), 4 * 32);
+    mbar_init(c.bar(BAR_P_FULL0 + b), SOFTMAX_WARPS);
     mbar_init(c.bar(BAR_PV_DONE0 + b), 1);
   }
   mbar_init(c.bar(BAR_S_FULL), 1);
-  mbar_init(c.bar(BAR_S_FREE), 4 * 32);
-  mbar_init(c.bar(BAR_O_FREE), 4 * 32);
+  mbar_init(c.bar(BAR_S_FREE), SOFTMAX_WARPS);
+  mbar_init(c.bar(BAR_O_FREE), SOFTMAX_WARPS);
   for (int e = 0; e < INFO_SLOTS; ++e) {
     mbar_init(c.bar(BAR_INFO_FULL0 + e), 1);
     mbar_init(c.bar(BAR_INFO_EMPTY0 + e), info_consumers);
   }
   mbar_init(c.bar(BAR_DRAIN_QK), 1);
   mbar_init(c.bar(BAR_DRAIN_PV), 1);
+  for (int q = 0; q < 4; ++q) mbar_init(c.bar(BAR_PAIR0 + q), 2);
   for (int s = 0; s < STAGES; ++s) {
     mbar_init(c.bar(BAR_RING + s), 1);
     mbar_init(c.bar(BAR_RING + STAGES + s), 1);
@@ -627,19 +714,23 @@ __device__ __forceinline__ bool read_tile(const Ctl &c, int k, TileInfo &t,
 template <int D>
 __device__ __forceinline__ bool pv_step(const Ctl &ctl, uint32_t tmem, uint32_t kv_s, long long g,
                                         int i, long long pos, volatile uint32_t *abort_flag,
-                                        unsigned long long timeout_ns) {
+                                        unsigned long long timeout_ns, int tslot) {
   using C = Cfg<D>;
   const int slot = (int)(pos % C::STAGES);
   const int pb = (int)(g & 1);
-  if (!wait_bounded(ctl.bar(BAR_P_FULL0 + pb), (uint32_t)(g >> 1) & 1u, abort_flag, timeout_ns) ||
-      !wait_bounded(ctl.bar(BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u, abort_flag,
+  if (!wait_bounded(ctl.bar(BAR_P_FULL0 + pb), (uint32_t)(g >> 1) & 1u, abort_flag, timeout_ns))
+    return false;
+  ATTN_TRACE_EV(1, g, 0);
+  if (!wait_bounded(ctl.bar(BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u, abort_flag,
                     timeout_ns))
     return false;
+  ATTN_TRACE_EV(1, g, 1);
   tc_fence_after();
   issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)pb,
               desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES), i > 0);
   tc_commit(ctl.bar(BAR_PV_DONE0 + pb));
   tc_commit(ctl.bar(BAR_RING + C::STAGES + slot));
+  ATTN_TRACE_EV(1, g, 2);
   return true;
 }
 
@@ -672,11 +763,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   ctl.bar0 = smem_u32(bars);
   ctl.words = reinterpret_cast<uint32_t *>(bars + BAR_RING + 2 * C::STAGES);
   ctl.info = reinterpret_cast<int *>(ctl.words + 4);
+  ctl.xv = reinterpret_cast<float *>(ctl.info + INFO_SLOTS * INFO_INTS);
+  ctl.xf = reinterpret_cast<int *>(ctl.xv + 4 * 2 * 32);
   volatile uint32_t *abort_flag = ctl.words + 1;
   const uint32_t q_s = base_s + C::OFF_Q;
   const uint32_t kv_s = base_s + C::OFF_KV;
-  // consumers of each tile-info entry: QK issuer, PV issuer, 4 softmax warps
-  constexpr uint32_t INFO_CONSUMERS = C::SPLIT_ISSUE ? 6 : 5;
+  const int tslot = ATTN_TRACE_SLOT();   // -1 unless built for tracing
+  // consumers of each tile-info entry: QK issuer, PV issuer, the softmax warps
+  constexpr uint32_t INFO_CONSUMERS = (C::SPLIT_ISSUE ? 2 : 1) + SOFTMAX_WARPS;
 
   if (warp == 1) {
     if (lane == 0) init_barriers<C::STAGES>(ctl, INFO_CONSUMERS);
@@ -747,6 +841,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool is_v = last || (item > 0 && (item & 1) == 0);
             const int kt = last ? n - 1 : (item == 0 ? 0 : (is_v ? item / 2 - 1 : (item + 1) / 2));
             mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
+            ATTN_TRACE_EV(4, pos >> 2, (int)(pos & 3));
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
@@ -790,12 +885,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (g > 0 && !(ok = wait_bounded(ctl.bar(BAR_S_FREE), (uint32_t)(g - 1) & 1u,
                                            abort_flag, p.timeout_ns)))
             break;
+          ATTN_TRACE_EV(0, g, 0);
           if (!(ok = wait_bounded(ctl.bar(BAR_RING + slot), (uint32_t)(pos / C::STAGES) & 1u,
                                   abort_flag, p.timeout_ns)))
             break;
+          ATTN_TRACE_EV(0, g, 1);
           tc_fence_after();
           issue_qk<D>(tmem + C::COL_S, qdesc, desc_add(kdesc0, slot * C::TILE_BYTES));
           tc_commit(ctl.bar(BAR_S_FULL));
+          ATTN_TRACE_EV(0, g, 2);
           tc_commit(ctl.bar(BAR_RING + C::STAGES + slot));
           if (j == t.n_kv - 1) tc_commit(ctl.bar(BAR_Q_EMPTY0 + qb));   // Q buffer free
           if (!C::SPLIT_ISSUE && j > 0) {
@@ -804,7 +902,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     p.timeout_ns)))
               break;
             ok = pv_step<D>(ctl, tmem, kv_s, g - 1, j - 1, pos_v(base, j - 1, t.n_kv),
-                            abort_flag, p.timeout_ns);
+                            abort_flag, p.timeout_ns, tslot);
           }
         }
         if (!C::SPLIT_ISSUE && ok) {
@@ -813,7 +911,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                               p.timeout_ns);
           if (ok)
             ok = pv_step<D>(ctl, tmem, kv_s, g - 1, t.n_kv - 1, pos_v(base, t.n_kv - 1, t.n_kv),
-                            abort_flag, p.timeout_ns);
+                            abort_flag, p.timeout_ns, tslot);
         }
         base += 2 * t.n_kv;
       }
@@ -821,7 +919,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       wait_drain(ctl.bar(BAR_DRAIN_QK), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == WARP_PV) {
     // ---------------- PV issuer: O (+)= P_i V_i once the softmax warps have
     // written P_i; a tile's first PV also waits until the epilogue of the
     // previous tile has read O.
@@ -837,7 +935,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                   p.timeout_ns)))
             break;
           ok = pv_step<D>(ctl, tmem, kv_s, g, i, pos_v(base, i, t.n_kv), abort_flag,
-                          p.timeout_ns);
+                          p.timeout_ns, tslot);
         }
         base += 2 * t.n_kv;
       }
@@ -845,11 +943,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       wait_drain(ctl.bar(BAR_DRAIN_PV), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
-    // ---------------- softmax warpgroup (warps 2-5)
-    const int wq = warp & 3;                        // TMEM lane quarter of this warp
+  } else if (warp < WARP_PV) {
+    // ---------------- softmax warps 2-9: warp w handles the rows of TMEM
+    // lane quarter w % 4 and keys 64 * half .. 64 * half + 63 of every tile,
+    // half = (w - 2) / 4; O columns are split the same way.
+    const int wq = warp & 3;
+    const int half = (warp - SOFTMAX_WARP0) >> 2;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    Pair pr{wq, half, lane, ctl.bar(BAR_PAIR0 + wq), ctl.xv, ctl.xf, 0u, abort_flag, p.timeout_ns};
+    constexpr int OC = D / 2;   // O columns per half
     const float c = p.scale_log2;
     long long g = 0;
     bool ok = true;
@@ -862,37 +965,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!t.valid) break;
       const int q_idx = t.qt * BM + row;            // row within the sequence
       RowState st{-INFINITY, 0.f, 0.f};
+      bool s_ready = false;   // early test of this step's S (from the previous step)
       for (int j = 0; j < t.n_kv; ++j, ++g) {
-        ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)g & 1u, abort_flag, p.timeout_ns);
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, s_ready) &&
+            !(ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)g & 1u, abort_flag, p.timeout_ns)))
+          break;
+        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 0);
         tc_fence_after();
-        float s[BN];
-        load_scores(tmem + lane_off + C::COL_S, s);
+        float hs[HB];
+        load_half(tmem + lane_off + C::COL_S + HB * half, hs);
         tc_fence_before();
-        mbar_arrive(ctl.bar(BAR_S_FREE));   // S may now take the next scores
-        const int kv0 = j * BN;
-        if ((kv0 + BN > t.len) || (p.causal && kv0 + BN - 1 > t.qt * BM))
-          mask_scores(s, kv0, p.causal ? min(t.len, q_idx + 1) : t.len);
+        warp_arrive(ctl.bar(BAR_S_FREE));   // S may now take the next scores
+        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 1);
+        const int key0 = j * BN + HB * half;
+        if ((j * BN + BN > t.len) || (p.causal && j * BN + BN - 1 > t.qt * BM))
+          mask_half(hs, key0, p.causal ? min(t.len, q_idx + 1) : t.len);
         const int pb = (int)(g & 1);
-        if (g >= 2) {   // P buffer pb was last read by PV_{g-2}
-          ok = wait_warp(ctl.bar(BAR_PV_DONE0 + pb), (uint32_t)((g - 2) >> 1) & 1u, abort_flag,
-                         p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        bool moved;
-        const float alpha =
-            softmax_tile(s, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)pb, moved);
-        if (__any_sync(0xffffffffu, moved && j > 0)) {   // rescale O after PV_{g-1} landed
-          ok = wait_warp(ctl.bar(BAR_PV_DONE0 + (pb ^ 1)), (uint32_t)((g - 1) >> 1) & 1u,
-                         abort_flag, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          rescale_o<D>(tmem + lane_off + C::COL_O, alpha);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(ctl.bar(BAR_P_FULL0 + pb));
+        StepBars sb;
+        sb.p_full = ctl.bar(BAR_P_FULL0 + pb);
+        sb.pbuf_done = ctl.bar(BAR_PV_DONE0 + pb);             // P_b last read by PV_{g-2}
+        sb.pbuf_parity = (uint32_t)((g - 2) >> 1) & 1u;
+        sb.prev_done = ctl.bar(BAR_PV_DONE0 + (pb ^ 1));       // PV_{g-1}
+        sb.prev_parity = (uint32_t)((g - 1) >> 1) & 1u;
+        sb.s_full = ctl.bar(BAR_S_FULL);
+        sb.s_next_parity = (uint32_t)(g + 1) & 1u;
+        ok = softmax_step<OC>(
+            hs, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)pb + 32u * (uint32_t)half,
+            tmem + lane_off + C::COL_O + OC * half, pr, sb, g >= 2, j > 0, j + 1 < t.n_kv,
+            s_ready, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 3);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE; then O is free for the next tile
@@ -901,12 +1003,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                      p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
+      float l_other, lr_other;   // the partner half's sums
+      if (!(ok = pr.exchange(st.l, l_other) && pr.exchange(st.lr, lr_other))) break;
+      const float l = st.l + l_other;
+      const float lr = st.lr + lr_other;
       const bool live = q_idx < t.len;
-      store_row<D>(tmem + lane_off + C::COL_O, st.lr > 0.f ? 1.f / st.lr : 0.f,
-                   p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D, live);
-      if (live) p.lse[t.lse_base + q_idx] = row_lse(st, p.scale);
+      store_cols<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
+                     p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D +
+                         OC * half,
+                     live);
+      if (live && half == 0) {
+        const float m_use = (st.m == -INFINITY) ? 0.f : st.m;
+        p.lse[t.lse_base + q_idx] = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
+      }
       tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_O_FREE));
+      warp_arrive(ctl.bar(BAR_O_FREE));
     }
   }
 
@@ -1100,6 +1211,22 @@ extern "C" attn_status attn_get_status(cudaStream_t stream) {
     return ATTN_ERR_CUDA;
   return static_cast<attn_status>(value);
 }
+
+#ifdef ATTN_TRACE
+// Diagnostic builds only: choose the traced CTAs (and clear the buffer), and
+// copy the stamps out (TRACE_CTAS x TRACE_ROLES x TRACE_STEPS x TRACE_EVENTS).
+extern "C" int attn_trace_setup(const int *ctas) {
+  static unsigned zero[attn::TRACE_CTAS][attn::TRACE_ROLES][attn::TRACE_STEPS]
+                      [attn::TRACE_EVENTS];
+  if (cudaMemcpyToSymbol(attn::g_trace, zero, sizeof zero) != cudaSuccess) return 1;
+  return cudaMemcpyToSymbol(attn::g_trace_cta, ctas, sizeof(int) * attn::TRACE_CTAS) !=
+         cudaSuccess;
+}
+extern "C" int attn_trace_read(unsigned *out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  return cudaMemcpyFromSymbol(out, attn::g_trace, sizeof(attn::g_trace)) != cudaSuccess;
+}
+#endif
 
 extern "C" const char *attn_status_string(attn_status s) {
   switch (s) {
