@@ -64,7 +64,7 @@ namespace attn {
 // pipeline events of up to four chosen CTAs, read back with
 // attn_trace_read().  Without the macro the hooks compile to nothing.
 #ifdef ATTN_TRACE
-constexpr int TRACE_CTAS = 4, TRACE_ROLES = 5, TRACE_STEPS = 64, TRACE_EVENTS = 4;
+constexpr int TRACE_CTAS = 4, TRACE_ROLES = 11, TRACE_STEPS = 64, TRACE_EVENTS = 12;
 __device__ unsigned g_trace[TRACE_CTAS][TRACE_ROLES][TRACE_STEPS][TRACE_EVENTS];
 __device__ int g_trace_cta[TRACE_CTAS] = {-1, -1, -1, -1};
 __device__ __forceinline__ int trace_slot() {
@@ -108,12 +108,19 @@ struct Cfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = TILE_BYTES * QB;
   static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
-  static constexpr uint32_t CTL_BYTES = 2048;
+  // Rounded row sums of P by the tensor core (P times a block of ones into
+  // tensor-memory columns COL_L..+15) where tensor memory has room for them.
+  static constexpr bool MMA_SUM = D <= 128;
+  static constexpr uint32_t CTL_BYTES = D == 64 ? 3072 : 2048;
+  static constexpr uint32_t ONES_BYTES = 512;   // 16 x 16 bf16 ones, no swizzle
+  static constexpr uint32_t OFF_ONES = OFF_CTL + CTL_BYTES - ONES_BYTES;
   static constexpr uint32_t SMEM_BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_P0 = 128;
   static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_L = COL_O + D;
   static_assert(D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(!MMA_SUM || COL_L + 32 <= TMEM_COLS, "tensor memory");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory");
 };
@@ -395,8 +402,9 @@ __device__ __forceinline__ float max_half(const float (&h)[HB]) {
 }
 
 // p = 2^(h*c - m*c) for 64 scores: bf16 pairs into pk; sums of the fp32
-// values into acc and of the bf16-rounded values into accr (four packed
-// accumulators each).
+// values into acc and, with RSUM, of the bf16-rounded values into accr (four
+// packed accumulators each).
+template <bool RSUM>
 __device__ __forceinline__ void exp_half(const float (&h)[HB], uint64_t c2, uint64_t nm2,
                                          uint32_t (&pk)[HB / 2], uint64_t (&acc)[4],
                                          uint64_t (&accr)[4]) {
@@ -410,7 +418,7 @@ __device__ __forceinline__ void exp_half(const float (&h)[HB], uint64_t c2, uint
     pk[x >> 1] = w;
     acc[(x >> 1) & 3] = f2_add(acc[(x >> 1) & 3], f2_pack(e0, e1));
     // the rounded values too: the P.V product sees exactly these weights
-    accr[(x >> 1) & 3] = f2_add(accr[(x >> 1) & 3], bf16x2_widen(w));
+    if (RSUM) accr[(x >> 1) & 3] = f2_add(accr[(x >> 1) & 3], bf16x2_widen(w));
   }
 }
 
@@ -424,7 +432,8 @@ __device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]) {
 // units, shared by both halves), the running sum of 2^((s - m) * c) over this
 // half's keys (for the LSE) and the running sum of the same weights rounded
 // to bf16 as the P.V product uses them (for O / l: a row dominated by one key
-// then returns that key's value exactly).
+// then returns that key's value exactly).  Where the tensor core forms the
+// rounded sums (next to O in tensor memory), lr stays unused.
 struct RowState {
   float m;
   float l;
@@ -503,36 +512,45 @@ struct StepBars {
 // share one reference, which is all that shift invariance requires.  The
 // waits whose conditions usually hold already are tested early and collected
 // late, so their shared-memory round trips overlap other work.
-template <int OC>
+template <int OC, bool RSUM>
 __device__ __forceinline__ bool softmax_step(const float (&h)[HB], RowState &st, float c,
-                                             uint32_t p_addr, uint32_t o_addr, Pair &pr,
+                                             uint32_t p_addr, uint32_t o_addr, uint32_t l_addr,
+                                             Pair &pr,
                                              const StepBars &sb, bool check_pbuf, bool rescale_ok,
                                              bool test_next, bool &s_next_ready,
                                              volatile uint32_t *abort_flag,
-                                             unsigned long long timeout_ns) {
+                                             unsigned long long timeout_ns, int tslot,
+                                             int trole, long long g) {
   const bool pbuf_early = !check_pbuf || mbar_test_wait(sb.pbuf_done, sb.pbuf_parity);
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 8);
   const uint64_t c2 = f2_pack(c, c);
   uint64_t acc[4] = {0, 0, 0, 0}, accr[4] = {0, 0, 0, 0};
   uint32_t pk[HB / 2];
   // identical across the pair (same rows, same reference) and voted warp-wide
   const bool have_ref = __all_sync(0xffffffffu, st.m != -INFINITY);
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 9);
   float sum = 0.f;
   if (have_ref) {
     const float neg_mc = -st.m * c;
-    exp_half(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
+    exp_half<RSUM>(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
+    if (trole >= 0) ATTN_TRACE_EV(trole, g, 10);
     sum = sum_acc(acc);
   }
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 11);
   const bool want = __any_sync(0xffffffffu, !have_ref || !(sum <= P_SUM_LIMIT));
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 2);
   pr.post(want);
   // the P buffer must be free (its previous PV done) before it is written
   if (!__all_sync(0xffffffffu, pbuf_early) &&
       !wait_warp(sb.pbuf_done, sb.pbuf_parity, abort_flag, timeout_ns))
     return false;
   tc_fence_after();
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 3);
   if (have_ref) tmem_st32(p_addr, pk);   // optimistic; rewritten on a redo
   s_next_ready = test_next && mbar_test_wait(sb.s_full, sb.s_next_parity);
   bool redo;
   if (!pr.collect(want, redo)) return false;
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 4);
   float alpha = 1.f;
   bool moved = false;
   if (redo) {   // first tile, or the reference must move: take the row maximum
@@ -550,20 +568,24 @@ __device__ __forceinline__ bool softmax_step(const float (&h)[HB], RowState &st,
     const float neg_mc = (st.m == -INFINITY) ? 0.f : -st.m * c;
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = accr[i] = 0;
-    exp_half(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
+    exp_half<RSUM>(h, c2, f2_pack(neg_mc, neg_mc), pk, acc, accr);
     tmem_st32(p_addr, pk);
     sum = sum_acc(acc);
   }
   st.l += sum;
-  st.lr += sum_acc(accr);
+  if (RSUM) st.lr += sum_acc(accr);
   if (__any_sync(0xffffffffu, moved && rescale_ok)) {   // rescale O after PV_{g-1} landed
     if (!wait_warp(sb.prev_done, sb.prev_parity, abort_flag, timeout_ns)) return false;
     tc_fence_after();
     rescale_o<OC>(o_addr, alpha);
+    if (!RSUM && pr.half == 0)   // the row-sum column (one copy per row)
+      tmem_st1(l_addr, __float_as_uint(__uint_as_float(tmem_ld_wait1(l_addr)) * alpha));
   }
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 5);
   tmem_wait_st();
   tc_fence_before();
   warp_arrive(sb.p_full);
+  if (trole >= 0) ATTN_TRACE_EV(trole, g, 6);
   return true;
 }
 
@@ -635,14 +657,21 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64
 // O (+)= P V_j: A = P from TMEM (bf16 pairs), B = V tile (vdesc) with keys as
 // K and the head dim as N (N contiguous: 64-wide swizzle atoms CHUNK_BYTES
 // apart, 8-key groups 1024 bytes apart, 16 keys = 2048 bytes per step).
-template <int D>
+//
+// With SUM, each step also adds P times a 16x16 block of ones into the
+// 16 columns at l_tmem: every such column then holds the row sums of P as
+// the product used them (bf16-rounded weights, fp32 accumulation).
+template <int D, bool SUM>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
-                                         bool accumulate) {
+                                         uint32_t l_tmem, uint64_t ones_desc, bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
+  constexpr uint32_t IDESC_SUM = idesc_bf16_f32(16, 0);
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk)
+  for (int kk = 0; kk < BN / 16; ++kk) {
     mma_ts(d_tmem, p_tmem + kk * 8, desc_add(vdesc, kk * 2048), IDESC,
            (accumulate || kk > 0) ? 1u : 0u);
+    if (SUM) mma_ts(l_tmem, p_tmem + kk * 8, ones_desc, IDESC_SUM, (accumulate || kk > 0) ? 1u : 0u);
+  }
 }
 
 // ---------------------------------------------------------------- control block
@@ -726,8 +755,10 @@ __device__ __forceinline__ bool pv_step(const Ctl &ctl, uint32_t tmem, uint32_t 
     return false;
   ATTN_TRACE_EV(1, g, 1);
   tc_fence_after();
-  issue_pv<D>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)pb,
-              desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES), i > 0);
+  issue_pv<D, C::MMA_SUM>(tmem + C::COL_O, tmem + C::COL_P0 + 64u * (uint32_t)pb,
+                          desc_add(smem_desc_sw128(kv_s, CHUNK_BYTES, 1024), slot * C::TILE_BYTES),
+                          tmem + C::COL_L, smem_desc_plain(kv_s - C::OFF_KV + C::OFF_ONES, 128, 256),
+                          i > 0);
   tc_commit(ctl.bar(BAR_PV_DONE0 + pb));
   tc_commit(ctl.bar(BAR_RING + C::STAGES + slot));
   ATTN_TRACE_EV(1, g, 2);
@@ -765,6 +796,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   ctl.info = reinterpret_cast<int *>(ctl.words + 4);
   ctl.xv = reinterpret_cast<float *>(ctl.info + INFO_SLOTS * INFO_INTS);
   ctl.xf = reinterpret_cast<int *>(ctl.xv + 4 * 2 * 32);
+  static_assert((BAR_RING + 2 * C::STAGES) * 8 + 16 + INFO_SLOTS * INFO_INTS * 4 + 4 * 2 * 32 * 4 +
+                        2 * 4 * 2 * 4 <=
+                    C::CTL_BYTES - C::ONES_BYTES,
+                "control block");
   volatile uint32_t *abort_flag = ctl.words + 1;
   const uint32_t q_s = base_s + C::OFF_Q;
   const uint32_t kv_s = base_s + C::OFF_KV;
@@ -781,6 +816,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
+  } else if (C::MMA_SUM && warp == SOFTMAX_WARP0) {
+    // the block of ones (bf16 1.0 = 0x3F80) that the row-sum products read
+    reinterpret_cast<uint4 *>(smem + C::OFF_ONES)[lane] =
+        make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -841,7 +881,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool is_v = last || (item > 0 && (item & 1) == 0);
             const int kt = last ? n - 1 : (item == 0 ? 0 : (is_v ? item / 2 - 1 : (item + 1) / 2));
             mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
-            ATTN_TRACE_EV(4, pos >> 2, (int)(pos & 3));
+            ATTN_TRACE_EV(10, pos >> 2, (int)(pos & 3));
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
@@ -970,13 +1010,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!__all_sync(0xffffffffu, s_ready) &&
             !(ok = wait_warp(ctl.bar(BAR_S_FULL), (uint32_t)g & 1u, abort_flag, p.timeout_ns)))
           break;
-        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 0);
+        if (lane == 0) ATTN_TRACE_EV(2 + 2 * wq + half, g, 0);
         tc_fence_after();
         float hs[HB];
         load_half(tmem + lane_off + C::COL_S + HB * half, hs);
         tc_fence_before();
         warp_arrive(ctl.bar(BAR_S_FREE));   // S may now take the next scores
-        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 1);
+        if (lane == 0) ATTN_TRACE_EV(2 + 2 * wq + half, g, 1);
         const int key0 = j * BN + HB * half;
         if ((j * BN + BN > t.len) || (p.causal && j * BN + BN - 1 > t.qt * BM))
           mask_half(hs, key0, p.causal ? min(t.len, q_idx + 1) : t.len);
@@ -989,12 +1029,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         sb.prev_parity = (uint32_t)((g - 1) >> 1) & 1u;
         sb.s_full = ctl.bar(BAR_S_FULL);
         sb.s_next_parity = (uint32_t)(g + 1) & 1u;
-        ok = softmax_step<OC>(
+        ok = softmax_step<OC, !C::MMA_SUM>(
             hs, st, c, tmem + lane_off + C::COL_P0 + 64u * (uint32_t)pb + 32u * (uint32_t)half,
-            tmem + lane_off + C::COL_O + OC * half, pr, sb, g >= 2, j > 0, j + 1 < t.n_kv,
-            s_ready, abort_flag, p.timeout_ns);
+            tmem + lane_off + C::COL_O + OC * half, tmem + lane_off + C::COL_L, pr, sb, g >= 2,
+            j > 0, j + 1 < t.n_kv,
+            s_ready, abort_flag, p.timeout_ns, tslot, lane == 0 ? 2 + 2 * wq + half : -1, g);
         if (!ok) break;
-        if (lane == 0 && wq == 0) ATTN_TRACE_EV(2 + half, g, 3);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE; then O is free for the next tile
@@ -1003,10 +1043,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                      p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
-      float l_other, lr_other;   // the partner half's sums
-      if (!(ok = pr.exchange(st.l, l_other) && pr.exchange(st.lr, lr_other))) break;
+      float l_other, lr;   // the partner half's exact sum; the row's rounded sum
+      if (!(ok = pr.exchange(st.l, l_other))) break;
+      if (C::MMA_SUM) {
+        lr = __uint_as_float(tmem_ld_wait1(tmem + lane_off + C::COL_L));
+      } else {
+        float lr_other;
+        if (!(ok = pr.exchange(st.lr, lr_other))) break;
+        lr = st.lr + lr_other;
+      }
       const float l = st.l + l_other;
-      const float lr = st.lr + lr_other;
       const bool live = q_idx < t.len;
       store_cols<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
                      p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D +
