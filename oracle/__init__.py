@@ -7,7 +7,8 @@ tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg use it.
 causal mask, grouped-query heads and packed variable-length sequences, in fp64,
 from the exact bf16 input values (see ``attn_oracle.c`` for the definition and
 the passages it follows: tang, sections 2.1-2.4 and 6; TileLang explainer,
-"FlashAttention, in tiles").
+"FlashAttention, in tiles").  Optional score and mask variants (tang, section
+7.3): a key window around each row, a soft cap and ALiBi slopes.
 
 Parity status: pinned.  The tests in ``tests/test_oracle.py`` check it against
 closed forms, invariants, an independent brute-force evaluation and the
@@ -51,6 +52,17 @@ def load_library(path: str):
         ctypes.c_double, ctypes.c_int, ctypes.c_int,        # scale causal round_p
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,      # nsel sel nthreads
     ]
+    lib.oracle_attn_fwd_var.restype = ctypes.c_int
+    lib.oracle_attn_fwd_var.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q k v
+        ctypes.c_void_p, ctypes.c_void_p,                   # o lse
+        ctypes.c_int, i64p, i64p, i64p, i64p,               # nseq, starts/lens
+        ctypes.c_int, ctypes.c_int, ctypes.c_int,           # Hq Hkv d
+        ctypes.c_double, ctypes.c_int,                      # scale causal
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_double,    # wl wr cap
+        ctypes.c_void_p, ctypes.c_int,                      # slopes round_p
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,      # nsel sel nthreads
+    ]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -82,7 +94,8 @@ def _bits(x) -> np.ndarray:
 
 
 def attention_core(q, k, v, q_start, q_len, k_start, k_len, Hq, Hkv, d, scale,
-                   causal, round_p=False, sel=None, nthreads=0, lib=None):
+                   causal, round_p=False, sel=None, nthreads=0, lib=None,
+                   window=(-1, -1), softcap=0.0, alibi_slopes=None):
     """Direct call of the C oracle.
 
     q: bf16 [rows_q, Hq, d]; k, v: bf16 [rows_k, Hkv, d] (torch bf16 tensors
@@ -92,6 +105,11 @@ def attention_core(q, k, v, q_start, q_len, k_start, k_len, Hq, Hkv, d, scale,
     Returns (o, lse) in fp64: with sel=None, o is [rows_q, Hq, d] and lse
     [rows_q, Hq] (rows outside every sequence stay NaN); with sel an int32
     array of (s, h, i) triples, o is [n, d] and lse [n].
+
+    Variants: window = (wl, wr) keeps keys i - wl <= j <= i + wr (negative:
+    unbounded; causal implies wr = 0); softcap > 0 maps a scaled score s to
+    softcap * tanh(s / softcap); alibi_slopes (Hq values) subtract
+    slope[h] * |i - j| after the cap.
     """
     lib = _load() if lib is None else lib
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -112,17 +130,25 @@ def attention_core(q, k, v, q_start, q_len, k_start, k_len, Hq, Hkv, d, scale,
         lse = np.full((sel.shape[0],), np.nan)
         nsel, selp = sel.shape[0], sel.ctypes.data
     i64 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
-    rc = lib.oracle_attn_fwd(
+    slopes = None
+    if alibi_slopes is not None:
+        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64).reshape(-1))
+        assert slopes.size == Hq
+    wl, wr = (int(window[0]), int(window[1]))
+    rc = lib.oracle_attn_fwd_var(
         qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, o.ctypes.data, lse.ctypes.data,
         nseq, i64(qs), i64(ql), i64(ks), i64(kl), Hq, Hkv, d, float(scale),
-        int(bool(causal)), int(bool(round_p)), nsel, selp, int(nthreads))
+        int(bool(causal)), wl, wr, float(softcap),
+        None if slopes is None else slopes.ctypes.data, int(bool(round_p)), nsel, selp,
+        int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd rejected its arguments (code {rc})")
     return o, lse
 
 
 def attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
-                    round_p=False, rows=None, nthreads=0, lib=None):
+                    round_p=False, rows=None, nthreads=0, lib=None, window=(-1, -1),
+                    softcap=0.0, alibi_slopes=None):
     """The oracle in the library's calling convention and layouts.
 
     Fixed batch (cu_seqlens None): q, o are [B, N, Hq, d]; k, v [B, N, Hkv, d];
@@ -131,7 +157,7 @@ def attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
 
     rows=None computes everything and returns (o, lse) in those layouts (fp64).
     rows = array of (seq, h, i) triples computes only those rows and returns
-    (o [n, d], lse [n]).
+    (o [n, d], lse [n]).  window, softcap, alibi_slopes: see attention_core.
     """
     if cu_seqlens is None:
         starts = [b * N for b in range(B)]
@@ -145,7 +171,8 @@ def attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
         T = int(cu[-1])
     o, lse = attention_core(q, k, v, starts, lens, starts, lens, Hq, Hkv, d, scale,
                             causal, round_p=round_p, sel=rows, nthreads=nthreads,
-                            lib=lib)
+                            lib=lib, window=window, softcap=softcap,
+                            alibi_slopes=alibi_slopes)
     if rows is not None:
         return o, lse
     if cu_seqlens is None:

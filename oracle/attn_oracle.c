@@ -18,6 +18,15 @@
  *     o[i,h,:]= sum_{j in valid} exp(s_ij - m_i) * v[j,kv,:] / l_i
  *     lse[i,h]= m_i + ln(l_i)
  *
+ * Score and mask variants (oracle_attn_fwd_var; all off by default):
+ *
+ *     window  : valid additionally requires i - wl <= j <= i + wr (wl, wr >= 0;
+ *               a negative bound is unbounded; causal makes wr = 0)
+ *     soft cap: s_ij <- cap * tanh(s_ij / cap)                 (cap > 0)
+ *     ALiBi   : s_ij <- s_ij - slope[h] * |i - j|              (after the cap)
+ *
+ *   and m, l, o, lse as above over the modified scores and the valid keys.
+ *
  * Sources:
  *  - tang (muni.works/research/tang), section 2.2 "Comprehensions and
  *    monoids" and section 2.3 "Rewrites" (stabilize_softmax): attention is
@@ -36,6 +45,12 @@
  *  - TileLang explainer (ai.thesatyajit.com/articles/tilelang), section
  *    "FlashAttention, in tiles": the per-block loop casts P to the input
  *    type before the P.V product; that is what round_p imitates.
+ *  - tang, section 2.3 (the variant lab) and section 7.3, "Attention variants
+ *    against FlexAttention and FA2": soft cap, ALiBi and a sliding window of
+ *    128 change only the score or the mask, not the monoid.  The pages print
+ *    no formulas for them; the readings above are the common ones (cap
+ *    applied to the scaled score, a linear distance penalty per head, a
+ *    window of keys around the query row).
  *
  * Rows with no valid key cannot occur when causal rows see themselves; if
  * one is requested anyway it gets o = 0 and lse = -inf.
@@ -73,37 +88,45 @@ static double round_to_bf16(double x) {
  *   qrow : pointer to q[i, h, 0]            (bf16 bits, d values)
  *   kbase: pointer to k[k_start, kv, 0]     (row stride kstride elements)
  *   vbase: pointer to v[k_start, kv, 0]
- *   nvalid: number of visible keys (keys 0 .. nvalid-1)
- *   scores: scratch of at least nvalid doubles
+ *   i    : the row's index within its sequence
+ *   jlo, jhi: the visible keys jlo .. jhi (none if jhi < jlo)
+ *   cap  : soft cap (0: none); slope: ALiBi slope of the head (0: none)
+ *   scores: scratch of at least jhi - jlo + 1 doubles
  *   out: d doubles; *lse_out: one double
  */
 static void one_row(const uint16_t *qrow, const uint16_t *kbase,
-                    const uint16_t *vbase, int64_t kstride, int64_t nvalid,
-                    int d, double scale, int round_p, double *scores,
-                    double *out, double *lse_out) {
+                    const uint16_t *vbase, int64_t kstride, int64_t i,
+                    int64_t jlo, int64_t jhi, int d, double scale, double cap,
+                    double slope, int round_p, double *scores, double *out,
+                    double *lse_out) {
   for (int t = 0; t < d; ++t) out[t] = 0.0;
+  const int64_t nvalid = jhi - jlo + 1;
   if (nvalid <= 0) {
     *lse_out = -INFINITY;
     return;
   }
-  /* pass 0: the score row */
-  for (int64_t j = 0; j < nvalid; ++j) {
+  /* pass 0: the score row (keys jlo + n) */
+  for (int64_t n = 0; n < nvalid; ++n) {
+    const int64_t j = jlo + n;
     const uint16_t *krow = kbase + j * kstride;
     double acc = 0.0;
     for (int t = 0; t < d; ++t) acc += bf16_to_double(qrow[t]) * bf16_to_double(krow[t]);
-    scores[j] = scale * acc;
+    double sc = scale * acc;
+    if (cap > 0.0) sc = cap * tanh(sc / cap);
+    sc -= slope * (double)(i > j ? i - j : j - i);
+    scores[n] = sc;
   }
   /* pass 1: the row maximum */
   double m = scores[0];
-  for (int64_t j = 1; j < nvalid; ++j)
-    if (scores[j] > m) m = scores[j];
+  for (int64_t n = 1; n < nvalid; ++n)
+    if (scores[n] > m) m = scores[n];
   /* pass 2: the sum of exponentials and the weighted value sum */
   double l = 0.0;
-  for (int64_t j = 0; j < nvalid; ++j) {
-    double p = exp(scores[j] - m);
+  for (int64_t n = 0; n < nvalid; ++n) {
+    double p = exp(scores[n] - m);
     l += p;
     double pw = round_p ? round_to_bf16(p) : p;
-    const uint16_t *vrow = vbase + j * kstride;
+    const uint16_t *vrow = vbase + (jlo + n) * kstride;
     for (int t = 0; t < d; ++t) out[t] += pw * bf16_to_double(vrow[t]);
   }
   for (int t = 0; t < d; ++t) out[t] /= l;
@@ -127,14 +150,19 @@ static void one_row(const uint16_t *qrow, const uint16_t *kbase,
  *
  * nthreads <= 0 uses the OpenMP default.  Returns 0, or a negative code on
  * invalid arguments (nothing is written then).
+ *
+ * oracle_attn_fwd_var adds the variants: window bounds wl, wr (negative:
+ * unbounded), soft cap (0: none) and ALiBi slopes (Hq values, or NULL).
  */
-int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    double *o, double *lse, int nseq, const int64_t *q_start,
-                    const int64_t *q_len, const int64_t *k_start,
-                    const int64_t *k_len, int Hq, int Hkv, int d, double scale,
-                    int causal, int round_p, int64_t nsel, const int32_t *sel,
-                    int nthreads) {
+int oracle_attn_fwd_var(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        double *o, double *lse, int nseq, const int64_t *q_start,
+                        const int64_t *q_len, const int64_t *k_start,
+                        const int64_t *k_len, int Hq, int Hkv, int d, double scale,
+                        int causal, int64_t wl, int64_t wr, double cap,
+                        const double *slopes, int round_p, int64_t nsel,
+                        const int32_t *sel, int nthreads) {
   if (nseq < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
+  if (!(cap >= 0.0)) return -6;
   int64_t kmax = 0;
   for (int s = 0; s < nseq; ++s) {
     if (q_len[s] < 0 || k_len[s] < 0) return -2;
@@ -189,8 +217,10 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         int s = list[3 * n], h = list[3 * n + 1];
         int64_t i = list[3 * n + 2];
         int kv = h / group;
-        int64_t nvalid = causal ? (i + 1) : k_len[s];
-        if (nvalid > k_len[s]) nvalid = k_len[s];
+        int64_t jhi = causal ? i : k_len[s] - 1;           /* visible keys jlo..jhi */
+        if (!causal && wr >= 0 && i + wr < jhi) jhi = i + wr;
+        if (jhi > k_len[s] - 1) jhi = k_len[s] - 1;
+        int64_t jlo = (wl >= 0 && i - wl > 0) ? i - wl : 0;
         const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;
         const uint16_t *kb = k + k_start[s] * kstride + (int64_t)kv * d;
         const uint16_t *vb = v + k_start[s] * kstride + (int64_t)kv * d;
@@ -204,13 +234,26 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
           orow = o + r * d;
           lrow = lse + r;
         }
-        one_row(qrow, kb, vb, kstride, nvalid, d, scale, round_p, scores, orow, lrow);
+        one_row(qrow, kb, vb, kstride, i, jlo, jhi, d, scale, cap,
+                slopes ? slopes[h] : 0.0, round_p, scores, orow, lrow);
       }
       free(scores);
     }
   }
   free(jobs);
   return failed ? -5 : 0;
+}
+
+/* The plain definition: no window, soft cap or ALiBi. */
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    double *o, double *lse, int nseq, const int64_t *q_start,
+                    const int64_t *q_len, const int64_t *k_start,
+                    const int64_t *k_len, int Hq, int Hkv, int d, double scale,
+                    int causal, int round_p, int64_t nsel, const int32_t *sel,
+                    int nthreads) {
+  return oracle_attn_fwd_var(q, k, v, o, lse, nseq, q_start, q_len, k_start, k_len, Hq,
+                             Hkv, d, scale, causal, -1, -1, 0.0, NULL, round_p, nsel,
+                             sel, nthreads);
 }
 
 /* The number of threads an OpenMP region would use (for reporting). */

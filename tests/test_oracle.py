@@ -59,6 +59,45 @@ def brute_force(q, k, v, lens, Hq, Hkv, d, scale, causal):
     return np.array(O), np.array(LSE)
 
 
+def brute_force_var(q, k, v, lens, Hq, Hkv, d, scale, causal, window=(-1, -1), cap=0.0,
+                    slopes=None):
+    """Exact-summation evaluation of the score and mask variants: keys
+    i - wl <= j <= i + wr (negative: unbounded; causal: wr = 0), soft cap
+    cap * tanh(s / cap) of the scaled score, then minus slope[h] * |i - j|."""
+    qf, kf, vf = q.float().tolist(), k.float().tolist(), v.float().tolist()
+    g = Hq // Hkv
+    wl, wr = window
+    T = sum(lens)
+    O = np.zeros((T, Hq, d))
+    LSE = np.zeros((T, Hq))
+    start = 0
+    for L in lens:
+        for i in range(L):
+            for h in range(Hq):
+                kvh = h // g
+                js = [j for j in range(L)
+                      if (j <= i if causal else (wr < 0 or j <= i + wr))
+                      and (wl < 0 or j >= i - wl)]
+                sc = []
+                for j in js:
+                    x = scale * math.fsum(qf[start + i][h][t] * kf[start + j][kvh][t]
+                                          for t in range(d))
+                    if cap > 0:
+                        x = cap * math.tanh(x / cap)
+                    if slopes is not None:
+                        x -= slopes[h] * abs(i - j)
+                    sc.append(x)
+                m = max(sc)
+                e = [math.exp(x - m) for x in sc]
+                l = math.fsum(e)
+                for t in range(d):
+                    O[start + i, h, t] = math.fsum(e[n] * vf[start + j][kvh][t]
+                                                   for n, j in enumerate(js)) / l
+                LSE[start + i, h] = m + math.log(l)
+        start += L
+    return O, LSE
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2), (6, 3), (4, 1)])
 def test_brute_force_fixed_batch(causal, Hq, Hkv):
@@ -350,3 +389,102 @@ def test_golden_regression_record():
                              meta["scale"], meta["causal"])
     np.testing.assert_allclose(o.reshape(-1), rec["o"], rtol=0, atol=1e-15)
     np.testing.assert_allclose(lse.reshape(-1), rec["lse"], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# score and mask variants (tang, section 7.3: soft cap, ALiBi, sliding window)
+# ---------------------------------------------------------------------------
+VARIANTS = [
+    dict(causal=True, window=(3, -1)),
+    dict(causal=False, window=(2, 4)),
+    dict(causal=False, window=(-1, 1)),
+    dict(causal=True, cap=1.5),
+    dict(causal=False, cap=0.7),
+    dict(causal=True, slopes=True),
+    dict(causal=False, slopes=True),
+    dict(causal=True, window=(4, -1), cap=2.0, slopes=True),
+    dict(causal=False, window=(1, 2), cap=3.0, slopes=True),
+]
+
+
+@pytest.mark.parametrize("var", VARIANTS, ids=lambda v: "-".join(f"{k}={v[k]}" for k in v))
+def test_variants_brute_force(var):
+    lens = [7, 3, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, Hq, Hkv, d = int(cu[-1]), 4, 2, 5
+    q = rand_bf16((T, Hq, d), 11, 2.0)
+    k = rand_bf16((T, Hkv, d), 12)
+    v = rand_bf16((T, Hkv, d), 13)
+    slopes = [0.5 ** (h + 1) for h in range(Hq)] if var.get("slopes") else None
+    window = var.get("window", (-1, -1))
+    cap = var.get("cap", 0.0)
+    o, lse = attn_fwd_oracle(q, k, v, 3, Hq, Hkv, T, d, 0.6, var["causal"], cu_seqlens=cu,
+                             window=window, softcap=cap, alibi_slopes=slopes)
+    Ob, Lb = brute_force_var(q, k, v, lens, Hq, Hkv, d, 0.6, var["causal"], window, cap,
+                             slopes)
+    np.testing.assert_allclose(o, Ob, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, Lb.T, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_of_one_key_returns_own_value(causal):
+    """Window (0, 0): each row sees only its own key, so O = V[i] and
+    LSE = s_ii (closed form)."""
+    B, N, H, d = 2, 11, 3, 8
+    q = rand_bf16((B, N, H, d), 21)
+    k = rand_bf16((B, N, H, d), 22)
+    v = rand_bf16((B, N, H, d), 23)
+    o, lse = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.3, causal, window=(0, 0))
+    np.testing.assert_allclose(o, v.double().numpy(), atol=1e-15, rtol=0)
+    s_ii = 0.3 * np.einsum("bnhd,bnhd->bhn", q.double().numpy(), k.double().numpy())
+    np.testing.assert_allclose(lse, s_ii, atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_unbounded_or_wide_window_is_plain(causal):
+    B, N, H, d = 1, 13, 2, 4
+    q = rand_bf16((B, N, H, d), 31, 2.0)
+    k = rand_bf16((B, N, H, d), 32)
+    v = rand_bf16((B, N, H, d), 33)
+    o0, l0 = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.5, causal)
+    for w in ((-1, -1), (N, N), (N - 1, -1), (-1, N - 1)):
+        o, l = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.5, causal, window=w)
+        np.testing.assert_array_equal(o, o0)
+        np.testing.assert_array_equal(l, l0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_alibi_zero_q_closed_form(causal):
+    """Q = 0 leaves only the ALiBi term: the weights of row i are
+    exp(-slope |i - j|), so LSE_i = ln sum_j exp(-slope |i - j|), a sum of
+    two geometric series."""
+    N, H, d = 12, 2, 4
+    q = torch.zeros((1, N, H, d), dtype=torch.bfloat16)
+    k = rand_bf16((1, N, H, d), 41)
+    v = rand_bf16((1, N, H, d), 42)
+    slopes = [0.25, 1.5]
+    o, lse = attn_fwd_oracle(q, k, v, 1, H, H, N, d, 1.0, causal, alibi_slopes=slopes)
+    for h, a in enumerate(slopes):
+        r = math.exp(-a)
+        for i in range(N):
+            left = (1 - r ** (i + 1)) / (1 - r)          # j = i, i-1, ..., 0
+            right = 0.0 if causal else r * (1 - r ** (N - 1 - i)) / (1 - r)   # j > i
+            assert abs(lse[0, h, i] - math.log(left + right)) < 1e-13
+            w = np.array([r ** abs(i - j) if (j <= i or not causal) else 0.0
+                          for j in range(N)])
+            ref = (w[:, None] * v[0, :, h].double().numpy()).sum(0) / w.sum()
+            np.testing.assert_allclose(o[0, i, h], ref, atol=1e-14, rtol=0)
+
+
+def test_softcap_bounds_the_scores():
+    """|cap tanh(s / cap)| < cap: each LSE lies within ln(n) +- cap, and a
+    huge score range collapses to (almost) uniform weights."""
+    N, H, d = 16, 2, 8
+    q = rand_bf16((1, N, H, d), 51, 40.0)
+    k = rand_bf16((1, N, H, d), 52, 40.0)
+    v = rand_bf16((1, N, H, d), 53)
+    cap = 0.05
+    o, lse = attn_fwd_oracle(q, k, v, 1, H, H, N, d, 1.0, False, softcap=cap)
+    assert np.all(np.abs(lse - math.log(N)) <= cap + 1e-12)
+    mean_v = v[0].double().numpy().mean(0)             # [H, d]
+    assert np.abs(o[0] - mean_v[None]).max() < 2 * cap * np.abs(v.double().numpy()).max()

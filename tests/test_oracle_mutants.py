@@ -19,17 +19,25 @@ from test_oracle import brute_force, rand_bf16
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
-    "causal bound off by one": ("nvalid = causal ? (i + 1)", "nvalid = causal ? (i)"),
+    "causal bound off by one": ("int64_t jhi = causal ? i :", "int64_t jhi = causal ? i - 1 :"),
     "group mapping h % Hkv": ("int kv = h / group;", "int kv = h % Hkv;"),
     "log2 instead of ln": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
-    "scale dropped": ("scores[j] = scale * acc;", "scores[j] = acc;"),
-    "value row fixed": ("const uint16_t *vrow = vbase + j * kstride;",
+    "scale dropped": ("double sc = scale * acc;", "double sc = acc;"),
+    "value row fixed": ("const uint16_t *vrow = vbase + (jlo + n) * kstride;",
                         "const uint16_t *vrow = vbase;"),
     "key used as value": ("out[t] += pw * bf16_to_double(vrow[t]);",
-                          "out[t] += pw * bf16_to_double(kbase[j * kstride + t]);"),
-    "no max subtraction": ("double p = exp(scores[j] - m);", "double p = exp(scores[j]);"),
+                          "out[t] += pw * bf16_to_double(kbase[(jlo + n) * kstride + t]);"),
+    "no max subtraction": ("double p = exp(scores[n] - m);", "double p = exp(scores[n]);"),
     "max starts at zero": ("double m = scores[0];", "double m = 0.0;"),
     "no normalisation": ("for (int t = 0; t < d; ++t) out[t] /= l;", ""),
+    "window lower bound off by one": ("(wl >= 0 && i - wl > 0) ? i - wl : 0",
+                                      "(wl >= 0 && i - wl + 1 > 0) ? i - wl + 1 : 0"),
+    "window right bound ignored": ("if (!causal && wr >= 0 && i + wr < jhi) jhi = i + wr;", ""),
+    "alibi sign": ("sc -= slope *", "sc += slope *"),
+    "alibi distance one-sided": ("(double)(i > j ? i - j : j - i)", "(double)(i - j)"),
+    "soft cap not scaled back": ("sc = cap * tanh(sc / cap);", "sc = tanh(sc / cap);"),
+    "soft cap on the raw product": ("double sc = scale * acc;\n    if (cap > 0.0) sc = cap * tanh(sc / cap);",
+                                    "double sc = acc;\n    if (cap > 0.0) sc = cap * tanh(sc / cap);\n    sc *= scale;"),
     "q row of the kv head": ("const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;",
                              "const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)kv * d;"),
 }
@@ -69,6 +77,24 @@ def _pins_pass(lib) -> bool:
     S = torch.einsum("bihd,bjhd->bhij", q.double(), k.double())
     if not (np.isfinite(o).all() and np.allclose(lse, torch.logsumexp(S, -1).numpy(), rtol=1e-13)):
         return False
+    # score and mask variants against the exact-summation evaluation
+    from test_oracle import VARIANTS, brute_force_var
+    lens = [7, 3, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, Hq, Hkv, d = int(cu[-1]), 4, 2, 5
+    q = rand_bf16((T, Hq, d), 11, 2.0)
+    k = rand_bf16((T, Hkv, d), 12)
+    v = rand_bf16((T, Hkv, d), 13)
+    for var in VARIANTS:
+        slopes = [0.5 ** (h + 1) for h in range(Hq)] if var.get("slopes") else None
+        window, cap = var.get("window", (-1, -1)), var.get("cap", 0.0)
+        o, lse = oracle.attn_fwd_oracle(q, k, v, 3, Hq, Hkv, T, d, 0.6, var["causal"],
+                                        cu_seqlens=cu, window=window, softcap=cap,
+                                        alibi_slopes=slopes, lib=lib)
+        Ob, Lb = brute_force_var(q, k, v, lens, Hq, Hkv, d, 0.6, var["causal"], window, cap,
+                                 slopes)
+        if not (np.allclose(o, Ob, atol=1e-12, rtol=0) and np.allclose(lse, Lb.T, atol=1e-12, rtol=0)):
+            return False
     # Q = 0 closed form
     q = torch.zeros((1, 9, 2, 4), dtype=torch.bfloat16)
     k = rand_bf16((1, 9, 2, 4), 5)
