@@ -86,6 +86,41 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float
                      const int *cu_seqlens, cudaStream_t stream);
 
 /*
+ * attn_variant -- score and mask variants of attn_fwd_ex.  They change only
+ * the scores or the mask, not the online-softmax monoid (tang, section 2.3
+ * and section 7.3, "Attention variants against FlexAttention and FA2": soft
+ * cap, ALiBi, a sliding window of 128).  The pages print no formulas; these
+ * are the common readings.  With s = scale * q_i . k_j:
+ *
+ *   window_left  : keys j < i - window_left are masked (< 0: unbounded).
+ *   window_right : keys j > i + window_right are masked (< 0: unbounded;
+ *                  causal forces 0).  Key tiles that no row of a query tile
+ *                  sees are skipped, not computed.
+ *   softcap      : > 0: s -> softcap * tanh(s / softcap); 0: off.
+ *   alibi_slopes : NULL, or device fp32[Hq] (4-byte aligned): after the cap,
+ *                  s -> s - alibi_slopes[h] * |i - j|.
+ *
+ * The LSE is that of the modified, masked scores.  A row that sees no key
+ * (possible only for padding rows) gets O = 0 and LSE = -inf.
+ */
+typedef struct {
+  int window_left;
+  int window_right;
+  float softcap;
+  const float *alibi_slopes;
+} attn_variant;
+
+/*
+ * attn_fwd_ex -- attn_fwd with score and mask variants (var == NULL: none;
+ * same as attn_fwd).  Same arguments, layouts, ownership and errors as
+ * attn_fwd, plus ATTN_ERR_INVALID_ARG for a softcap that is negative or not
+ * finite and ATTN_ERR_ALIGNMENT for misaligned alibi_slopes.
+ */
+attn_status attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                        int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                        const int *cu_seqlens, const attn_variant *var, cudaStream_t stream);
+
+/*
  * attn_get_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.

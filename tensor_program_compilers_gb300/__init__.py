@@ -37,7 +37,14 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_BAD_SEQLENS = 6
 
-EXPORTED = ["attn_fwd", "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
+EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_get_status", "attn_status_string",
+            "attn_selftest_timeout"]
+
+
+class AttnVariant(ctypes.Structure):
+    """``attn_variant`` of include/attn.h: key window, soft cap, ALiBi slopes."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -78,6 +85,9 @@ def _load():
         vp, i = ctypes.c_void_p, ctypes.c_int
         lib.attn_fwd.restype = i
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, vp]
+        lib.attn_fwd_ex.restype = i
+        lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp,
+                                    ctypes.POINTER(AttnVariant), vp]
         lib.attn_get_status.restype = i
         lib.attn_get_status.argtypes = [vp]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -129,6 +139,26 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
     return rc
 
 
+def make_variant(window=None, softcap: float = 0.0, alibi_slopes=None) -> AttnVariant:
+    """window = (left, right) key bounds around each row (None or a negative
+    side: unbounded); softcap > 0 caps scaled scores at +-softcap via tanh;
+    alibi_slopes: device fp32 tensor [Hq] (or a raw pointer) or None."""
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    return AttnVariant(wl, wr, float(softcap), _ptr(alibi_slopes))
+
+
+def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
+                window=None, softcap=0.0, alibi_slopes=None, stream=None, check=True) -> int:
+    """Call the C ``attn_fwd_ex`` (attn_fwd plus the score and mask variants)."""
+    var = make_variant(window, softcap, alibi_slopes)
+    rc = _load().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                             int(Hkv), int(N), int(d), float(scale), int(bool(causal)),
+                             _ptr(cu_seqlens), ctypes.byref(var), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_ex")
+    return rc
+
+
 def attn_get_status(stream=None) -> int:
     """Synchronise the stream and read/clear the device status word."""
     return _load().attn_get_status(_stream(stream))
@@ -139,12 +169,14 @@ def attn_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
 
 
 def attention(q, k, v, causal: bool, scale: Optional[float] = None, cu_seqlens=None,
-              out=None, lse=None, stream=None):
-    """Allocate outputs (torch, on q's device) and run ``attn_fwd``.
+              out=None, lse=None, stream=None, window=None, softcap: float = 0.0,
+              alibi_slopes=None):
+    """Allocate outputs (torch, on q's device) and run ``attn_fwd_ex``.
 
     Fixed batch: q [B, N, Hq, d], k/v [B, N, Hkv, d] -> o like q, lse [B, Hq, N].
     Packed: q [T, Hq, d], k/v [T, Hkv, d], cu_seqlens int32 [B+1] on the
-    device -> o like q, lse [Hq, T].
+    device -> o like q, lse [Hq, T].  window / softcap / alibi_slopes: the
+    score and mask variants (see ``make_variant``).
     """
     import torch
     d = q.shape[-1]
@@ -167,5 +199,6 @@ def attention(q, k, v, causal: bool, scale: Optional[float] = None, cu_seqlens=N
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, out, lse, B, Hq, Hkv, n_arg, d, scale, causal, cu_seqlens, stream)
+    attn_fwd_ex(q, k, v, out, lse, B, Hq, Hkv, n_arg, d, scale, causal, cu_seqlens,
+                window=window, softcap=softcap, alibi_slopes=alibi_slopes, stream=stream)
     return out, lse

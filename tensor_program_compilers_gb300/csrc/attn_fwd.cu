@@ -159,6 +159,15 @@ struct Params {
   const int *cu_seqlens;
   int B, Hq, Hkv, N, group;
   int causal;
+  // key window: row i sees keys i - wl .. i + wr (clamped to the sequence;
+  // causal makes wr 0; an unbounded side is the largest sequence length)
+  int wl, wr;
+  // score modifiers (kernels with MOD): soft cap s -> cap_k1 tanh(s cap_k2)
+  // in raw score units (cap_k1 = cap / scale, cap_k2 = scale / cap), then
+  // minus alibi[h] / scale * |i - j|
+  int has_cap;
+  float cap_k1, cap_k2;
+  const float *alibi;
   int unit_rows;        // query rows per CTA work unit (one tile)
   int num_units;        // fixed batch: ceil(N / unit_rows)
   float scale;          // score multiplier
@@ -381,11 +390,36 @@ __device__ __forceinline__ void load_half(uint32_t taddr, float (&h)[HB]) {
   }
 }
 
-// Keys key0 + x >= lim are invisible: they read -inf, the identity of max.
-__device__ __forceinline__ void mask_half(float (&h)[HB], int key0, int lim) {
+// Keys key0 + x outside [lo, lim) are invisible: they read -inf, the
+// identity of max.
+__device__ __forceinline__ void mask_half(float (&h)[HB], int key0, int lo, int lim) {
 #pragma unroll
   for (int x = 0; x < HB; ++x)
-    if (key0 + x >= lim) h[x] = -INFINITY;
+    if (key0 + x < lo || key0 + x >= lim) h[x] = -INFINITY;
+}
+
+// Score modifiers, in raw score units (the softmax multiplies by scale
+// later): soft cap k1 tanh(s k2), then the ALiBi term -ak |i - j|.
+__device__ __forceinline__ void modify_half(float (&h)[HB], int key0, int row, bool cap,
+                                            float k1, float k2, float ak) {
+#pragma unroll
+  for (int x = 0; x < HB; ++x) {
+    float v = h[x];
+    if (cap) v = k1 * tanhf(v * k2);
+    v -= ak * fabsf((float)(row - (key0 + x)));
+    h[x] = v;
+  }
+}
+
+// Key tiles a query tile visits: first tile j_lo and count n (keys any of
+// rows r0 .. r0 + BM - 1 sees through the window, within the sequence).
+__device__ __forceinline__ void kv_range(const Params &p, int qt, int len, int &j_lo, int &n) {
+  const long long r0 = (long long)qt * BM;
+  const long long lo_key = r0 - p.wl > 0 ? r0 - p.wl : 0;
+  long long hi_key = r0 + BM - 1 + p.wr;
+  if (hi_key > len - 1) hi_key = len - 1;
+  j_lo = (int)(lo_key / BN);
+  n = hi_key >= lo_key ? (int)(hi_key / BN) - j_lo + 1 : 0;
 }
 
 // Maximum of 64 scores: four independent chains of 3-input max.
@@ -778,7 +812,7 @@ __device__ __forceinline__ long long pos_v(long long base, int i, int n) {
 // Persistent: with G = gridDim.x CTAs, CTA b processes one tile of each
 // round of G tiles of the longest-first list -- tile b of even rounds, tile
 // G-1-b of odd rounds -- until the producer publishes an invalid tile.
-template <int D>
+template <int D, bool MOD>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -837,8 +871,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // the CTA given the longest tile of a round gets the shortest next
       const long long G = gridDim.x;
       const Tile t = decode_tile(p, (long long)k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x));
-      const int kv_tiles = (t.len + BN - 1) / BN;
-      const int n = t.valid ? (p.causal ? min(t.unit + 1, kv_tiles) : kv_tiles) : 0;
+      int j_lo = 0, n = 0;
+      if (t.valid) kv_range(p, t.unit, t.len, j_lo, n);
       if (lane == 0) {
         const int e = k % INFO_SLOTS;
         ok = wait_bounded(ctl.bar(BAR_INFO_EMPTY0 + e), ((uint32_t)(k / INFO_SLOTS) & 1u) ^ 1u,
@@ -885,7 +919,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
-                          c * 64, kvh, t.seq_start + kt * BN);
+                          c * 64, kvh, t.seq_start + (j_lo + kt) * BN);
           }
         }
       }
@@ -1004,6 +1038,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(ctl.bar(BAR_INFO_EMPTY0 + k % INFO_SLOTS));
       if (!t.valid) break;
       const int q_idx = t.qt * BM + row;            // row within the sequence
+      int j_lo, n_unused;
+      kv_range(p, t.qt, t.len, j_lo, n_unused);
+      // this row's visible keys [lo, lim); a tile needs masking when some
+      // row of the query tile does not see all of its keys
+      const int lo = q_idx - p.wl;                                     // wl <= N
+      const int lim = p.wr >= t.len - q_idx ? t.len : q_idx + p.wr + 1;   // no overflow
+      const int r0 = t.qt * BM;
+      const float ak = (MOD && p.alibi) ? __ldg(p.alibi + t.h) / p.scale : 0.f;
       RowState st{-INFINITY, 0.f, 0.f};
       bool s_ready = false;   // early test of this step's S (from the previous step)
       for (int j = 0; j < t.n_kv; ++j, ++g) {
@@ -1017,9 +1059,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_before();
         warp_arrive(ctl.bar(BAR_S_FREE));   // S may now take the next scores
         if (lane == 0) ATTN_TRACE_EV(2 + 2 * wq + half, g, 1);
-        const int key0 = j * BN + HB * half;
-        if ((j * BN + BN > t.len) || (p.causal && j * BN + BN - 1 > t.qt * BM))
-          mask_half(hs, key0, p.causal ? min(t.len, q_idx + 1) : t.len);
+        const int kb = (j_lo + j) * BN;   // the tile's first key
+        const int key0 = kb + HB * half;
+        if (MOD) modify_half(hs, key0, q_idx, p.has_cap != 0, p.cap_k1, p.cap_k2, ak);
+        // some row of the query tile misses keys of this tile: the sequence
+        // ends inside it, or it reaches past the window of row r0 (right) or
+        // of row r0 + BM - 1 (left)
+        if (kb + BN > t.len || kb + BN - 1 - r0 > p.wr || r0 + BM - 1 - kb > p.wl)
+          mask_half(hs, key0, lo, lim);
         const int pb = (int)(g & 1);
         StepBars sb;
         sb.p_full = ctl.bar(BAR_P_FULL0 + pb);
@@ -1154,9 +1201,12 @@ static attn_status prepare_device(int dev) {
           cudaSuccess ||
       g_sm_count[dev] < 1)
     return ATTN_ERR_CUDA;
-  if (!opt_in_smem(attn_fwd_kernel<64>, Cfg<64>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<128>, Cfg<128>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<256>, Cfg<256>::SMEM_BYTES))
+  if (!opt_in_smem(attn_fwd_kernel<64, false>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, false>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, false>, Cfg<256>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<64, true>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, true>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, true>, Cfg<256>::SMEM_BYTES))
     return ATTN_ERR_CUDA;
   state[dev] = 1;
   return ATTN_OK;
@@ -1177,10 +1227,22 @@ static unsigned long long wait_timeout_ns() {
 extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                                 const int *cu_seqlens, cudaStream_t stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, nullptr,
+                     stream);
+}
+
+extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                                   int causal, const int *cu_seqlens, const attn_variant *var,
+                                   cudaStream_t stream) {
   using namespace attn;
   if (B < 0 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  const float cap = var ? var->softcap : 0.f;
+  if (!(cap >= 0.f) || !std::isfinite(cap)) return ATTN_ERR_INVALID_ARG;
+  const float *slopes = var ? var->alibi_slopes : nullptr;
+  if (slopes && (reinterpret_cast<uintptr_t>(slopes) & 3u)) return ATTN_ERR_ALIGNMENT;
   if (B == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
   auto misaligned = [](const void *ptr, uintptr_t a) {
@@ -1215,6 +1277,15 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
   p.N = N;
   p.group = Hq / Hkv;
   p.causal = causal ? 1 : 0;
+  // window bounds; a bound of N or more never masks anything
+  const long long wl_in = var ? var->window_left : -1, wr_in = var ? var->window_right : -1;
+  p.wl = (int)((wl_in < 0 || wl_in > N) ? N : wl_in);
+  p.wr = causal ? 0 : (int)((wr_in < 0 || wr_in > N) ? N : wr_in);
+  p.has_cap = cap > 0.f ? 1 : 0;
+  p.cap_k1 = cap > 0.f ? cap / scale : 0.f;
+  p.cap_k2 = cap > 0.f ? scale / cap : 0.f;
+  p.alibi = slopes;
+  const bool mod = cap > 0.f || slopes != nullptr;
   p.unit_rows = BM;
   p.num_units = (N + p.unit_rows - 1) / p.unit_rows;
   p.scale = scale;
@@ -1232,18 +1303,14 @@ extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, voi
   // scheduler balances small grids better than fixed rounds).
   const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
 
-  switch (d) {
-    case 64:
-      attn_fwd_kernel<64><<<(unsigned)grid, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
-      break;
-    case 128:
-      attn_fwd_kernel<128><<<(unsigned)grid, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv,
-                                                                                    p);
-      break;
-    default:
-      attn_fwd_kernel<256><<<(unsigned)grid, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv,
-                                                                                    p);
-      break;
+  const unsigned gr = (unsigned)grid;
+  switch (d * 2 + (mod ? 1 : 0)) {
+    case 128: attn_fwd_kernel<64, false><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 129: attn_fwd_kernel<64, true><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 256: attn_fwd_kernel<128, false><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 257: attn_fwd_kernel<128, true><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 512: attn_fwd_kernel<256, false><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    default: attn_fwd_kernel<256, true><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

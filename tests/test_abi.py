@@ -79,3 +79,32 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         pkg.library()
+
+
+def call_ex(window=None, softcap=0.0, alibi_slopes=None, **kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=2, Hq=8, Hkv=2, N=256,
+                d=128, scale=0.088, causal=1, cu_seqlens=None, stream=0)
+    args.update(kw)
+    return pkg.attn_fwd_ex(check=False, window=window, softcap=softcap,
+                           alibi_slopes=alibi_slopes, **args)
+
+
+@pytest.mark.parametrize("cap", [-1.0, float("inf"), float("nan")])
+def test_variant_bad_softcap_rejected(lib, cap):
+    assert call_ex(softcap=cap) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_variant_misaligned_slopes_rejected(lib):
+    assert call_ex(alibi_slopes=0x6002) == pkg.ATTN_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(N=0)])
+def test_variant_empty_problem_is_a_no_op(lib, kw):
+    assert call_ex(window=(128, 0), softcap=30.0, alibi_slopes=0x6000, **kw) == pkg.ATTN_OK
+
+
+def test_variant_struct_layout():
+    """attn_variant is {int, int, float, const float *}: pointer at offset 16."""
+    import ctypes
+    assert ctypes.sizeof(pkg.AttnVariant) == 24
+    assert pkg.AttnVariant.alibi_slopes.offset == 16
