@@ -182,3 +182,22 @@ def attn_fwd_oracle(q, k, v, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None,
         o = o.reshape(T, Hq, d)
         lse = lse.reshape(T, Hq).T.copy()
     return o, lse
+
+
+def attn_decode_oracle(q, k, v, seqlens_k, causal, scale, nthreads=0, lib=None):
+    """The oracle in the decode convention: q [B, Nq, Hq, d] are the last Nq
+    positions of sequences whose keys are k, v [B, Nk_max, Hkv, d] rows
+    0 .. seqlens_k[b] - 1 (the rest of each cache is ignored).  With causal,
+    query r of sequence b sees keys j <= seqlens_k[b] - Nq + r.
+
+    Returns (o [B, Nq, Hq, d], lse [B, Hq, Nq]) in fp64.
+    """
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    kl = [int(x) for x in np.asarray(seqlens_k).reshape(-1)]
+    assert len(kl) == B and all(Nq <= x <= Nk for x in kl)
+    o, lse = attention_core(q.reshape(B * Nq, Hq, d), k.reshape(B * Nk, Hkv, d),
+                            v.reshape(B * Nk, Hkv, d), [b * Nq for b in range(B)], [Nq] * B,
+                            [b * Nk for b in range(B)], kl, Hq, Hkv, d, scale, causal,
+                            nthreads=nthreads, lib=lib)
+    return o.reshape(B, Nq, Hq, d), lse.reshape(B, Nq, Hq).transpose(0, 2, 1).copy()

@@ -10,7 +10,10 @@
  *
  *   for every sequence s, query head h, query row i of s:
  *     kv      = floor(h / (Hq / Hkv))                 grouped-query head map
- *     valid   = { j : 0 <= j < Lk(s) }  and, if causal, j <= i
+ *     p       = i + Lk(s) - Lq(s)                      the row's key position
+ *                                                       (queries are the last
+ *                                                       Lq(s) positions)
+ *     valid   = { j : 0 <= j < Lk(s) }  and, if causal, j <= p
  *     s_ij    = scale * sum_t q[i,h,t] * k[j,kv,t]     (fp64, inputs widened
  *                                                       exactly from bf16)
  *     m_i     = max_{j in valid} s_ij
@@ -20,10 +23,10 @@
  *
  * Score and mask variants (oracle_attn_fwd_var; all off by default):
  *
- *     window  : valid additionally requires i - wl <= j <= i + wr (wl, wr >= 0;
+ *     window  : valid additionally requires p - wl <= j <= p + wr (wl, wr >= 0;
  *               a negative bound is unbounded; causal makes wr = 0)
  *     soft cap: s_ij <- cap * tanh(s_ij / cap)                 (cap > 0)
- *     ALiBi   : s_ij <- s_ij - slope[h] * |i - j|              (after the cap)
+ *     ALiBi   : s_ij <- s_ij - slope[h] * |p - j|              (after the cap)
  *
  *   and m, l, o, lse as above over the modified scores and the valid keys.
  *
@@ -88,7 +91,7 @@ static double round_to_bf16(double x) {
  *   qrow : pointer to q[i, h, 0]            (bf16 bits, d values)
  *   kbase: pointer to k[k_start, kv, 0]     (row stride kstride elements)
  *   vbase: pointer to v[k_start, kv, 0]
- *   i    : the row's index within its sequence
+ *   i    : the row's key position (its index among the keys)
  *   jlo, jhi: the visible keys jlo .. jhi (none if jhi < jlo)
  *   cap  : soft cap (0: none); slope: ALiBi slope of the head (0: none)
  *   scores: scratch of at least jhi - jlo + 1 doubles
@@ -139,8 +142,9 @@ static void one_row(const uint16_t *qrow, const uint16_t *kbase,
  * q: [*, Hq, d] bf16 bits; k, v: [*, Hkv, d] bf16 bits (token rows packed;
  * row r of sequence s is token q_start[s] + r, resp. k_start[s] + r).
  * nseq sequences; sequence s has q_len[s] query rows and k_len[s] keys.
- * causal requires q_len[s] == k_len[s]; key j is visible from row i iff
- * j <= i.
+ * causal requires q_len[s] <= k_len[s]; key j is visible from row i iff
+ * j <= i + k_len[s] - q_len[s] (the queries are the sequence's last q_len[s]
+ * positions: equal lengths give j <= i).
  *
  * If nsel < 0, every row is computed:
  *   o  [(q_start[s] + i) * Hq + h) * d + t]
@@ -166,7 +170,7 @@ int oracle_attn_fwd_var(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   int64_t kmax = 0;
   for (int s = 0; s < nseq; ++s) {
     if (q_len[s] < 0 || k_len[s] < 0) return -2;
-    if (causal && q_len[s] != k_len[s]) return -3;
+    if (causal && q_len[s] > k_len[s]) return -3;
     if (k_len[s] > kmax) kmax = k_len[s];
   }
   const int group = Hq / Hkv;
@@ -217,10 +221,11 @@ int oracle_attn_fwd_var(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         int s = list[3 * n], h = list[3 * n + 1];
         int64_t i = list[3 * n + 2];
         int kv = h / group;
-        int64_t jhi = causal ? i : k_len[s] - 1;           /* visible keys jlo..jhi */
-        if (!causal && wr >= 0 && i + wr < jhi) jhi = i + wr;
+        const int64_t pos = i + k_len[s] - q_len[s];       /* the row's key position */
+        int64_t jhi = causal ? pos : k_len[s] - 1;         /* visible keys jlo..jhi */
+        if (!causal && wr >= 0 && pos + wr < jhi) jhi = pos + wr;
         if (jhi > k_len[s] - 1) jhi = k_len[s] - 1;
-        int64_t jlo = (wl >= 0 && i - wl > 0) ? i - wl : 0;
+        int64_t jlo = (wl >= 0 && pos - wl > 0) ? pos - wl : 0;
         const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;
         const uint16_t *kb = k + k_start[s] * kstride + (int64_t)kv * d;
         const uint16_t *vb = v + k_start[s] * kstride + (int64_t)kv * d;
@@ -234,7 +239,7 @@ int oracle_attn_fwd_var(const uint16_t *q, const uint16_t *k, const uint16_t *v,
           orow = o + r * d;
           lrow = lse + r;
         }
-        one_row(qrow, kb, vb, kstride, i, jlo, jhi, d, scale, cap,
+        one_row(qrow, kb, vb, kstride, pos, jlo, jhi, d, scale, cap,
                 slopes ? slopes[h] : 0.0, round_p, scores, orow, lrow);
       }
       free(scores);

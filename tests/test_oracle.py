@@ -98,6 +98,33 @@ def brute_force_var(q, k, v, lens, Hq, Hkv, d, scale, causal, window=(-1, -1), c
     return O, LSE
 
 
+def brute_force_decode(q, k, v, seqlens_k, causal, scale):
+    """Exact-summation evaluation for queries that are the last Nq positions
+    of their sequences (q [B, Nq, Hq, d], k/v [B, Nk, Hkv, d])."""
+    B, Nq, Hq, d = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    qf, kf, vf = q.float().tolist(), k.float().tolist(), v.float().tolist()
+    O = np.zeros((B, Nq, Hq, d))
+    LSE = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        L = int(seqlens_k[b])
+        for r in range(Nq):
+            pos = L - Nq + r
+            js = list(range(pos + 1)) if causal else list(range(L))
+            for h in range(Hq):
+                kvh = h // g
+                sc = [scale * math.fsum(qf[b][r][h][t] * kf[b][j][kvh][t] for t in range(d))
+                      for j in js]
+                m = max(sc)
+                e = [math.exp(x - m) for x in sc]
+                l = math.fsum(e)
+                for t in range(d):
+                    O[b, r, h, t] = math.fsum(e[n] * vf[b][j][kvh][t] for n, j in enumerate(js)) / l
+                LSE[b, h, r] = m + math.log(l)
+    return O, LSE
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 2), (6, 3), (4, 1)])
 def test_brute_force_fixed_batch(causal, Hq, Hkv):
@@ -488,3 +515,47 @@ def test_softcap_bounds_the_scores():
     assert np.all(np.abs(lse - math.log(N)) <= cap + 1e-12)
     mean_v = v[0].double().numpy().mean(0)             # [H, d]
     assert np.abs(o[0] - mean_v[None]).max() < 2 * cap * np.abs(v.double().numpy()).max()
+
+
+# ---------------------------------------------------------------------------
+# decode shapes: the queries are the last positions of longer key sequences
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq", [1, 3])
+def test_decode_brute_force(causal, Nq):
+    B, Nk, Hq, Hkv, d = 3, 13, 6, 2, 5
+    kl = [13, 7, Nq]
+    q = rand_bf16((B, Nq, Hq, d), 71, 2.0)
+    k = rand_bf16((B, Nk, Hkv, d), 72)
+    v = rand_bf16((B, Nk, Hkv, d), 73)
+    o, lse = oracle.attn_decode_oracle(q, k, v, kl, causal, 0.7)
+    Ob, Lb = brute_force_decode(q, k, v, kl, causal, 0.7)
+    np.testing.assert_allclose(o, Ob, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, Lb, atol=1e-12, rtol=0)
+
+
+def test_decode_rows_equal_the_last_prefill_rows():
+    """The last Nq rows of a causal prefill over the whole sequence are the
+    decode of those Nq queries against the same keys."""
+    N, Nq, H, d = 40, 4, 2, 8
+    q = rand_bf16((1, N, H, d), 81)
+    k = rand_bf16((1, N, H, d), 82)
+    v = rand_bf16((1, N, H, d), 83)
+    of, lf = attn_fwd_oracle(q, k, v, 1, H, H, N, d, 0.4, True)
+    od, ld = oracle.attn_decode_oracle(q[:, N - Nq:].contiguous(), k, v, [N], True, 0.4)
+    np.testing.assert_array_equal(od[0], of[0, N - Nq:])
+    np.testing.assert_array_equal(ld[0], lf[0, :, N - Nq:])
+
+
+def test_decode_ignores_cache_rows_past_the_length():
+    B, Nq, Nk, H, d = 1, 1, 20, 2, 4
+    q = rand_bf16((B, Nq, H, d), 91)
+    k = rand_bf16((B, Nk, H, d), 92)
+    v = rand_bf16((B, Nk, H, d), 93)
+    o1, l1 = oracle.attn_decode_oracle(q, k, v, [9], False, 0.5)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, 9:] = 1e4
+    v2[:, 9:] = float("nan")
+    o2, l2 = oracle.attn_decode_oracle(q, k2, v2, [9], False, 0.5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

@@ -19,7 +19,9 @@ from test_oracle import brute_force, rand_bf16
 SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
 
 MUTANTS = {
-    "causal bound off by one": ("int64_t jhi = causal ? i :", "int64_t jhi = causal ? i - 1 :"),
+    "causal bound off by one": ("int64_t jhi = causal ? pos :", "int64_t jhi = causal ? pos - 1 :"),
+    "decode offset dropped": ("const int64_t pos = i + k_len[s] - q_len[s];",
+                              "const int64_t pos = i;"),
     "group mapping h % Hkv": ("int kv = h / group;", "int kv = h % Hkv;"),
     "log2 instead of ln": ("*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
     "scale dropped": ("double sc = scale * acc;", "double sc = acc;"),
@@ -30,9 +32,9 @@ MUTANTS = {
     "no max subtraction": ("double p = exp(scores[n] - m);", "double p = exp(scores[n]);"),
     "max starts at zero": ("double m = scores[0];", "double m = 0.0;"),
     "no normalisation": ("for (int t = 0; t < d; ++t) out[t] /= l;", ""),
-    "window lower bound off by one": ("(wl >= 0 && i - wl > 0) ? i - wl : 0",
-                                      "(wl >= 0 && i - wl + 1 > 0) ? i - wl + 1 : 0"),
-    "window right bound ignored": ("if (!causal && wr >= 0 && i + wr < jhi) jhi = i + wr;", ""),
+    "window lower bound off by one": ("(wl >= 0 && pos - wl > 0) ? pos - wl : 0",
+                                      "(wl >= 0 && pos - wl + 1 > 0) ? pos - wl + 1 : 0"),
+    "window right bound ignored": ("if (!causal && wr >= 0 && pos + wr < jhi) jhi = pos + wr;", ""),
     "alibi sign": ("sc -= slope *", "sc += slope *"),
     "alibi distance one-sided": ("(double)(i > j ? i - j : j - i)", "(double)(i - j)"),
     "soft cap not scaled back": ("sc = cap * tanh(sc / cap);", "sc = tanh(sc / cap);"),
@@ -94,6 +96,18 @@ def _pins_pass(lib) -> bool:
         Ob, Lb = brute_force_var(q, k, v, lens, Hq, Hkv, d, 0.6, var["causal"], window, cap,
                                  slopes)
         if not (np.allclose(o, Ob, atol=1e-12, rtol=0) and np.allclose(lse, Lb.T, atol=1e-12, rtol=0)):
+            return False
+    # decode shapes: a few queries at the end of longer key sequences
+    from test_oracle import brute_force_decode
+    for causal in (False, True):
+        B, Nq, Nk, Hq, Hkv, d = 2, 3, 11, 4, 2, 5
+        kl = [11, 6]
+        q = rand_bf16((B, Nq, Hq, d), 61, 2.0)
+        k = rand_bf16((B, Nk, Hkv, d), 62)
+        v = rand_bf16((B, Nk, Hkv, d), 63)
+        o, lse = oracle.attn_decode_oracle(q, k, v, kl, causal, 0.6, lib=lib)
+        Ob, Lb = brute_force_decode(q, k, v, kl, causal, 0.6)
+        if not (np.allclose(o, Ob, atol=1e-12, rtol=0) and np.allclose(lse, Lb, atol=1e-12, rtol=0)):
             return False
     # Q = 0 closed form
     q = torch.zeros((1, 9, 2, 4), dtype=torch.bfloat16)
