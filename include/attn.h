@@ -121,6 +121,45 @@ attn_status attn_fwd_ex(const void *q, const void *k, const void *v, void *o, fl
                         const int *cu_seqlens, const attn_variant *var, cudaStream_t stream);
 
 /*
+ * attn_fwd_decode -- attention of a few new queries against long key/value
+ * caches, split along the keys (the online-softmax merge is associative:
+ * tang, section 2.2, "Online softmax is the monoid ..."; section 2.5, "split
+ * ... valid for any monoid because combine is associative, including online
+ * softmax").  Each (sequence, kv head, key split) computes a partial state
+ * of its rows (the group's Hq/Hkv query heads x Nq positions); a second
+ * kernel merges the splits: LSE = log sum_s exp(LSE_s),
+ * O = sum_s exp(LSE_s - LSE) O_s.
+ *
+ *   q        : device bf16 [B, Nq, Hq, d] -- the last Nq positions of each
+ *              sequence (16-byte aligned).
+ *   k, v     : device bf16 [B, Nk, Hkv, d] caches; sequence b uses rows
+ *              0 .. seqlens_k[b] - 1.  Rows past a sequence's length must
+ *              hold finite values (they are read, weighted by zero).
+ *   o        : device bf16 [B, Nq, Hq, d];  lse: device fp32 [B, Hq, Nq].
+ *   Nq, Nk   : queries per sequence, cache rows per sequence;
+ *              1 <= Nq <= Nk and (Hq / Hkv) * Nq <= 128.
+ *   causal   : nonzero: query r of sequence b sees keys
+ *              j <= seqlens_k[b] - Nq + r (bottom-right alignment);
+ *              zero: all seqlens_k[b] keys.
+ *   seqlens_k: NULL (every sequence has Nk keys), or device int32[B] with
+ *              Nq <= seqlens_k[b] <= Nk (checked on the device; a bad value
+ *              is reported as ATTN_ERR_BAD_SEQLENS by attn_get_status and
+ *              that sequence's outputs stay unwritten).
+ *   workspace: device memory owned by the caller, 16-byte aligned, at least
+ *              attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) bytes
+ *              (may be NULL when that is 0).  It holds the partial states
+ *              between the two kernels; nothing else is allocated.
+ *
+ * Other arguments and errors as attn_fwd; too small a workspace is
+ * ATTN_ERR_INVALID_ARG.  The split count depends on the device's SM count.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                            int causal, const int *seqlens_k, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_get_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.

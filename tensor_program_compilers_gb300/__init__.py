@@ -37,8 +37,8 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_BAD_SEQLENS = 6
 
-EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_get_status", "attn_status_string",
-            "attn_selftest_timeout"]
+EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
+            "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
 
 
 class AttnVariant(ctypes.Structure):
@@ -88,6 +88,11 @@ def _load():
         lib.attn_fwd_ex.restype = i
         lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp,
                                     ctypes.POINTER(AttnVariant), vp]
+        lib.attn_fwd_decode.restype = i
+        lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i,
+                                        vp, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
         lib.attn_get_status.argtypes = [vp]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -157,6 +162,53 @@ def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=Non
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_ex")
     return rc
+
+
+def attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d) -> int:
+    """Workspace bytes ``attn_fwd_decode`` needs on the current device."""
+    return int(_load().attn_decode_workspace_bytes(int(B), int(Hq), int(Hkv), int(Nq), int(Nk),
+                                                   int(d)))
+
+
+def attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k=None,
+                    workspace=None, workspace_bytes=None, stream=None, check=True) -> int:
+    """Call the C ``attn_fwd_decode`` (split-key attention for decode shapes).
+
+    q, o [B, Nq, Hq, d]; k, v [B, Nk, Hkv, d]; lse [B, Hq, Nq]; seqlens_k
+    int32 [B] on the device or None; workspace: a device buffer of at least
+    ``attn_decode_workspace_bytes`` bytes (a tensor, or a raw pointer with
+    workspace_bytes).
+    """
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = _load().attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                                 int(Hkv), int(Nq), int(Nk), int(d), float(scale),
+                                 int(bool(causal)), _ptr(seqlens_k), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_decode")
+    return rc
+
+
+def decode(q, k, v, causal: bool = False, scale: Optional[float] = None, seqlens_k=None,
+           out=None, lse=None, workspace=None, stream=None):
+    """Allocate outputs and workspace (torch, on q's device) and run
+    ``attn_fwd_decode``: q [B, Nq, Hq, d], k/v caches [B, Nk, Hkv, d]."""
+    import torch
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    scale = d ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+        workspace = torch.empty((max(n, 16) + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    attn_fwd_decode(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
+                    workspace, stream=stream)
+    return out, lse
 
 
 def attn_get_status(stream=None) -> int:

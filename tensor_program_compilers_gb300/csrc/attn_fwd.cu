@@ -168,6 +168,14 @@ struct Params {
   int has_cap;
   float cap_k1, cap_k2;
   const float *alibi;
+  // decode (split keys): q [B, dq_n, Hq, d] are the last dq_n positions of
+  // sequences with keys k, v [B, dk_n, Hkv, d] rows 0 .. seqlens_k[b] - 1;
+  // a work unit is (b, kv head, split) over keys split * chunk .. + chunk,
+  // rows = the group's query heads x dq_n positions (head fastest).
+  int dq_n, dk_n, splits, chunk;
+  const int *seqlens_k;
+  float *ws_o;          // splits > 1: partial O / l [B, Hq, dq_n, splits, d]
+  float *ws_lse;        // and partial LSE [B, Hq, dq_n, splits]
   int unit_rows;        // query rows per CTA work unit (one tile)
   int num_units;        // fixed batch: ceil(N / unit_rows)
   float scale;          // score multiplier
@@ -276,10 +284,29 @@ __device__ int units_at_or_above(const SeqUnits &su, const int *cu, int B, int x
 // ordered longest first -- descending unit index, i.e. descending number of
 // causal key tiles -- with heads fastest so that the query heads of one
 // key/value head run side by side.
-__device__ Tile decode_tile(const Params &p, long long idx) {
+__device__ Tile decode_tile(const Params &p, long long idx, bool dec) {
   Tile t{};
   const int lane = threadIdx.x & 31;
   const int U = p.unit_rows;
+  if (dec) {   // (b, kv head, split), split fastest
+    const long long units = (long long)p.B * p.Hkv * p.splits;
+    if (idx >= units) return t;
+    const int s = (int)(idx % p.splits);
+    const long long r = idx / p.splits;
+    t.h = (int)(r % p.Hkv);
+    t.seq_start = (int)(r / p.Hkv);   // the sequence index b
+    const int L = p.seqlens_k ? __ldg(p.seqlens_k + t.seq_start) : p.dk_n;
+    t.valid = 1;
+    if (L < p.dq_n || L > p.dk_n) {   // an impossible length: report; no keys (skipped)
+      if (lane == 0) record_status(ATTN_ERR_BAD_SEQLENS);
+      t.len = 0;
+      return t;
+    }
+    t.len = L;
+    t.unit = s;
+    t.valid = 1;
+    return t;
+  }
   if (p.cu_seqlens == nullptr) {
     const long long per = (long long)p.B * p.Hq;
     const int lvl = (int)(idx / per);
@@ -413,7 +440,15 @@ __device__ __forceinline__ void modify_half(float (&h)[HB], int key0, int row, b
 
 // Key tiles a query tile visits: first tile j_lo and count n (keys any of
 // rows r0 .. r0 + BM - 1 sees through the window, within the sequence).
-__device__ __forceinline__ void kv_range(const Params &p, int qt, int len, int &j_lo, int &n) {
+__device__ __forceinline__ void kv_range(const Params &p, int qt, int len, int &j_lo, int &n,
+                                         bool dec) {
+  if (dec) {   // the split's keys qt * chunk .. min(len, (qt + 1) * chunk) - 1
+    const int k0 = qt * p.chunk;
+    const int k1 = min(len, k0 + p.chunk);
+    j_lo = k0 / BN;
+    n = k1 > k0 ? (k1 - k0 + BN - 1) / BN : 0;
+    return;
+  }
   const long long r0 = (long long)qt * BM;
   const long long lo_key = r0 - p.wl > 0 ? r0 - p.wl : 0;
   long long hi_key = r0 + BM - 1 + p.wr;
@@ -674,6 +709,48 @@ __device__ __forceinline__ void store_cols(uint32_t taddr, float inv_l, __nv_bfl
   }
 }
 
+// As store_cols, in fp32 (partial results of a key split).
+template <int NCOLS>
+__device__ __forceinline__ void store_cols_f32(uint32_t taddr, float inv_l, float *orow,
+                                               bool live) {
+#pragma unroll 1
+  for (int cc = 0; cc < NCOLS; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+    if (live) {
+      uint4 *dst = reinterpret_cast<uint4 *>(orow + cc);
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+        dst[x] = make_uint4(__float_as_uint(__uint_as_float(o[4 * x]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * x + 1]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * x + 2]) * inv_l),
+                            __float_as_uint(__uint_as_float(o[4 * x + 3]) * inv_l));
+    }
+  }
+}
+
+// Decode: the producer warp copies the query rows of work unit (b, kv head
+// kvh) -- row r = query head kvh * group + r % group at position r / group --
+// into a Q buffer in the layout a 128-byte-swizzled tile load would give
+// (row r at byte 128 r of each 64-column chunk, 16-byte pieces XOR r % 8).
+// The other rows of the buffer stay zero.
+template <int D>
+__device__ __forceinline__ void gather_q(const Params &p, int b, int kvh, uint32_t dst) {
+  const int lane = threadIdx.x & 31;
+  const int G = p.group, rows = G * p.dq_n;
+  constexpr int PIECES = D / 8;   // 16-byte pieces per row
+  for (int idx = lane; idx < rows * PIECES; idx += 32) {
+    const int r = idx / PIECES, piece = idx % PIECES;
+    const long long src_row = ((long long)b * p.dq_n + r / G) * p.Hq + (long long)kvh * G + r % G;
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.q + src_row * D) + piece);
+    st_shared_v4(dst + (uint32_t)(piece >> 3) * CHUNK_BYTES + (uint32_t)r * 128u +
+                     ((uint32_t)((piece & 7) ^ (r & 7)) << 4),
+                 v);
+  }
+}
+
 // One 128x128xd QK^T into TMEM: A = Q tile (qdesc), B = K tile (kdesc), both
 // K-major in 64-column swizzle chunks.  Per step of 16 head-dim columns the
 // operands advance 32 bytes inside a 128-byte swizzle row, and CHUNK_BYTES
@@ -812,12 +889,15 @@ __device__ __forceinline__ long long pos_v(long long base, int i, int n) {
 // Persistent: with G = gridDim.x CTAs, CTA b processes one tile of each
 // round of G tiles of the longest-first list -- tile b of even rounds, tile
 // G-1-b of odd rounds -- until the producer publishes an invalid tile.
-template <int D, bool MOD>
+// KIND 0: plain; 1: score modifiers (soft cap, ALiBi); 2: decode (split keys).
+template <int D, int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D>;
+  constexpr bool MOD = KIND == 1;
+  constexpr bool DEC = KIND == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t base_s = smem_u32(smem);
@@ -866,13 +946,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     long long pos = 0;   // global ring position
     int q_loads = 0;     // Q tiles loaded so far (buffer q_loads % QB next)
     bool ok = true;
+    long long round = 0;
+    if (DEC) {   // padding rows of both Q buffers stay zero
+      for (uint32_t off = (uint32_t)lane * 16u; off < C::QB * C::TILE_BYTES; off += 512u)
+        st_shared_zero16(q_s + off);
+    }
     for (int k = 0; ok; ++k) {
-      // round k covers tiles [k G, (k+1) G); odd rounds run backwards so that
-      // the CTA given the longest tile of a round gets the shortest next
+      // round r covers units [r G, (r+1) G); odd rounds run backwards so that
+      // the CTA given the longest unit of a round gets the shortest next.
+      // Decode splits past the end of their sequence hold no keys: skipped.
       const long long G = gridDim.x;
-      const Tile t = decode_tile(p, (long long)k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x));
+      Tile t;
       int j_lo = 0, n = 0;
-      if (t.valid) kv_range(p, t.unit, t.len, j_lo, n);
+      for (;;) {
+        t = decode_tile(p, round * G + ((round & 1) ? G - 1 - blockIdx.x : blockIdx.x), DEC);
+        ++round;
+        if (!t.valid) break;
+        kv_range(p, t.unit, t.len, j_lo, n, DEC);
+        if (n > 0) break;
+      }
       if (lane == 0) {
         const int e = k % INFO_SLOTS;
         ok = wait_bounded(ctl.bar(BAR_INFO_EMPTY0 + e), ((uint32_t)(k / INFO_SLOTS) & 1u) ^ 1u,
@@ -889,19 +981,38 @@ __global__ void __launch_bounds__(THREADS, 1)
           dst[7] = (int)(t.lse_base >> 32);
           mbar_arrive(ctl.bar(BAR_INFO_FULL0 + e));   // release: the entry is visible
         }
+      }
+      const int qb = k % C::QB;
+      if (DEC) {
+        // Q buffer qb last served tile k - QB; then the warp gathers the
+        // group's query rows (head fastest) into it in the swizzled layout
+        if (lane == 0 && ok && t.valid && k >= C::QB)
+          ok = wait_bounded(ctl.bar(BAR_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
+                            abort_flag, p.timeout_ns);
+        if (__shfl_sync(0xffffffffu, (ok && t.valid) ? 1 : 0, 0)) {
+          gather_q<D>(p, t.seq_start, t.h, q_s + qb * C::TILE_BYTES);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl.bar(BAR_Q_FULL0 + qb));
+        }
+      }
+      if (lane == 0) {
         if (ok && t.valid) {
-          const int kvh = t.h / p.group;
-          const int qb = k % C::QB;
-          // Q buffer qb last served tile k - QB
-          if (k >= C::QB)
-            ok = wait_bounded(ctl.bar(BAR_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
-                              abort_flag, p.timeout_ns);
-          if (ok) {
-            ++q_loads;
-            mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL0 + qb), C::TILE_BYTES);
-            for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(q_s + qb * C::TILE_BYTES + c * CHUNK_BYTES, &tm_q,
-                          ctl.bar(BAR_Q_FULL0 + qb), c * 64, t.h, t.seq_start + t.unit * BM);
+          const int kvh = DEC ? t.h : t.h / p.group;
+          // first key row of the sequence in the K/V tensors
+          const int kv_row0 = DEC ? t.seq_start * p.dk_n : t.seq_start;
+          if (!DEC) {
+            // Q buffer qb last served tile k - QB
+            if (k >= C::QB)
+              ok = wait_bounded(ctl.bar(BAR_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
+                                abort_flag, p.timeout_ns);
+            if (ok) {
+              ++q_loads;
+              mbar_arrive_expect_tx(ctl.bar(BAR_Q_FULL0 + qb), C::TILE_BYTES);
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_3d(q_s + qb * C::TILE_BYTES + c * CHUNK_BYTES, &tm_q,
+                            ctl.bar(BAR_Q_FULL0 + qb), c * 64, t.h, t.seq_start + t.unit * BM);
+            }
           }
           // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
           for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
@@ -919,7 +1030,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
             for (int c = 0; c < C::CHUNKS; ++c)
               tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
-                          c * 64, kvh, t.seq_start + (j_lo + kt) * BN);
+                          c * 64, kvh, kv_row0 + (j_lo + kt) * BN);
           }
         }
       }
@@ -1039,11 +1150,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!t.valid) break;
       const int q_idx = t.qt * BM + row;            // row within the sequence
       int j_lo, n_unused;
-      kv_range(p, t.qt, t.len, j_lo, n_unused);
+      kv_range(p, t.qt, t.len, j_lo, n_unused, DEC);
+      // decode: the row is query head (kv head * group + row % group) at
+      // position row / group of the dq_n last positions; the split ends at
+      // key k_end, and causal rows see keys up to their own position
+      const int dq_pos = DEC ? row / p.group : 0;
+      const int k_end = DEC ? min(t.len, (t.qt + 1) * p.chunk) : t.len;
+      const int dec_lim =
+          (p.causal && dq_pos < p.dq_n) ? min(k_end, t.len - p.dq_n + dq_pos + 1) : k_end;
       // this row's visible keys [lo, lim); a tile needs masking when some
       // row of the query tile does not see all of its keys
-      const int lo = q_idx - p.wl;                                     // wl <= N
-      const int lim = p.wr >= t.len - q_idx ? t.len : q_idx + p.wr + 1;   // no overflow
+      const int lo = DEC ? 0 : q_idx - p.wl;                           // wl <= N
+      const int lim = DEC ? dec_lim
+                          : (p.wr >= t.len - q_idx ? t.len : q_idx + p.wr + 1);   // no overflow
       const int r0 = t.qt * BM;
       const float ak = (MOD && p.alibi) ? __ldg(p.alibi + t.h) / p.scale : 0.f;
       RowState st{-INFINITY, 0.f, 0.f};
@@ -1065,7 +1184,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // some row of the query tile misses keys of this tile: the sequence
         // ends inside it, or it reaches past the window of row r0 (right) or
         // of row r0 + BM - 1 (left)
-        if (kb + BN > t.len || kb + BN - 1 - r0 > p.wr || r0 + BM - 1 - kb > p.wl)
+        if (DEC ? (kb + BN > k_end || (p.causal && kb + BN - 1 > t.len - p.dq_n))
+                : (kb + BN > t.len || kb + BN - 1 - r0 > p.wr || r0 + BM - 1 - kb > p.wl))
           mask_half(hs, key0, lo, lim);
         const int pb = (int)(g & 1);
         StepBars sb;
@@ -1100,14 +1220,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         lr = st.lr + lr_other;
       }
       const float l = st.l + l_other;
-      const bool live = q_idx < t.len;
-      store_cols<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
-                     p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D +
-                         OC * half,
-                     live);
-      if (live && half == 0) {
-        const float m_use = (st.m == -INFINITY) ? 0.f : st.m;
-        p.lse[t.lse_base + q_idx] = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
+      const float m_use = (st.m == -INFINITY) ? 0.f : st.m;
+      const float lse_val = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
+      if (DEC) {
+        // row -> (position, query head); o [B, dq_n, Hq, d], lse [B, Hq, dq_n]
+        const bool live = row < p.group * p.dq_n;
+        const int hq = t.h * p.group + row % p.group;
+        const long long lrow = ((long long)t.seq_start * p.Hq + hq) * p.dq_n + dq_pos;
+        if (p.splits == 1) {
+          store_cols<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
+                         p.o + (((long long)t.seq_start * p.dq_n + dq_pos) * p.Hq + hq) * D +
+                             OC * half,
+                         live);
+          if (live && half == 0) p.lse[lrow] = lse_val;
+        } else {   // partial state of this split: O / l and its LSE
+          store_cols_f32<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
+                             p.ws_o + (lrow * p.splits + t.qt) * D + OC * half, live);
+          if (live && half == 0) p.ws_lse[lrow * p.splits + t.qt] = lse_val;
+        }
+      } else {
+        const bool live = q_idx < t.len;
+        store_cols<OC>(tmem + lane_off + C::COL_O + OC * half, lr > 0.f ? 1.f / lr : 0.f,
+                       p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D +
+                           OC * half,
+                       live);
+        if (live && half == 0) p.lse[t.lse_base + q_idx] = lse_val;
       }
       tc_fence_before();
       warp_arrive(ctl.bar(BAR_O_FREE));
@@ -1134,6 +1271,47 @@ __global__ void selftest_timeout_kernel(unsigned long long timeout_ns) {
   }
   __syncthreads();
   wait_bounded(smem_u32(&barrier_word), 0, &abort_word, timeout_ns);
+}
+
+// Decode with several key splits: merge the partial states of each row
+// (one warp per row) with the online-softmax combine in (LSE, O) form:
+// LSE = log sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  Splits past a
+// sequence's end hold nothing and are skipped.
+template <int D>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)p.B * p.Hq * p.dq_n;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // (b Hq + h) dq_n + r
+  if (row >= rows) return;
+  const int b = (int)(row / ((long long)p.Hq * p.dq_n));
+  const int h = (int)((row / p.dq_n) % p.Hq);
+  const int r = (int)(row % p.dq_n);
+  const int L = p.seqlens_k ? __ldg(p.seqlens_k + b) : p.dk_n;
+  if (L < p.dq_n || L > p.dk_n) return;   // reported by the attention kernel
+  const int ns = (L + p.chunk - 1) / p.chunk;
+  const float *lse_s = p.ws_lse + row * p.splits;
+  float m = -INFINITY;
+  for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse_s[s]);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  constexpr int PER = D / 32;   // columns per lane
+  float acc[PER];
+#pragma unroll
+  for (int x = 0; x < PER; ++x) acc[x] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float w = expf(lse_s[s] - m);
+      wsum += w;
+      const float *os = p.ws_o + (row * p.splits + s) * D + lane * PER;
+#pragma unroll
+      for (int x = 0; x < PER; ++x) acc[x] += w * os[x];
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16 *dst = p.o + (((long long)b * p.dq_n + r) * p.Hq + h) * D + lane * PER;
+#pragma unroll
+  for (int x = 0; x < PER; ++x) dst[x] = __float2bfloat16_rn(acc[x] * inv);
+  if (lane == 0) p.lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host
@@ -1201,12 +1379,15 @@ static attn_status prepare_device(int dev) {
           cudaSuccess ||
       g_sm_count[dev] < 1)
     return ATTN_ERR_CUDA;
-  if (!opt_in_smem(attn_fwd_kernel<64, false>, Cfg<64>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<128, false>, Cfg<128>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<256, false>, Cfg<256>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<64, true>, Cfg<64>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<128, true>, Cfg<128>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<256, true>, Cfg<256>::SMEM_BYTES))
+  if (!opt_in_smem(attn_fwd_kernel<64, 0>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, 0>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, 0>, Cfg<256>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<64, 1>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, 1>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, 1>, Cfg<256>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<64, 2>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, 2>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, 2>, Cfg<256>::SMEM_BYTES))
     return ATTN_ERR_CUDA;
   state[dev] = 1;
   return ATTN_OK;
@@ -1305,14 +1486,120 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
 
   const unsigned gr = (unsigned)grid;
   switch (d * 2 + (mod ? 1 : 0)) {
-    case 128: attn_fwd_kernel<64, false><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
-    case 129: attn_fwd_kernel<64, true><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
-    case 256: attn_fwd_kernel<128, false><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
-    case 257: attn_fwd_kernel<128, true><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
-    case 512: attn_fwd_kernel<256, false><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
-    default: attn_fwd_kernel<256, true><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 128: attn_fwd_kernel<64, 0><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 129: attn_fwd_kernel<64, 1><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 256: attn_fwd_kernel<128, 0><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 257: attn_fwd_kernel<128, 1><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    case 512: attn_fwd_kernel<256, 0><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
+    default: attn_fwd_kernel<256, 1><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+namespace attn {
+// Key splits of a decode launch: about two units per SM, whole key tiles.
+static void decode_splits(int B, int Hkv, int Nk, int sms, int &splits, int &chunk) {
+  const long long per = (long long)B * Hkv;
+  long long want = (2LL * sms + per - 1) / per;
+  const int tiles = (Nk + BN - 1) / BN;
+  if (want > tiles) want = tiles;
+  if (want < 1) want = 1;
+  chunk = (int)(((tiles + want - 1) / want) * BN);
+  splits = (Nk + chunk - 1) / chunk;
+}
+
+static size_t decode_ws_bytes(int B, int Hq, int Nq, int d, int splits) {
+  if (splits <= 1) return 0;
+  return (size_t)B * Hq * Nq * splits * ((size_t)d + 1) * sizeof(float);
+}
+}  // namespace attn
+
+extern "C" size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  using namespace attn;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || prepare_device(dev) != ATTN_OK) return 0;
+  int splits, chunk;
+  decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  return decode_ws_bytes(B, Hq, Nq, d, splits);
+}
+
+extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o,
+                                       float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                       float scale, int causal, const int *seqlens_k,
+                                       void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
+  using namespace attn;
+  if (B < 0 || Nq < 0 || Nk < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((long long)(Hq / Hkv) * Nq > BM || Nq > Nk) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Nq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void *ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+      misaligned(lse, 4) || misaligned(seqlens_k, 4) || misaligned(workspace, 16))
+    return ATTN_ERR_ALIGNMENT;
+  const long long krows = (long long)B * Nk;
+  if (krows > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn_status st = prepare_device(dev);
+  if (st != ATTN_OK) return st;
+  int splits, chunk;
+  decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  const size_t need = decode_ws_bytes(B, Hq, Nq, d, splits);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!make_map(enc, &mk, k, Hkv, krows, d) || !make_map(enc, &mv, v, Hkv, krows, d))
+    return ATTN_ERR_INVALID_ARG;
+
+  Params p{};
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+  p.o = reinterpret_cast<__nv_bfloat16 *>(o);
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = Nk;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.dq_n = Nq;
+  p.dk_n = Nk;
+  p.splits = splits;
+  p.chunk = chunk;
+  p.seqlens_k = seqlens_k;
+  p.ws_o = reinterpret_cast<float *>(workspace);
+  p.ws_lse = need > 0 ? p.ws_o + (size_t)B * Hq * Nq * splits * d : nullptr;
+  p.unit_rows = BM;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_timeout_ns();
+
+  const long long units = (long long)B * Hkv * splits;
+  const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
+  const unsigned gr = (unsigned)grid;
+  switch (d) {   // no Q tensor map: decode gathers its query rows
+    case 64: attn_fwd_kernel<64, 2><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    case 128: attn_fwd_kernel<128, 2><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    default: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (splits > 1) {
+    const unsigned cg = (unsigned)(((long long)B * Hq * Nq + 7) / 8);
+    switch (d) {
+      case 64: attn_combine_kernel<64><<<cg, 256, 0, stream>>>(p); break;
+      case 128: attn_combine_kernel<128><<<cg, 256, 0, stream>>>(p); break;
+      default: attn_combine_kernel<256><<<cg, 256, 0, stream>>>(p); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
 }
 
 extern "C" attn_status attn_get_status(cudaStream_t stream) {

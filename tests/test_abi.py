@@ -108,3 +108,30 @@ def test_variant_struct_layout():
     import ctypes
     assert ctypes.sizeof(pkg.AttnVariant) == 24
     assert pkg.AttnVariant.alibi_slopes.offset == 16
+
+
+def call_dec(**kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=2, Hq=8, Hkv=2, Nq=1,
+                Nk=4096, d=128, scale=0.088, causal=0, seqlens_k=None, workspace=0x7000,
+                workspace_bytes=1 << 20, stream=0)
+    args.update(kw)
+    return pkg.attn_fwd_decode(check=False, **args)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(d=96), dict(Hq=6, Hkv=4), dict(Nq=33, Hq=8, Hkv=2),   # group x Nq > 128
+    dict(Nq=5, Nk=4), dict(B=-1), dict(scale=0.0), dict(q=None), dict(lse=None),
+    dict(Nk=1 << 30, B=4),
+])
+def test_decode_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert call_dec(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(q=0x1008), dict(workspace=0x7004), dict(seqlens_k=0x6002)])
+def test_decode_misaligned_pointers_rejected(lib, kw):
+    assert call_dec(**kw) == pkg.ATTN_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Nq=0)])
+def test_decode_empty_problem_is_a_no_op(lib, kw):
+    assert call_dec(**kw) == pkg.ATTN_OK
