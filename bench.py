@@ -237,6 +237,79 @@ def run_workload(pkg, W, wl, seed, steps, warmup, dev, flush, sample_clocks=Fals
                 tensors=(q, k, v, o, lse, cu), step=step)
 
 
+def time_steps(step, steps, warmup, flush, stream):
+    """CUDA-event times (ms) of `steps` calls of step(), L2 flushed before each."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+
+
+def run_window(pkg, dev, flush, steps):
+    """Causal sliding window of 128 keys (tang, section 7.3's variant table:
+    n = 8k, d = 64) against full causal attention on the same inputs; FLOPs
+    count the visible (query, key) pairs only, 4 d per pair."""
+    import torch
+    B, H, N, d, Wn = 4, 16, 8192, 64, 128
+    g = torch.Generator().manual_seed(2001)
+    q, k, v = (torch.randn((B, N, H, d), generator=g).to(torch.bfloat16).to(dev)
+               for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    win = lambda: pkg.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, d ** -0.5, True,
+                                  window=(Wn - 1, -1), stream=stream.cuda_stream)
+    full = lambda: pkg.attn_fwd(q, k, v, o, lse, B, H, H, N, d, d ** -0.5, True,
+                                stream=stream.cuda_stream)
+    tw = statistics.median(time_steps(win, steps, 3, flush, stream))
+    tf = statistics.median(time_steps(full, steps, 3, flush, stream))
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"window run: {pkg.attn_status_string(st)}")
+    pairs = B * H * (Wn * N - Wn * (Wn - 1) // 2)
+    return {"workload": f"sliding window {Wn} causal B{B} H{H} N{N} d{d}",
+            "tflops": round(4 * d * pairs / (tw / 1e3) / 1e12, 2), "ms_per_step": round(tw, 5),
+            "full_causal_ms_per_step": round(tf, 5)}
+
+
+def run_decode(pkg, dev, flush, steps, hbm_gbs):
+    """Decode step: one new query per sequence against full key/value caches
+    (split keys + merge).  HBM-bound: GB/s of the bytes that must move (K, V
+    caches read once, Q read, O and LSE written)."""
+    import torch
+    B, Hq, Hkv, d, Nk, Nq = 16, 32, 8, 128, 8192, 1
+    g = torch.Generator().manual_seed(2002)
+    q = torch.randn((B, Nq, Hq, d), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((B, Nk, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, Nk, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    n = pkg.attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+    ws = torch.empty(((max(n, 16) + 15) // 16 * 4,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: pkg.attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, d ** -0.5,
+                                       False, None, ws, stream=stream.cuda_stream)
+    t = statistics.median(time_steps(step, steps, 3, flush, stream))
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"decode run: {pkg.attn_status_string(st)}")
+    nbytes = 2 * k.numel() * 2 + 2 * q.numel() * 2 + lse.numel() * 4
+    gbs = nbytes / (t / 1e3) / 1e9
+    return {"workload": f"decode B{B} Hq{Hq} Hkv{Hkv} d{d} Nq{Nq} Nk{Nk} (full caches)",
+            "gbs": round(gbs, 1), "ms_per_step": round(t, 5), "bytes_per_step": nbytes,
+            "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
+            "workspace_bytes": n}
+
+
 def run_e2e(pkg, W, wl, inp, dev, steps):
     """Same metric through the public C ABI with host buffers: every step
     copies Q, K, V from pinned host memory, runs attn_fwd and reads O and LSE
@@ -363,6 +436,9 @@ def native(args):
             per_workload[key] = {"workload": other.name, "tflops": round(tf, 2),
                                  "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peak, 4)}
             del rr
+        per_workload["window"] = run_window(pkg, dev, flush, min(args.steps, 20))
+        per_workload["decode"] = run_decode(pkg, dev, flush, min(args.steps, 20),
+                                            peaks.get("hbm_gbs"))
 
     base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
