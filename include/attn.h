@@ -160,6 +160,30 @@ attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o
                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_fwd_decode_static -- attn_fwd_decode without a caller workspace and
+ * without any allocation: the partial states live in a fixed 8 MiB device
+ * array inside the library (one per device).  The pages have no
+ * counterpart; this exists for callers that cannot provide or allocate
+ * memory (for example inside a captured CUDA graph).
+ *
+ *   - Problems whose attn_decode_workspace_bytes() exceeds 8 MiB
+ *     (8388608 bytes) are rejected with ATTN_ERR_INVALID_ARG.
+ *   - The array's address is looked up once per device, on the first call
+ *     of any entry point on that device; make that first call outside
+ *     stream capture.
+ *   - Nothing in the array needs to start at zero: every slot the merge
+ *     kernel reads is written earlier in the same call.
+ *   - Calls that overlap in time on one device (different streams, or host
+ *     threads) race on the array: serialise them, e.g. on one stream.
+ *
+ * Other arguments, layouts and errors as attn_fwd_decode.
+ */
+attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v, void *o,
+                                   float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                   float scale, int causal, const int *seqlens_k,
+                                   cudaStream_t stream);
+
+/*
  * attn_get_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.

@@ -38,7 +38,8 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_BAD_SEQLENS = 6
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
-            "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
+            "attn_fwd_decode_static", "attn_get_status", "attn_status_string",
+            "attn_selftest_timeout"]
 
 
 class AttnVariant(ctypes.Structure):
@@ -91,6 +92,9 @@ def _load():
         lib.attn_fwd_decode.restype = i
         lib.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float, i,
                                         vp, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_decode_static.restype = i
+        lib.attn_fwd_decode_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                               ctypes.c_float, i, vp, vp]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
@@ -188,6 +192,23 @@ def attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqle
                                  int(workspace_bytes), _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_decode")
+    return rc
+
+
+DECODE_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def attn_fwd_decode_static(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k=None,
+                           stream=None, check=True) -> int:
+    """Call the C ``attn_fwd_decode_static``: attn_fwd_decode with the
+    library's fixed 8 MiB scratch instead of a workspace (no allocation;
+    overlapping calls on one device race)."""
+    rc = _load().attn_fwd_decode_static(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                        int(Hq), int(Hkv), int(Nq), int(Nk), int(d),
+                                        float(scale), int(bool(causal)), _ptr(seqlens_k),
+                                        _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_decode_static")
     return rc
 
 

@@ -1360,6 +1360,13 @@ static bool opt_in_smem(K kernel, uint32_t bytes) {
 // kernel instantiations, done once.
 static int g_sm_count[MAX_DEVICES];
 
+// Scratch of attn_fwd_decode_static: a fixed device array (the library
+// allocates nothing); its address on each device is looked up once, when
+// the device is first prepared.
+constexpr size_t DECODE_SCRATCH_BYTES = 8u << 20;
+static __device__ __align__(256) float g_decode_scratch[DECODE_SCRATCH_BYTES / sizeof(float)];
+static void *g_scratch_ptr[MAX_DEVICES];
+
 static attn_status prepare_device(int dev) {
   static std::mutex mu;
   static signed char state[MAX_DEVICES];   // 0 unknown, 1 ready, -1 unsupported
@@ -1388,6 +1395,8 @@ static attn_status prepare_device(int dev) {
       !opt_in_smem(attn_fwd_kernel<64, 2>, Cfg<64>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<128, 2>, Cfg<128>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<256, 2>, Cfg<256>::SMEM_BYTES))
+    return ATTN_ERR_CUDA;
+  if (cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch) != cudaSuccess)
     return ATTN_ERR_CUDA;
   state[dev] = 1;
   return ATTN_OK;
@@ -1524,12 +1533,12 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, in
   return decode_ws_bytes(B, Hq, Nq, d, splits);
 }
 
-extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o,
-                                       float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                                       float scale, int causal, const int *seqlens_k,
-                                       void *workspace, size_t workspace_bytes,
-                                       cudaStream_t stream) {
-  using namespace attn;
+namespace attn {
+// The decode call; with use_static the workspace is the fixed device array.
+static attn_status decode_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                               int causal, const int *seqlens_k, void *workspace,
+                               size_t workspace_bytes, bool use_static, cudaStream_t stream) {
   if (B < 0 || Nq < 0 || Nk < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1552,6 +1561,10 @@ extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void 
   int splits, chunk;
   decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
   const size_t need = decode_ws_bytes(B, Hq, Nq, d, splits);
+  if (use_static) {
+    workspace = g_scratch_ptr[dev];
+    workspace_bytes = DECODE_SCRATCH_BYTES;
+  }
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
@@ -1600,6 +1613,24 @@ extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void 
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
+}
+}  // namespace attn
+
+extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o,
+                                       float *lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                       float scale, int causal, const int *seqlens_k,
+                                       void *workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
+  return attn::decode_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
+                           workspace, workspace_bytes, false, stream);
+}
+
+extern "C" attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v,
+                                              void *o, float *lse, int B, int Hq, int Hkv,
+                                              int Nq, int Nk, int d, float scale, int causal,
+                                              const int *seqlens_k, cudaStream_t stream) {
+  return attn::decode_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
+                           nullptr, 0, true, stream);
 }
 
 extern "C" attn_status attn_get_status(cudaStream_t stream) {
