@@ -525,6 +525,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows-per-head", type=int, default=24)
+    ap.add_argument("--extra", choices=["window", "decode"], default=None,
+                    help="time only this extra path (one JSON line; for profiling)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -533,9 +535,25 @@ def parse_args(argv=None):
     return a
 
 
+def extra_only(args):
+    import torch
+    import tensor_program_compilers_gb300 as pkg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkg.build()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.extra == "window":
+        out = run_window(pkg, dev, flush, args.steps)
+    else:
+        out = run_decode(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.extra:
+        extra_only(args)
+    elif args.impl == "reference":
         reference(args)
     else:
         native(args)
