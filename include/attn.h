@@ -53,7 +53,8 @@ typedef enum {
   ATTN_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
   ATTN_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed           */
   ATTN_ERR_TIMEOUT = 5,            /* a kernel pipeline wait ran out (device-side) */
-  ATTN_ERR_BAD_SEQLENS = 6         /* cu_seqlens inconsistent (device-side check)  */
+  ATTN_ERR_BAD_SEQLENS = 6,        /* cu_seqlens inconsistent (device-side check)  */
+  ATTN_ERR_BAD_PAGE_TABLE = 7      /* a page number outside the cache (device-side) */
 } attn_status;
 
 /*
@@ -158,6 +159,38 @@ attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o
                             int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
                             int causal, const int *seqlens_k, void *workspace,
                             size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_fwd_decode_paged -- attn_fwd_decode reading paged key/value caches
+ * (tang, section 2.1 "Views": a paged KV cache is a gathered read, the page
+ * number of a key being data read from an index tensor; Table 1 row "paged
+ * KV cache").
+ *
+ *   k_cache, v_cache: device bf16 [num_pages, page_size, Hkv, d], 16-byte
+ *              aligned.  Rows of pages past a sequence's length must hold
+ *              finite values (they are read, weighted by zero).
+ *   seqlens_k: device int32[B] (required), Nq <= seqlens_k[b] <=
+ *              max_blocks * page_size.
+ *   block_table: device int32[B * max_blocks] (4-byte aligned): key j of
+ *              sequence b is row j % page_size of page
+ *              block_table[b * max_blocks + j / page_size].  Entries past
+ *              a sequence's last page are not read.  A page number outside
+ *              [0, num_pages) is reported as ATTN_ERR_BAD_PAGE_TABLE through
+ *              attn_get_status (its keys then read as zeros).
+ *   page_size: 16, 32 or 64, or a multiple of 128.
+ *   workspace: at least attn_decode_paged_workspace_bytes(B, Hq, Hkv, Nq,
+ *              max_blocks, page_size, d) bytes (may be NULL when that is 0).
+ *
+ * Everything else as attn_fwd_decode.
+ */
+size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq, int max_blocks,
+                                         int page_size, int d);
+attn_status attn_fwd_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                                  void *o, float *lse, int B, int Hq, int Hkv, int Nq, int d,
+                                  float scale, int causal, const int *seqlens_k,
+                                  const int *block_table, int max_blocks, int page_size,
+                                  int num_pages, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
 
 /*
  * attn_fwd_decode_static -- attn_fwd_decode without a caller workspace and

@@ -201,3 +201,27 @@ def attn_decode_oracle(q, k, v, seqlens_k, causal, scale, nthreads=0, lib=None):
                             [b * Nk for b in range(B)], kl, Hq, Hkv, d, scale, causal,
                             nthreads=nthreads, lib=lib)
     return o.reshape(B, Nq, Hq, d), lse.reshape(B, Nq, Hq).transpose(0, 2, 1).copy()
+
+
+def attn_decode_paged_oracle(q, k_cache, v_cache, seqlens_k, block_table, page_size, causal,
+                             scale, nthreads=0, lib=None):
+    """The decode oracle over paged caches (tang, section 2.1 "Views": a paged
+    KV cache is a gathered read -- the page holding key j is data, read from
+    the block table).  Key j of sequence b is row j % page_size of page
+    block_table[b, j // page_size] of k_cache, v_cache [num_pages, page_size,
+    Hkv, d]; the gathered rows form ordinary caches for attn_decode_oracle.
+    """
+    import torch
+    table = torch.as_tensor(np.asarray(block_table), dtype=torch.long)
+    B, max_blocks = table.shape
+    Nk = max_blocks * page_size
+    kl = [int(x) for x in np.asarray(seqlens_k).reshape(-1)]
+    Hkv, d = k_cache.shape[2], k_cache.shape[3]
+    k = torch.zeros((B, Nk, Hkv, d), dtype=k_cache.dtype)
+    v = torch.zeros((B, Nk, Hkv, d), dtype=v_cache.dtype)
+    for b in range(B):
+        for j in range(kl[b]):
+            page = int(table[b, j // page_size])
+            k[b, j] = k_cache[page, j % page_size]
+            v[b, j] = v_cache[page, j % page_size]
+    return attn_decode_oracle(q, k, v, kl, causal, scale, nthreads=nthreads, lib=lib)

@@ -36,8 +36,10 @@ ATTN_ERR_UNSUPPORTED_DEVICE = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_BAD_SEQLENS = 6
+ATTN_ERR_BAD_PAGE_TABLE = 7
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
+            "attn_fwd_decode_paged", "attn_decode_paged_workspace_bytes",
             "attn_fwd_decode_static", "attn_get_status", "attn_status_string",
             "attn_selftest_timeout"]
 
@@ -95,6 +97,11 @@ def _load():
         lib.attn_fwd_decode_static.restype = i
         lib.attn_fwd_decode_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                                ctypes.c_float, i, vp, vp]
+        lib.attn_fwd_decode_paged.restype = i
+        lib.attn_fwd_decode_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i,
+                                              vp, vp, i, i, i, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_paged_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
@@ -192,6 +199,31 @@ def attn_fwd_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqle
                                  int(workspace_bytes), _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_decode")
+    return rc
+
+
+def attn_decode_paged_workspace_bytes(B, Hq, Hkv, Nq, max_blocks, page_size, d) -> int:
+    """Workspace bytes ``attn_fwd_decode_paged`` needs on the current device."""
+    return int(_load().attn_decode_paged_workspace_bytes(int(B), int(Hq), int(Hkv), int(Nq),
+                                                         int(max_blocks), int(page_size), int(d)))
+
+
+def attn_fwd_decode_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nq, d, scale, causal,
+                          seqlens_k, block_table, max_blocks, page_size, num_pages,
+                          workspace=None, workspace_bytes=None, stream=None, check=True) -> int:
+    """Call the C ``attn_fwd_decode_paged``: decode over paged caches
+    k_cache, v_cache [num_pages, page_size, Hkv, d] addressed through
+    block_table [B, max_blocks] (int32, device) and seqlens_k [B]."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = _load().attn_fwd_decode_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+        int(Nq), int(d), float(scale), int(bool(causal)), _ptr(seqlens_k), _ptr(block_table),
+        int(max_blocks), int(page_size), int(num_pages), _ptr(workspace), int(workspace_bytes),
+        _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_decode_paged")
     return rc
 
 

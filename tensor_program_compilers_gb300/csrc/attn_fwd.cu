@@ -174,6 +174,11 @@ struct Params {
   // rows = the group's query heads x dq_n positions (head fastest).
   int dq_n, dk_n, splits, chunk;
   const int *seqlens_k;
+  // paged caches (KIND 3): k, v [num_pages, page_size, Hkv, d]; key j of
+  // sequence b is row j % page_size of page block_table[b * max_blocks +
+  // j / page_size]; dk_n = max_blocks * page_size
+  const int *block_table;
+  int max_blocks, page_size, num_pages;
   float *ws_o;          // splits > 1: partial O / l [B, Hq, dq_n, splits, d]
   float *ws_lse;        // and partial LSE [B, Hq, dq_n, splits]
   int unit_rows;        // query rows per CTA work unit (one tile)
@@ -889,7 +894,8 @@ __device__ __forceinline__ long long pos_v(long long base, int i, int n) {
 // Persistent: with G = gridDim.x CTAs, CTA b processes one tile of each
 // round of G tiles of the longest-first list -- tile b of even rounds, tile
 // G-1-b of odd rounds -- until the producer publishes an invalid tile.
-// KIND 0: plain; 1: score modifiers (soft cap, ALiBi); 2: decode (split keys).
+// KIND 0: plain; 1: score modifiers (soft cap, ALiBi); 2: decode (split
+// keys); 3: decode from paged caches.
 template <int D, int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -897,7 +903,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D>;
   constexpr bool MOD = KIND == 1;
-  constexpr bool DEC = KIND == 2;
+  constexpr bool DEC = KIND >= 2;
+  constexpr bool PAGED = KIND == 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t base_s = smem_u32(smem);
@@ -1028,9 +1035,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
             ATTN_TRACE_EV(10, pos >> 2, (int)(pos & 3));
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
-            for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
-                          c * 64, kvh, kv_row0 + (j_lo + kt) * BN);
+            if (PAGED) {
+              // the tile's keys come in boxes of min(page, 128) rows, each from
+              // its page; keys past the sequence (and bad page numbers) read a
+              // box wholly outside the tensor, i.e. zeros
+              const int rows = min(p.page_size, BN);
+              for (int r = 0; r < BN; r += rows) {
+                const int j = (j_lo + kt) * BN + r;
+                int page = -1;
+                if (j < t.len) {
+                  page = __ldg(p.block_table + (long long)t.seq_start * p.max_blocks +
+                               j / p.page_size);
+                  if (page < 0 || page >= p.num_pages) {
+                    record_status(ATTN_ERR_BAD_PAGE_TABLE);
+                    page = -1;
+                  }
+                }
+                const int row = page < 0 ? -rows : page * p.page_size + j % p.page_size;
+                for (int c = 0; c < C::CHUNKS; ++c)
+                  tma_load_3d(dst + c * CHUNK_BYTES + (uint32_t)r * 128u, is_v ? &tm_v : &tm_k,
+                              ctl.bar(BAR_RING + slot), c * 64, kvh, row);
+              }
+            } else {
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
+                            c * 64, kvh, kv_row0 + (j_lo + kt) * BN);
+            }
           }
         }
       }
@@ -1337,10 +1367,10 @@ static EncodeTiledFn get_encode_fn() {
 
 // [rows, heads, d] bf16, boxes of 128 rows x 64 columns of one head.
 static bool make_map(EncodeTiledFn enc, CUtensorMap *m, const void *base, int heads,
-                     long long rows, int d) {
+                     long long rows, int d, int box_rows = BM) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * (cuuint64_t)d * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)BM};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1394,7 +1424,10 @@ static attn_status prepare_device(int dev) {
       !opt_in_smem(attn_fwd_kernel<256, 1>, Cfg<256>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<64, 2>, Cfg<64>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<128, 2>, Cfg<128>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<256, 2>, Cfg<256>::SMEM_BYTES))
+      !opt_in_smem(attn_fwd_kernel<256, 2>, Cfg<256>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<64, 3>, Cfg<64>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<128, 3>, Cfg<128>::SMEM_BYTES) ||
+      !opt_in_smem(attn_fwd_kernel<256, 3>, Cfg<256>::SMEM_BYTES))
     return ATTN_ERR_CUDA;
   if (cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -1535,10 +1568,18 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, in
 
 namespace attn {
 // The decode call; with use_static the workspace is the fixed device array.
+struct PagedArgs {
+  const int *block_table;
+  int max_blocks, page_size, num_pages;
+};
+
+// The decode call; with use_static the workspace is the fixed device array;
+// with pg the caches are paged (Nk = max_blocks * page_size).
 static attn_status decode_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                                int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
                                int causal, const int *seqlens_k, void *workspace,
-                               size_t workspace_bytes, bool use_static, cudaStream_t stream) {
+                               size_t workspace_bytes, bool use_static, const PagedArgs *pg,
+                               cudaStream_t stream) {
   if (B < 0 || Nq < 0 || Nk < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -1551,7 +1592,7 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
       misaligned(lse, 4) || misaligned(seqlens_k, 4) || misaligned(workspace, 16))
     return ATTN_ERR_ALIGNMENT;
-  const long long krows = (long long)B * Nk;
+  const long long krows = pg ? (long long)pg->num_pages * pg->page_size : (long long)B * Nk;
   if (krows > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -1569,7 +1610,9 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
   CUtensorMap mk, mv;
-  if (!make_map(enc, &mk, k, Hkv, krows, d) || !make_map(enc, &mv, v, Hkv, krows, d))
+  const int box_rows = pg ? std::min(pg->page_size, BN) : BM;
+  if (!make_map(enc, &mk, k, Hkv, krows, d, box_rows) ||
+      !make_map(enc, &mv, v, Hkv, krows, d, box_rows))
     return ATTN_ERR_INVALID_ARG;
 
   Params p{};
@@ -1587,6 +1630,12 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   p.splits = splits;
   p.chunk = chunk;
   p.seqlens_k = seqlens_k;
+  if (pg) {
+    p.block_table = pg->block_table;
+    p.max_blocks = pg->max_blocks;
+    p.page_size = pg->page_size;
+    p.num_pages = pg->num_pages;
+  }
   p.ws_o = reinterpret_cast<float *>(workspace);
   p.ws_lse = need > 0 ? p.ws_o + (size_t)B * Hq * Nq * splits * d : nullptr;
   p.unit_rows = BM;
@@ -1597,10 +1646,13 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   const long long units = (long long)B * Hkv * splits;
   const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
   const unsigned gr = (unsigned)grid;
-  switch (d) {   // no Q tensor map: decode gathers its query rows
-    case 64: attn_fwd_kernel<64, 2><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    case 128: attn_fwd_kernel<128, 2><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    default: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+  switch (d * 2 + (pg ? 1 : 0)) {   // no Q tensor map: decode gathers its query rows
+    case 128: attn_fwd_kernel<64, 2><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    case 129: attn_fwd_kernel<64, 3><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    case 256: attn_fwd_kernel<128, 2><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    case 257: attn_fwd_kernel<128, 3><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    case 512: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    default: attn_fwd_kernel<256, 3><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   if (splits > 1) {
@@ -1622,7 +1674,36 @@ extern "C" attn_status attn_fwd_decode(const void *q, const void *k, const void 
                                        void *workspace, size_t workspace_bytes,
                                        cudaStream_t stream) {
   return attn::decode_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
-                           workspace, workspace_bytes, false, stream);
+                           workspace, workspace_bytes, false, nullptr, stream);
+}
+
+extern "C" size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int Nq,
+                                                     int max_blocks, int page_size, int d) {
+  const long long nk = (long long)max_blocks * page_size;
+  if (max_blocks < 1 || page_size < 1 || nk > 0x7FFFFFFFLL) return 0;
+  return attn_decode_workspace_bytes(B, Hq, Hkv, Nq, (int)nk, d);
+}
+
+extern "C" attn_status attn_fwd_decode_paged(const void *q, const void *k_cache,
+                                             const void *v_cache, void *o, float *lse, int B,
+                                             int Hq, int Hkv, int Nq, int d, float scale,
+                                             int causal, const int *seqlens_k,
+                                             const int *block_table, int max_blocks,
+                                             int page_size, int num_pages, void *workspace,
+                                             size_t workspace_bytes, cudaStream_t stream) {
+  // pages of 16, 32 or 64 rows fill a 128-key tile with several boxes;
+  // pages of a multiple of 128 rows hold whole tiles
+  constexpr int BN = attn::BN;
+  const bool page_ok = page_size >= 16 && ((BN % page_size == 0 && (page_size & 15) == 0) ||
+                                           page_size % BN == 0);
+  if (!page_ok || max_blocks < 1 || num_pages < 1 || !seqlens_k || !block_table)
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)max_blocks * page_size > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_table) & 3u) return ATTN_ERR_ALIGNMENT;
+  const attn::PagedArgs pg{block_table, max_blocks, page_size, num_pages};
+  return attn::decode_impl(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nq, max_blocks * page_size,
+                           d, scale, causal, seqlens_k, workspace, workspace_bytes, false, &pg,
+                           stream);
 }
 
 extern "C" attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v,
@@ -1630,7 +1711,7 @@ extern "C" attn_status attn_fwd_decode_static(const void *q, const void *k, cons
                                               int Nq, int Nk, int d, float scale, int causal,
                                               const int *seqlens_k, cudaStream_t stream) {
   return attn::decode_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, seqlens_k,
-                           nullptr, 0, true, stream);
+                           nullptr, 0, true, nullptr, stream);
 }
 
 extern "C" attn_status attn_get_status(cudaStream_t stream) {
@@ -1668,6 +1749,7 @@ extern "C" const char *attn_status_string(attn_status s) {
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
     case ATTN_ERR_BAD_SEQLENS: return "ATTN_ERR_BAD_SEQLENS";
+    case ATTN_ERR_BAD_PAGE_TABLE: return "ATTN_ERR_BAD_PAGE_TABLE";
   }
   return "ATTN_UNKNOWN_STATUS";
 }

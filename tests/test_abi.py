@@ -135,3 +135,28 @@ def test_decode_misaligned_pointers_rejected(lib, kw):
 @pytest.mark.parametrize("kw", [dict(B=0), dict(Nq=0)])
 def test_decode_empty_problem_is_a_no_op(lib, kw):
     assert call_dec(**kw) == pkg.ATTN_OK
+
+
+def call_paged(**kw):
+    args = dict(q=0x1000, k_cache=0x2000, v_cache=0x3000, o=0x4000, lse=0x5000, B=2, Hq=8,
+                Hkv=2, Nq=1, d=128, scale=0.088, causal=0, seqlens_k=0x6000,
+                block_table=0x7000, max_blocks=64, page_size=64, num_pages=200,
+                workspace=0x8000, workspace_bytes=1 << 20, stream=0)
+    args.update(kw)
+    return pkg.attn_fwd_decode_paged(check=False, **args)
+
+
+@pytest.mark.parametrize("kw", [dict(page_size=8), dict(page_size=48), dict(page_size=96),
+                                dict(page_size=200), dict(max_blocks=0), dict(num_pages=0),
+                                dict(seqlens_k=None), dict(block_table=None), dict(d=80),
+                                dict(Nq=40)])
+def test_paged_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert call_paged(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_paged_misaligned_table_rejected(lib):
+    assert call_paged(block_table=0x7002) == pkg.ATTN_ERR_ALIGNMENT
+
+
+def test_paged_status_string(lib):
+    assert pkg.attn_status_string(7) == "ATTN_ERR_BAD_PAGE_TABLE"

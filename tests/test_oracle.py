@@ -559,3 +559,46 @@ def test_decode_ignores_cache_rows_past_the_length():
     o2, l2 = oracle.attn_decode_oracle(q, k2, v2, [9], False, 0.5)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# paged caches: the page holding a key is read from the block table
+# ---------------------------------------------------------------------------
+def test_paged_decode_identity_table_is_plain_decode():
+    B, Nq, Hq, Hkv, d, P, nb = 2, 2, 4, 2, 8, 4, 5
+    kl = [17, 9]
+    q = rand_bf16((B, Nq, Hq, d), 101)
+    k = rand_bf16((B, nb * P, Hkv, d), 102)
+    v = rand_bf16((B, nb * P, Hkv, d), 103)
+    kc = k.reshape(B * nb, P, Hkv, d)
+    vc = v.reshape(B * nb, P, Hkv, d)
+    table = np.arange(B * nb).reshape(B, nb)
+    for causal in (False, True):
+        o1, l1 = oracle.attn_decode_paged_oracle(q, kc, vc, kl, table, P, causal, 0.5)
+        o2, l2 = oracle.attn_decode_oracle(q, k, v, kl, causal, 0.5)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
+
+
+def test_paged_decode_is_invariant_to_page_placement():
+    """Moving pages to other slots of the pool, with the table updated,
+    changes nothing; pages the table does not reach are never read."""
+    B, Nq, Hq, Hkv, d, P, nb = 2, 1, 4, 1, 8, 4, 4
+    kl = [13, 6]
+    q = rand_bf16((B, Nq, Hq, d), 111, 2.0)
+    pool_k = rand_bf16((12, P, Hkv, d), 112)
+    pool_v = rand_bf16((12, P, Hkv, d), 113)
+    table = np.array([[3, 7, 1, 10], [0, 5, -1, -1]])
+    o1, l1 = oracle.attn_decode_paged_oracle(q, pool_k, pool_v, kl, table, P, True, 0.5)
+    perm = np.random.default_rng(0).permutation(12)            # new slot of old page p
+    k2 = torch.empty_like(pool_k)
+    v2 = torch.empty_like(pool_v)
+    k2[perm] = pool_k
+    v2[perm] = pool_v
+    t2 = np.where(table >= 0, perm[np.maximum(table, 0)], -1)
+    for unused in set(range(12)) - set(perm[table[table >= 0]].tolist()):
+        k2[unused] = float("nan")
+        v2[unused] = float("nan")
+    o2, l2 = oracle.attn_decode_paged_oracle(q, k2, v2, kl, t2, P, True, 0.5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
