@@ -310,6 +310,38 @@ def run_decode(pkg, dev, flush, steps, hbm_gbs):
             "workspace_bytes": n}
 
 
+def run_decode_paged(pkg, dev, flush, steps, hbm_gbs, page_size=16):
+    """The decode step of run_decode over paged caches: pages of page_size
+    rows in a shuffled pool, addressed through a block table."""
+    import torch
+    B, Hq, Hkv, d, Nk, Nq = 16, 32, 8, 128, 8192, 1
+    nb = Nk // page_size
+    g = torch.Generator().manual_seed(2003)
+    q = torch.randn((B, Nq, Hq, d), generator=g).to(torch.bfloat16).to(dev)
+    kc = torch.randn((B * nb, page_size, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    vc = torch.randn((B * nb, page_size, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    table = torch.randperm(B * nb, generator=g).to(torch.int32).reshape(B, nb).to(dev)
+    sl = torch.full((B,), Nk, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    n = pkg.attn_decode_paged_workspace_bytes(B, Hq, Hkv, Nq, nb, page_size, d)
+    ws = torch.empty(((max(n, 16) + 15) // 16 * 4,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: pkg.attn_fwd_decode_paged(q, kc, vc, o, lse, B, Hq, Hkv, Nq, d, d ** -0.5,
+                                             False, sl, table, nb, page_size, B * nb, ws,
+                                             stream=stream.cuda_stream)
+    t = statistics.median(time_steps(step, steps, 3, flush, stream))
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"paged decode run: {pkg.attn_status_string(st)}")
+    nbytes = 2 * kc.numel() * 2 + 2 * q.numel() * 2 + lse.numel() * 4 + table.numel() * 4
+    gbs = nbytes / (t / 1e3) / 1e9
+    return {"workload": f"paged decode B{B} Hq{Hq} Hkv{Hkv} d{d} Nq{Nq} Nk{Nk} page {page_size} "
+                        f"(shuffled pool)",
+            "gbs": round(gbs, 1), "ms_per_step": round(t, 5), "bytes_per_step": nbytes,
+            "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None}
+
+
 def run_e2e(pkg, W, wl, inp, dev, steps):
     """Same metric through the public C ABI with host buffers: every step
     copies Q, K, V from pinned host memory, runs attn_fwd and reads O and LSE
@@ -439,6 +471,8 @@ def native(args):
         per_workload["window"] = run_window(pkg, dev, flush, min(args.steps, 20))
         per_workload["decode"] = run_decode(pkg, dev, flush, min(args.steps, 20),
                                             peaks.get("hbm_gbs"))
+        per_workload["decode_paged"] = run_decode_paged(pkg, dev, flush, min(args.steps, 20),
+                                                        peaks.get("hbm_gbs"))
 
     base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -525,7 +559,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows-per-head", type=int, default=24)
-    ap.add_argument("--extra", choices=["window", "decode"], default=None,
+    ap.add_argument("--extra", choices=["window", "decode", "decode_paged"], default=None,
                     help="time only this extra path (one JSON line; for profiling)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -544,6 +578,8 @@ def extra_only(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.extra == "window":
         out = run_window(pkg, dev, flush, args.steps)
+    elif args.extra == "decode_paged":
+        out = run_decode_paged(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
     else:
         out = run_decode(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
     print(json.dumps(out), flush=True)

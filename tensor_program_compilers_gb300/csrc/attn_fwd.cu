@@ -890,6 +890,16 @@ __device__ __forceinline__ long long pos_v(long long base, int i, int n) {
   return base + (i == n - 1 ? 2 * n - 1 : 2 * i + 2);
 }
 
+// The producer's load order K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}: item 0 is
+// K_0, the last item V_{n-1}, odd items K_{(item+1)/2}, even ones V_{item/2-1}.
+__device__ __forceinline__ bool item_is_v(int item, int n) {
+  return item == 2 * n - 1 || (item > 0 && (item & 1) == 0);
+}
+__device__ __forceinline__ int item_tile(int item, int n) {
+  return item == 2 * n - 1 ? n - 1
+                           : (item == 0 ? 0 : ((item & 1) == 0 ? item / 2 - 1 : (item + 1) / 2));
+}
+
 // ================================================================ kernel
 // Persistent: with G = gridDim.x CTAs, CTA b processes one tile of each
 // round of G tiles of the longest-first list -- tile b of even rounds, tile
@@ -1021,46 +1031,59 @@ __global__ void __launch_bounds__(THREADS, 1)
                             ctl.bar(BAR_Q_FULL0 + qb), c * 64, t.h, t.seq_start + t.unit * BM);
             }
           }
-          // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1}
-          for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
+          // K_0, K_1, V_0, K_2, V_1, ..., V_{n-1} (paged caches: below, by the warp)
+          for (int item = 0; !PAGED && ok && item < 2 * n; ++item, ++pos) {
             const int slot = (int)(pos % C::STAGES);
             if (!(ok = wait_bounded(ctl.bar(BAR_RING + C::STAGES + slot),
                                     ((uint32_t)(pos / C::STAGES) & 1u) ^ 1u, abort_flag,
                                     p.timeout_ns)))
               break;
-            // item 0: K_0; last item: V_{n-1}; odd: K_{(item+1)/2}; even: V_{item/2-1}
-            const bool last = item == 2 * n - 1;
-            const bool is_v = last || (item > 0 && (item & 1) == 0);
-            const int kt = last ? n - 1 : (item == 0 ? 0 : (is_v ? item / 2 - 1 : (item + 1) / 2));
+            const int kt = item_tile(item, n);
+            const bool is_v = item_is_v(item, n);
             mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
             ATTN_TRACE_EV(10, pos >> 2, (int)(pos & 3));
             const uint32_t dst = kv_s + slot * C::TILE_BYTES;
-            if (PAGED) {
-              // the tile's keys come in boxes of min(page, 128) rows, each from
-              // its page; keys past the sequence (and bad page numbers) read a
-              // box wholly outside the tensor, i.e. zeros
-              const int rows = min(p.page_size, BN);
-              for (int r = 0; r < BN; r += rows) {
-                const int j = (j_lo + kt) * BN + r;
-                int page = -1;
-                if (j < t.len) {
-                  page = __ldg(p.block_table + (long long)t.seq_start * p.max_blocks +
-                               j / p.page_size);
-                  if (page < 0 || page >= p.num_pages) {
-                    record_status(ATTN_ERR_BAD_PAGE_TABLE);
-                    page = -1;
-                  }
-                }
-                const int row = page < 0 ? -rows : page * p.page_size + j % p.page_size;
-                for (int c = 0; c < C::CHUNKS; ++c)
-                  tma_load_3d(dst + c * CHUNK_BYTES + (uint32_t)r * 128u, is_v ? &tm_v : &tm_k,
-                              ctl.bar(BAR_RING + slot), c * 64, kvh, row);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
+                          c * 64, kvh, kv_row0 + (j_lo + kt) * BN);
+          }
+        }
+      }
+      if (PAGED) {
+        // The tile's keys come in boxes of min(page, 128) rows, each from its
+        // page: lane i issues box i / CHUNKS, column chunk i % CHUNKS (at most
+        // 8 boxes x 4 chunks), so the page-number loads and the copies of one
+        // tile go out together.  Keys past the sequence (and bad page
+        // numbers) read a box wholly outside the tensor, i.e. zeros.
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && t.valid;
+        const int rows = min(p.page_size, BN);
+        const int boxes = BN / rows;
+        const int *tbl = p.block_table + (long long)t.seq_start * p.max_blocks;
+        for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
+          const int slot = (int)(pos % C::STAGES);
+          if (lane == 0) {
+            ok = wait_bounded(ctl.bar(BAR_RING + C::STAGES + slot),
+                              ((uint32_t)(pos / C::STAGES) & 1u) ^ 1u, abort_flag, p.timeout_ns);
+            if (ok) mbar_arrive_expect_tx(ctl.bar(BAR_RING + slot), C::TILE_BYTES);
+          }
+          if (!(ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0)) break;
+          const int kt = item_tile(item, n);
+          const bool is_v = item_is_v(item, n);
+          if (lane < boxes * C::CHUNKS) {
+            const int i = lane / C::CHUNKS, c = lane % C::CHUNKS;
+            const int j = (j_lo + kt) * BN + i * rows;
+            int page = -1;
+            if (j < t.len) {
+              page = __ldg(tbl + j / p.page_size);
+              if (page < 0 || page >= p.num_pages) {
+                record_status(ATTN_ERR_BAD_PAGE_TABLE);
+                page = -1;
               }
-            } else {
-              for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_3d(dst + c * CHUNK_BYTES, is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot),
-                            c * 64, kvh, kv_row0 + (j_lo + kt) * BN);
             }
+            const int row = page < 0 ? -rows : page * p.page_size + j % p.page_size;
+            tma_load_3d(kv_s + slot * C::TILE_BYTES + c * CHUNK_BYTES + (uint32_t)(i * rows) * 128u,
+                        is_v ? &tm_v : &tm_k, ctl.bar(BAR_RING + slot), c * 64,
+                        DEC ? t.h : t.h / p.group, row);
           }
         }
       }
