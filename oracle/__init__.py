@@ -63,6 +63,14 @@ def load_library(path: str):
         ctypes.c_void_p, ctypes.c_int,                      # slopes round_p
         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,      # nsel sel nthreads
     ]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # q k v dout
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,                   # dq dk dv
+        ctypes.c_int, i64p, i64p,                                            # nseq start len
+        ctypes.c_int, ctypes.c_int, ctypes.c_int,                            # Hq Hkv d
+        ctypes.c_double, ctypes.c_int, ctypes.c_int,                         # scale causal nthreads
+    ]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -225,3 +233,32 @@ def attn_decode_paged_oracle(q, k_cache, v_cache, seqlens_k, block_table, page_s
             k[b, j] = k_cache[page, j % page_size]
             v[b, j] = v_cache[page, j % page_size]
     return attn_decode_oracle(q, k, v, kl, causal, scale, nthreads=nthreads, lib=lib)
+
+
+def attn_bwd_oracle(q, k, v, dout, B, Hq, Hkv, N, d, scale, causal, cu_seqlens=None, nthreads=0,
+                    lib=None):
+    """Gradients (dq, dk, dv) in fp64 of O = attention(q, k, v) against the
+    output gradient dout, in the forward's layouts (fixed batch [B, N, H, d],
+    packed [T, H, d] with cu_seqlens).  See oracle_attn_bwd in attn_oracle.c
+    (tang, section 3 "Gradients are comprehensions")."""
+    lib = _load() if lib is None else lib
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    if cu_seqlens is None:
+        starts = np.arange(B, dtype=np.int64) * N
+        lens = np.full(B, N, dtype=np.int64)
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64).reshape(-1)
+        starts, lens = cu[:-1].copy(), (cu[1:] - cu[:-1]).copy()
+    rows = qb.size // (Hq * d)
+    dq = np.full((rows, Hq, d), np.nan)
+    dk = np.full((rows, Hkv, d), np.nan)
+    dv = np.full((rows, Hkv, d), np.nan)
+    i64 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    rc = lib.oracle_attn_bwd(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, gb.ctypes.data,
+                             dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, len(lens),
+                             i64(starts), i64(lens), Hq, Hkv, d, float(scale), int(bool(causal)),
+                             int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd rejected its arguments (code {rc})")
+    shape = lambda a, H: a.reshape((B, N, H, d) if cu_seqlens is None else (rows, H, d))
+    return shape(dq, Hq), shape(dk, Hkv), shape(dv, Hkv)

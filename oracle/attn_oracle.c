@@ -269,3 +269,107 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * oracle_attn_bwd -- gradients of attention (fixed or packed batches; query
+ * and key lengths equal per sequence), fp64, from the plain definition:
+ * with P the softmax rows of the forward (masked keys excluded) and dO the
+ * output gradient, for every sequence s, head h (kv = h / group) and row i:
+ *
+ *     dP_ij = dO_i . v_j                      D_i = sum_j P_ij dP_ij
+ *     dS_ij = P_ij (dP_ij - D_i)               (the softmax Jacobian)
+ *     dQ_i  = scale sum_j dS_ij k_j
+ *     dK_j += scale dS_ij q_i                  (summed over rows and the
+ *     dV_j += P_ij dO_i                         group's query heads)
+ *
+ * Source: tang, section 3 "Gradients are comprehensions": the gradient of
+ * the attention comprehension is again a set of contractions over the same
+ * scores (the flash backward identity of section 6 is D_i = sum_j P_ij dP_ij
+ * = dO_i . O_i).  Jobs are (sequence, kv head); dq, dk, dv are written in the
+ * input layouts (token rows x heads x d).  Returns 0 or a negative code.
+ */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    const uint16_t *dout, double *dq, double *dk, double *dv, int nseq,
+                    const int64_t *start, const int64_t *len, int Hq, int Hkv, int d,
+                    double scale, int causal, int nthreads) {
+  if (nseq < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
+  int64_t lmax = 0;
+  for (int s = 0; s < nseq; ++s) {
+    if (len[s] < 0) return -2;
+    if (len[s] > lmax) lmax = len[s];
+  }
+  const int group = Hq / Hkv;
+  const int64_t qstride = (int64_t)Hq * d, kstride = (int64_t)Hkv * d;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int failed = 0;
+#pragma omp parallel
+  {
+    double *p = (double *)malloc(sizeof(double) * (size_t)(lmax > 0 ? lmax : 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(lmax > 0 ? lmax : 1));
+    if (!p || !dp) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t job = 0; job < (int64_t)nseq * Hkv; ++job) {
+        const int s = (int)(job / Hkv), kv = (int)(job % Hkv);
+        const int64_t L = len[s], r0 = start[s];
+        for (int64_t j = 0; j < L; ++j)
+          for (int t = 0; t < d; ++t) {
+            dk[((r0 + j) * Hkv + kv) * d + t] = 0.0;
+            dv[((r0 + j) * Hkv + kv) * d + t] = 0.0;
+          }
+        for (int g = 0; g < group; ++g) {
+          const int h = kv * group + g;
+          for (int64_t i = 0; i < L; ++i) {
+            const uint16_t *qi = q + (r0 + i) * qstride + (int64_t)h * d;
+            const uint16_t *doi = dout + (r0 + i) * qstride + (int64_t)h * d;
+            const int64_t n = causal ? i + 1 : L;   /* visible keys 0 .. n-1 */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+              const uint16_t *kj = k + (r0 + j) * kstride + (int64_t)kv * d;
+              double acc = 0.0;
+              for (int t = 0; t < d; ++t) acc += bf16_to_double(qi[t]) * bf16_to_double(kj[t]);
+              p[j] = scale * acc;
+              if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+              p[j] = exp(p[j] - m);
+              l += p[j];
+            }
+            double D = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+              p[j] /= l;
+              const uint16_t *vj = v + (r0 + j) * kstride + (int64_t)kv * d;
+              double acc = 0.0;
+              for (int t = 0; t < d; ++t) acc += bf16_to_double(doi[t]) * bf16_to_double(vj[t]);
+              dp[j] = acc;
+              D += p[j] * acc;
+            }
+            double *dqi = dq + ((r0 + i) * Hq + h) * d;
+            for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+              const double ds = p[j] * (dp[j] - D);
+              const uint16_t *kj = k + (r0 + j) * kstride + (int64_t)kv * d;
+              double *dkj = dk + ((r0 + j) * Hkv + kv) * d;
+              double *dvj = dv + ((r0 + j) * Hkv + kv) * d;
+              for (int t = 0; t < d; ++t) {
+                dqi[t] += scale * ds * bf16_to_double(kj[t]);
+                dkj[t] += scale * ds * bf16_to_double(qi[t]);
+                dvj[t] += p[j] * bf16_to_double(doi[t]);
+              }
+            }
+          }
+        }
+      }
+    }
+    free(p);
+    free(dp);
+  }
+  return failed ? -5 : 0;
+}

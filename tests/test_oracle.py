@@ -602,3 +602,97 @@ def test_paged_decode_is_invariant_to_page_placement():
     o2, l2 = oracle.attn_decode_paged_oracle(q, k2, v2, kl, t2, P, True, 0.5)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# backward (tang, section 3: gradients are comprehensions)
+# ---------------------------------------------------------------------------
+def _forward_python(q, k, v, scale, causal, g):
+    """Plain Python forward of one head group: returns sum(O * G)."""
+    N, H, d = len(q), len(q[0]), len(q[0][0])
+    Hkv = len(k[0])
+    grp = H // Hkv
+    total = 0.0
+    for h in range(H):
+        kv = h // grp
+        for i in range(N):
+            js = range(i + 1) if causal else range(N)
+            sc = [scale * sum(q[i][h][t] * k[j][kv][t] for t in range(d)) for j in js]
+            m = max(sc)
+            e = [math.exp(x - m) for x in sc]
+            l = sum(e)
+            for t in range(d):
+                o = sum(e[n] * v[j][kv][t] for n, j in enumerate(js)) / l
+                total += o * g[i][h][t]
+    return total
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    """Central differences of sum(O * dO) in plain Python floats, at the
+    bf16 input values, against the oracle's gradients."""
+    N, Hq, Hkv, d, scale = 4, 2, 1, 3, 0.7
+    q = rand_bf16((1, N, Hq, d), 121, 1.5)
+    k = rand_bf16((1, N, Hkv, d), 122)
+    v = rand_bf16((1, N, Hkv, d), 123)
+    g = rand_bf16((1, N, Hq, d), 124)
+    dq, dk, dv = oracle.attn_bwd_oracle(q, k, v, g, 1, Hq, Hkv, N, d, scale, causal)
+    base = [x.float()[0].tolist() for x in (q, k, v)]
+    gl = g.float()[0].tolist()
+    eps = 1e-6
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        arr = base[which]
+        for i in range(N):
+            for h in range(len(arr[0])):
+                for t in range(d):
+                    keep = arr[i][h][t]
+                    arr[i][h][t] = keep + eps
+                    up = _forward_python(*base, scale, causal, gl)
+                    arr[i][h][t] = keep - eps
+                    dn = _forward_python(*base, scale, causal, gl)
+                    arr[i][h][t] = keep
+                    assert abs((up - dn) / (2 * eps) - grad[0, i, h, t]) < 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_torch_autograd_fp64(causal):
+    B, N, Hq, Hkv, d, scale = 2, 9, 4, 2, 6, 0.45
+    q = rand_bf16((B, N, Hq, d), 131, 2.0)
+    k = rand_bf16((B, N, Hkv, d), 132)
+    v = rand_bf16((B, N, Hkv, d), 133)
+    g = rand_bf16((B, N, Hq, d), 134)
+    dq, dk, dv = oracle.attn_bwd_oracle(q, k, v, g, B, Hq, Hkv, N, d, scale, causal)
+    qt, kt, vt = (x.double().requires_grad_() for x in (q, k, v))
+    ke = kt.repeat_interleave(Hq // Hkv, dim=2)
+    ve = vt.repeat_interleave(Hq // Hkv, dim=2)
+    s = torch.einsum("bihd,bjhd->bhij", qt, ke) * scale
+    if causal:
+        s = s.masked_fill(torch.triu(torch.ones(N, N, dtype=torch.bool), 1), float("-inf"))
+    o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s, -1), ve)
+    o.backward(g.double())
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_softmax_jacobian_invariants(causal):
+    """Rows of P sum to one and rows of dS to zero, so per sequence and kv
+    head: sum_j dV_j = sum over the group's heads and rows of dO_i, and
+    sum_j dK_j = 0."""
+    lens = [7, 12]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, Hq, Hkv, d = int(cu[-1]), 6, 2, 5
+    q = rand_bf16((T, Hq, d), 141, 2.0)
+    k = rand_bf16((T, Hkv, d), 142)
+    v = rand_bf16((T, Hkv, d), 143)
+    g = rand_bf16((T, Hq, d), 144)
+    dq, dk, dv = oracle.attn_bwd_oracle(q, k, v, g, 2, Hq, Hkv, T, d, 0.5, causal, cu_seqlens=cu)
+    gd = g.double().numpy()
+    for s in range(2):
+        a, b = cu[s], cu[s + 1]
+        for kv in range(Hkv):
+            heads = range(kv * 3, kv * 3 + 3)
+            np.testing.assert_allclose(dv[a:b, kv].sum(0), gd[a:b, list(heads)].sum((0, 1)),
+                                       atol=1e-12, rtol=0)
+            np.testing.assert_allclose(dk[a:b, kv].sum(0), 0.0, atol=1e-12)

@@ -40,6 +40,15 @@ MUTANTS = {
     "soft cap not scaled back": ("sc = cap * tanh(sc / cap);", "sc = tanh(sc / cap);"),
     "soft cap on the raw product": ("double sc = scale * acc;\n    if (cap > 0.0) sc = cap * tanh(sc / cap);",
                                     "double sc = acc;\n    if (cap > 0.0) sc = cap * tanh(sc / cap);\n    sc *= scale;"),
+    "backward: D with the wrong sign": ("const double ds = p[j] * (dp[j] - D);",
+                                        "const double ds = p[j] * (dp[j] + D);"),
+    "backward: dK without the scale": ("dkj[t] += scale * ds * bf16_to_double(qi[t]);",
+                                       "dkj[t] += ds * bf16_to_double(qi[t]);"),
+    "backward: dV weighted by dS": ("dvj[t] += p[j] * bf16_to_double(doi[t]);",
+                                    "dvj[t] += ds * bf16_to_double(doi[t]);"),
+    "backward: causal bound off by one": ("const int64_t n = causal ? i + 1 : L;",
+                                          "const int64_t n = causal ? i : L;"),
+    "backward: P not normalised": ("      p[j] /= l;\n", ""),
     "q row of the kv head": ("const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;",
                              "const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)kv * d;"),
 }
@@ -109,6 +118,23 @@ def _pins_pass(lib) -> bool:
         Ob, Lb = brute_force_decode(q, k, v, kl, causal, 0.6)
         if not (np.allclose(o, Ob, atol=1e-12, rtol=0) and np.allclose(lse, Lb, atol=1e-12, rtol=0)):
             return False
+    # backward against torch fp64 autograd
+    for causal in (False, True):
+        B, N, Hq, Hkv, d, scale = 1, 9, 4, 2, 6, 0.45
+        q = rand_bf16((B, N, Hq, d), 131, 2.0)
+        k = rand_bf16((B, N, Hkv, d), 132)
+        v = rand_bf16((B, N, Hkv, d), 133)
+        g = rand_bf16((B, N, Hq, d), 134)
+        dq, dk, dv = oracle.attn_bwd_oracle(q, k, v, g, B, Hq, Hkv, N, d, scale, causal, lib=lib)
+        qt, kt, vt = (x.double().requires_grad_() for x in (q, k, v))
+        s_ = torch.einsum("bihd,bjhd->bhij", qt, kt.repeat_interleave(2, dim=2)) * scale
+        if causal:
+            s_ = s_.masked_fill(torch.triu(torch.ones(N, N, dtype=torch.bool), 1), float("-inf"))
+        o = torch.einsum("bhij,bjhd->bihd", torch.softmax(s_, -1), vt.repeat_interleave(2, dim=2))
+        o.backward(g.double())
+        for mine, ref in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+            if not np.allclose(mine, ref.numpy(), atol=1e-12, rtol=0):
+                return False
     # Q = 0 closed form
     q = torch.zeros((1, 9, 2, 4), dtype=torch.bfloat16)
     k = rand_bf16((1, 9, 2, 4), 5)
