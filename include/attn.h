@@ -217,6 +217,30 @@ attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v, 
                                    cudaStream_t stream);
 
 /*
+ * attn_bwd -- gradients of attn_fwd (fixed batches): dq, dk, dv of
+ * O = softmax(scale Q K^T + mask) V for the output gradient dout (tang,
+ * section 3 "Gradients are comprehensions"; section 6: the flash backward
+ * identity D_i = sum_j P_ij dP_ij = dO_i . O_i):
+ *   P = exp(scale S - LSE) (recomputed), dV = P^T dO, dP = dO V^T,
+ *   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q
+ * (dK, dV summed over the query heads of each kv head).
+ *
+ *   q, o, dout, dq: device bf16 [B, N, Hq, d];  k, v, dk, dv: [B, N, Hkv, d]
+ *              (16-byte aligned);  lse: the forward's fp32 [B, Hq, N].
+ *   d        : 64 or 128.
+ *   workspace: caller-owned device memory of at least
+ *              attn_bwd_workspace_bytes(B, Hq, N) bytes, 16-byte aligned
+ *              (per-row D and LSE log2(e)); nothing else is allocated.
+ * Other arguments, ownership and errors as attn_fwd; too small a workspace
+ * is ATTN_ERR_INVALID_ARG.  dq, dk, dv are overwritten (no accumulation).
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                     int Hq, int Hkv, int N, int d, float scale, int causal, void *workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_get_status -- synchronises `stream`, then reads and clears the
  * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
  * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.

@@ -20,7 +20,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 INCLUDE_DIR = os.path.join(_ROOT, "include")
 SOURCES = [os.path.join(_CSRC, "attn_fwd.cu")]
-DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(INCLUDE_DIR, "attn.h")]
+DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(_CSRC, "attn_bwd.cuh"),
+                     os.path.join(INCLUDE_DIR, "attn.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -40,8 +41,8 @@ ATTN_ERR_BAD_PAGE_TABLE = 7
 
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
             "attn_fwd_decode_paged", "attn_decode_paged_workspace_bytes",
-            "attn_fwd_decode_static", "attn_get_status", "attn_status_string",
-            "attn_selftest_timeout"]
+            "attn_fwd_decode_static", "attn_bwd", "attn_bwd_workspace_bytes",
+            "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
 
 
 class AttnVariant(ctypes.Structure):
@@ -102,6 +103,11 @@ def _load():
                                               vp, vp, i, i, i, vp, ctypes.c_size_t, vp]
         lib.attn_decode_paged_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                 ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
@@ -225,6 +231,43 @@ def attn_fwd_decode_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nq, d, scale,
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_decode_paged")
     return rc
+
+
+def attn_bwd_workspace_bytes(B, Hq, N) -> int:
+    """Workspace bytes ``attn_bwd`` needs (two fp32 rows per (batch, head))."""
+    return int(_load().attn_bwd_workspace_bytes(int(B), int(Hq), int(N)))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+             workspace=None, workspace_bytes=None, stream=None, check=True) -> int:
+    """Call the C ``attn_bwd``: dq, dk, dv of the forward's O for output
+    gradient dout (fixed batch layouts; lse from the forward)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = _load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(N), int(d),
+                          float(scale), int(bool(causal)), _ptr(workspace),
+                          int(workspace_bytes), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return rc
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool, scale: Optional[float] = None,
+                       stream=None):
+    """Allocate dq, dk, dv and the workspace (torch, on q's device) and run
+    ``attn_bwd`` for a fixed batch q [B, N, Hq, d], k/v [B, N, Hkv, d]."""
+    import torch
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    n = attn_bwd_workspace_bytes(B, Hq, N)
+    ws = torch.empty(((max(n, 16) + 15) // 16 * 4,), dtype=torch.float32, device=q.device)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, ws,
+             stream=stream)
+    return dq, dk, dv
 
 
 DECODE_STATIC_SCRATCH_BYTES = 8 << 20

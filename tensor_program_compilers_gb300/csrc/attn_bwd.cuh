@@ -1,0 +1,601 @@
+// attn_bwd.cuh -- attention backward on sm_103a (included at the end of
+// attn_fwd.cu, whose device helpers, waits and host set-up it shares).
+//
+// Gradients of O = softmax(scale Q K^T + mask) V (tang, section 3
+// "Gradients are comprehensions": the backward is again contractions over
+// the same scores; section 6: the flash backward identity
+// D_i = sum_j P_ij dP_ij = dO_i . O_i):
+//
+//   P  = exp(scale S - LSE)           recomputed from the forward's LSE
+//   dV = P^T dO      dP = dO V^T      dS = P o (dP - D)
+//   dQ = scale dS K  dK = scale dS^T Q
+//
+// Three kernels: a row pass computes D = rowsum(dO o O) and LSE log2(e) into
+// padded per-(batch, head) rows; the dK/dV kernel owns one 128-key block of
+// one kv head and walks the query blocks (of every query head of its group),
+// with S^T, dP^T, dV, dK in tensor memory; the dQ kernel owns one 128-row
+// query block and walks the key blocks, with S, dP, dQ in tensor memory.
+// Both recompute the scores, so no partial sums cross CTAs.  Per step the
+// softmax warps turn the fp32 tiles into bf16 P^T / dS^T (dS) written over
+// the scores they came from; the MMAs that follow read them from tensor
+// memory.  Fixed batches, d = 64 or 128.
+
+namespace attn {
+namespace bwd {
+
+constexpr int BWD_THREADS = 192;   // producer, MMA issuer, 4 softmax warps
+
+struct BwdParams {
+  __nv_bfloat16 *dq, *dk, *dv;
+  const __nv_bfloat16 *o, *dout;
+  const float *lse;      // [B, Hq, N] (natural log)
+  float *lse2;           // [B Hq, Npad]: LSE log2(e); +inf on padding rows
+  float *dsum;           // [B Hq, Npad]: D = rowsum(dO o O); 0 on padding rows
+  int B, Hq, Hkv, N, Npad, group, nblk, causal;
+  float scale, scale_log2;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct BCfg {
+  static constexpr int CHUNKS = D / 64;
+  static constexpr uint32_t TILE = CHUNKS * CHUNK_BYTES;   // one 128 x d bf16 tile
+  static constexpr int STAGES = 2;
+  // dK/dV kernel: K, V, then STAGES x {Q, dO, lse2 row, dsum row}
+  static constexpr uint32_t A_SLOT = 2 * TILE + 1024;
+  static constexpr uint32_t A_OFF_RING = 2 * TILE;
+  static constexpr uint32_t A_OFF_CTL = A_OFF_RING + STAGES * A_SLOT;
+  // dQ kernel: Q, dO, then STAGES x {K, V}
+  static constexpr uint32_t B_SLOT = 2 * TILE;
+  static constexpr uint32_t B_OFF_RING = 2 * TILE;
+  static constexpr uint32_t B_OFF_CTL = B_OFF_RING + STAGES * B_SLOT;
+  static constexpr uint32_t CTL_BYTES = 256;
+  // at least 116 KB so that one CTA holds an SM (and all of its tensor memory)
+  static constexpr uint32_t MIN_SMEM = 116u << 10;
+  static constexpr uint32_t A_SMEM =
+      A_OFF_CTL + CTL_BYTES + 1024 > MIN_SMEM ? A_OFF_CTL + CTL_BYTES + 1024 : MIN_SMEM;
+  static constexpr uint32_t B_SMEM =
+      B_OFF_CTL + CTL_BYTES + 1024 > MIN_SMEM ? B_OFF_CTL + CTL_BYTES + 1024 : MIN_SMEM;
+  static_assert(A_SMEM <= 232448 && B_SMEM <= 232448, "shared memory");
+  static_assert(256 + 2 * D <= (int)TMEM_COLS, "tensor memory");
+};
+
+// barriers of the control block
+enum : int {
+  B_STATIC_FULL = 0,   // K, V (dK/dV kernel) or Q, dO (dQ kernel) loaded
+  B_FULL0,             // ring slot s loaded, s < 2
+  B_FULL1,
+  B_EMPTY0,            // ring slot s consumed (MMA commit)
+  B_EMPTY1,
+  B_S_FULL,            // the step's two score-shaped products are in TMEM
+  B_P_FULL,            // the softmax warps wrote P / dS (4 arrivals)
+  B_DONE,              // the accumulators are final
+  B_DRAIN,             // abort drain of the MMA issuer
+  B_COUNT
+};
+
+// ------------------------------------------------------------------ row pass
+// One warp per (batch, head, row): D = sum_c dO o O, LSE log2(e); rows past
+// N (up to Npad) get D = 0 and +inf, which zeroes their P in the kernels.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // bh Npad + i
+  if (row >= (long long)p.B * p.Hq * p.Npad) return;
+  const int i = (int)(row % p.Npad);
+  const long long bh = row / p.Npad;
+  const int b = (int)(bh / p.Hq), h = (int)(bh % p.Hq);
+  if (i >= p.N) {
+    if (lane == 0) {
+      p.lse2[row] = INFINITY;
+      p.dsum[row] = 0.f;
+    }
+    return;
+  }
+  constexpr int PER = D / 32;
+  const long long off = (((long long)b * p.N + i) * p.Hq + h) * D + lane * PER;
+  float acc = 0.f;
+#pragma unroll
+  for (int x = 0; x < PER; ++x)
+    acc += __bfloat162float(p.o[off + x]) * __bfloat162float(p.dout[off + x]);
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    p.dsum[row] = acc;
+    p.lse2[row] = p.lse[((long long)b * p.Hq + h) * p.N + i] * 1.4426950408889634f;
+  }
+}
+
+// ------------------------------------------------------------------ shared pieces
+struct BCtl {
+  uint32_t bar0;
+  uint32_t *words;   // [0] TMEM base, [1] abort flag
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
+  mbar_init(c.bar(B_STATIC_FULL), 1);
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(c.bar(B_FULL0 + s), 1);
+    mbar_init(c.bar(B_EMPTY0 + s), 1);
+  }
+  mbar_init(c.bar(B_S_FULL), 1);
+  mbar_init(c.bar(B_P_FULL), 4);
+  mbar_init(c.bar(B_DONE), 1);
+  mbar_init(c.bar(B_DRAIN), 1);
+  c.words[1] = 0u;
+  mbar_init_fence();
+}
+
+// 32 columns of a softmax-warp row from two fp32 tiles in TMEM.
+__device__ __forceinline__ void ld_pair32(uint32_t ta, uint32_t tb, float (&a)[32],
+                                          float (&b)[32]) {
+  uint32_t ua[32], ub[32];
+  tmem_ld32(ta, ua);
+  tmem_ld32(tb, ub);
+  tmem_wait_ld();
+  reg_fence32(ua);
+  reg_fence32(ub);
+#pragma unroll
+  for (int x = 0; x < 32; ++x) {
+    a[x] = __uint_as_float(ua[x]);
+    b[x] = __uint_as_float(ub[x]);
+  }
+}
+
+// Epilogue of one accumulator row: NCOLS fp32 columns * mul -> bf16, 16-byte
+// stores (if live).
+template <int NCOLS>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *dst,
+                                               bool live) {
+#pragma unroll 1
+  for (int cc = 0; cc < NCOLS; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+    uint32_t w[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x)
+      w[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * mul, __uint_as_float(o[2 * x + 1]) * mul);
+    if (live) {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV
+// Unit = (b, kv head, key block jb); steps = (query head of the group, query
+// block ib), ib >= jb when causal.  TMEM: S^T [0,128) (P^T bf16 written over
+// its first 64 columns), dP^T [128,256) (dS^T over its first 64), dV
+// [256, 256+D), dK [256+D, 256+2D).
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  BCtl ctl;
+  ctl.bar0 = base + C::A_OFF_CTL;
+  ctl.words = reinterpret_cast<uint32_t *>(smem + C::A_OFF_CTL + 8 * B_COUNT);
+  volatile uint32_t *abort_flag = ctl.words + 1;
+
+  const int jb = blockIdx.x % p.nblk;
+  const int r = blockIdx.x / p.nblk;
+  const int kvh = r % p.Hkv, b = r / p.Hkv;
+  const int i0 = p.causal ? jb : 0;
+  const int steps = p.group * (p.nblk - i0);
+  const uint32_t k_s = base, v_s = base + C::TILE;
+
+  if (warp == 1) {
+    if (lane == 0) bwd_init_barriers(ctl);
+    __syncwarp();
+    tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
+    tmem_relinquish();
+  } else if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_do);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.words[0];
+  constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(ctl.bar(B_STATIC_FULL), 2 * C::TILE);
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        tma_load_3d(k_s + c * CHUNK_BYTES, &tm_k, ctl.bar(B_STATIC_FULL), c * 64, kvh,
+                    b * p.N + jb * BM);
+        tma_load_3d(v_s + c * CHUNK_BYTES, &tm_v, ctl.bar(B_STATIC_FULL), c * 64, kvh,
+                    b * p.N + jb * BM);
+      }
+      for (int s = 0; ok && s < steps; ++s) {
+        const int slot = s & 1;
+        if (s >= 2 && !(ok = wait_bounded(ctl.bar(B_EMPTY0 + slot), (uint32_t)((s - 2) >> 1) & 1u,
+                                          abort_flag, p.timeout_ns)))
+          break;
+        const int h = kvh * p.group + s / (p.nblk - i0);
+        const int ib = i0 + s % (p.nblk - i0);
+        const uint32_t dst = base + C::A_OFF_RING + slot * C::A_SLOT;
+        mbar_arrive_expect_tx(ctl.bar(B_FULL0 + slot), 2 * C::TILE + 1024);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          tma_load_3d(dst + c * CHUNK_BYTES, &tm_q, ctl.bar(B_FULL0 + slot), c * 64, h,
+                      b * p.N + ib * BM);
+          tma_load_3d(dst + C::TILE + c * CHUNK_BYTES, &tm_do, ctl.bar(B_FULL0 + slot), c * 64, h,
+                      b * p.N + ib * BM);
+        }
+        const long long row0 = ((long long)b * p.Hq + h) * p.Npad + (long long)ib * BM;
+        bulk_load(dst + 2 * C::TILE, p.lse2 + row0, 512, ctl.bar(B_FULL0 + slot));
+        bulk_load(dst + 2 * C::TILE + 512, p.dsum + row0, 512, ctl.bar(B_FULL0 + slot));
+        ++issued;
+      }
+      if (*abort_flag) {   // drain: bounded waits for the copies issued
+        wait_drain(ctl.bar(B_STATIC_FULL), 0, p.timeout_ns);
+        for (int s = 0; s < 2 && s < issued; ++s) {
+          const int last = s + 2 * ((issued - 1 - s) / 2);
+          wait_drain(ctl.bar(B_FULL0 + s), (uint32_t)(last >> 1) & 1u, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
+      const uint64_t vdesc = smem_desc_sw128(v_s, 16, 1024);
+      bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      for (int s = 0; ok && s < steps; ++s) {
+        const int slot = s & 1;
+        if (!(ok = wait_bounded(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
+                                p.timeout_ns)))
+          break;
+        tc_fence_after();
+        const uint32_t q_s = base + C::A_OFF_RING + slot * C::A_SLOT;
+        const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
+        const uint64_t dodesc = smem_desc_sw128(q_s + C::TILE, 16, 1024);
+        // S^T = K Q^T and dP^T = V dO^T (the previous step's dV, dK products,
+        // issued earlier by this thread, have read P^T, dS^T before these
+        // overwrite them: one thread's MMAs run in issue order)
+        issue_qk<D>(tmem + COL_ST, kdesc, qdesc);
+        issue_qk<D>(tmem + COL_DPT, vdesc, dodesc);
+        tc_commit(ctl.bar(B_S_FULL));
+        if (!(ok = wait_bounded(ctl.bar(B_P_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        // dV += P^T dO, dK += dS^T Q (dO, Q as N-major B operands)
+        const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
+        const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
+        issue_pv<D, false>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, 0, s > 0);
+        issue_pv<D, false>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, 0, s > 0);
+        tc_commit(ctl.bar(B_EMPTY0 + slot));
+      }
+      if (ok) tc_commit(ctl.bar(B_DONE));
+      tc_commit(ctl.bar(B_DRAIN));
+      wait_drain(ctl.bar(B_DRAIN), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // softmax warps: thread = key row jb*128 + row of TMEM lane quarter warp%4
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int key = jb * BM + row;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; ok && s < steps; ++s) {
+      const int slot = s & 1;
+      if (!(ok = wait_warp(ctl.bar(B_S_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)) ||
+          !(ok = wait_warp(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
+                           p.timeout_ns)))
+        break;
+      tc_fence_after();
+      const int ib = i0 + s % (p.nblk - i0);
+      const float *lse2 =
+          reinterpret_cast<const float *>(smem + C::A_OFF_RING + slot * C::A_SLOT + 2 * C::TILE);
+      const float *dsum = lse2 + 128;
+      const bool diag = p.causal && ib == jb;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float sv[32], dp[32];
+        ld_pair32(tmem + lane_off + COL_ST + 32 * ch, tmem + lane_off + COL_DPT + 32 * ch, sv, dp);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const int qc = 32 * ch + x;
+          float p0 = ex2_approx(sv[x] * c - lse2[qc]);
+          float p1 = ex2_approx(sv[x + 1] * c - lse2[qc + 1]);
+          if (diag) {   // query ib*128 + qc sees key iff query >= key
+            if (ib * BM + qc < key) p0 = 0.f;
+            if (ib * BM + qc + 1 < key) p1 = 0.f;
+          }
+          pw[x >> 1] = pack_bf16x2(p0, p1);
+          dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum[qc]), p1 * (dp[x + 1] - dsum[qc + 1]));
+        }
+        // bf16 P^T and dS^T over scores this warp has already read
+        tmem_st16(tmem + lane_off + COL_ST + 16 * ch, pw);
+        tmem_st16(tmem + lane_off + COL_DPT + 16 * ch, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(ctl.bar(B_P_FULL));
+    }
+    if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
+      tc_fence_after();
+      const bool live = key < p.N;
+      const long long off = (((long long)b * p.N + key) * p.Hkv + kvh) * D;
+      store_row_bf16<D>(tmem + lane_off + COL_DV, 1.f, p.dv + off, live);
+      store_row_bf16<D>(tmem + lane_off + COL_DK, p.scale, p.dk + off, live);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+// Unit = (b, head h, query block ib); steps = key blocks jb (<= ib when
+// causal).  TMEM: S [0,128), dP [128,256) (dS bf16 over its first 64
+// columns), dQ [256, 256+D).
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const BwdParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t base = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  BCtl ctl;
+  ctl.bar0 = base + C::B_OFF_CTL;
+  ctl.words = reinterpret_cast<uint32_t *>(smem + C::B_OFF_CTL + 8 * B_COUNT);
+  volatile uint32_t *abort_flag = ctl.words + 1;
+
+  const int ib = blockIdx.x % p.nblk;
+  const int r = blockIdx.x / p.nblk;
+  const int h = r % p.Hq, b = r / p.Hq;
+  const int kvh = h / p.group;
+  const int steps = p.causal ? ib + 1 : p.nblk;
+  const uint32_t q_s = base, do_s = base + C::TILE;
+
+  if (warp == 1) {
+    if (lane == 0) bwd_init_barriers(ctl);
+    __syncwarp();
+    tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
+    tmem_relinquish();
+  } else if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_do);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.words[0];
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(ctl.bar(B_STATIC_FULL), 2 * C::TILE);
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        tma_load_3d(q_s + c * CHUNK_BYTES, &tm_q, ctl.bar(B_STATIC_FULL), c * 64, h,
+                    b * p.N + ib * BM);
+        tma_load_3d(do_s + c * CHUNK_BYTES, &tm_do, ctl.bar(B_STATIC_FULL), c * 64, h,
+                    b * p.N + ib * BM);
+      }
+      for (int s = 0; ok && s < steps; ++s) {
+        const int slot = s & 1;
+        if (s >= 2 && !(ok = wait_bounded(ctl.bar(B_EMPTY0 + slot), (uint32_t)((s - 2) >> 1) & 1u,
+                                          abort_flag, p.timeout_ns)))
+          break;
+        const uint32_t dst = base + C::B_OFF_RING + slot * C::B_SLOT;
+        mbar_arrive_expect_tx(ctl.bar(B_FULL0 + slot), 2 * C::TILE);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          tma_load_3d(dst + c * CHUNK_BYTES, &tm_k, ctl.bar(B_FULL0 + slot), c * 64, kvh,
+                      b * p.N + s * BM);
+          tma_load_3d(dst + C::TILE + c * CHUNK_BYTES, &tm_v, ctl.bar(B_FULL0 + slot), c * 64,
+                      kvh, b * p.N + s * BM);
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        wait_drain(ctl.bar(B_STATIC_FULL), 0, p.timeout_ns);
+        for (int s = 0; s < 2 && s < issued; ++s) {
+          const int last = s + 2 * ((issued - 1 - s) / 2);
+          wait_drain(ctl.bar(B_FULL0 + s), (uint32_t)(last >> 1) & 1u, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
+      const uint64_t dodesc = smem_desc_sw128(do_s, 16, 1024);
+      bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      for (int s = 0; ok && s < steps; ++s) {
+        const int slot = s & 1;
+        if (!(ok = wait_bounded(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
+                                p.timeout_ns)))
+          break;
+        tc_fence_after();
+        const uint32_t k_s = base + C::B_OFF_RING + slot * C::B_SLOT;
+        const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
+        const uint64_t vdesc = smem_desc_sw128(k_s + C::TILE, 16, 1024);
+        issue_qk<D>(tmem + COL_S, qdesc, kdesc);     // S = Q K^T
+        issue_qk<D>(tmem + COL_DP, dodesc, vdesc);   // dP = dO V^T
+        tc_commit(ctl.bar(B_S_FULL));
+        if (!(ok = wait_bounded(ctl.bar(B_P_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        // dQ += dS K (K as the N-major B operand)
+        issue_pv<D, false>(tmem + COL_DQ, tmem + COL_DP, smem_desc_sw128(k_s, CHUNK_BYTES, 1024),
+                           0, 0, s > 0);
+        tc_commit(ctl.bar(B_EMPTY0 + slot));
+      }
+      if (ok) tc_commit(ctl.bar(B_DONE));
+      tc_commit(ctl.bar(B_DRAIN));
+      wait_drain(ctl.bar(B_DRAIN), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // softmax warps: thread = query row ib*128 + row
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int qrow = ib * BM + row;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float c = p.scale_log2;
+    const long long prow = ((long long)b * p.Hq + h) * p.Npad + qrow;
+    const float lse2 = p.lse2[prow];   // +inf on padding rows: P = 0
+    const float dsum = p.dsum[prow];
+    bool ok = true;
+    for (int s = 0; ok && s < steps; ++s) {
+      if (!(ok = wait_warp(ctl.bar(B_S_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
+      tc_fence_after();
+      const bool edge = (s * BM + BM > p.N) || (p.causal && s == ib);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        float sv[32], dp[32];
+        ld_pair32(tmem + lane_off + COL_S + 32 * ch, tmem + lane_off + COL_DP + 32 * ch, sv, dp);
+        uint32_t dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const int k0 = s * BM + 32 * ch + x;
+          float p0 = ex2_approx(sv[x] * c - lse2);
+          float p1 = ex2_approx(sv[x + 1] * c - lse2);
+          if (edge) {   // keys past the sequence, or after the query (causal)
+            if (k0 >= p.N || (p.causal && k0 > qrow)) p0 = 0.f;
+            if (k0 + 1 >= p.N || (p.causal && k0 + 1 > qrow)) p1 = 0.f;
+          }
+          dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum), p1 * (dp[x + 1] - dsum));
+        }
+        tmem_st16(tmem + lane_off + COL_DP + 16 * ch, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(ctl.bar(B_P_FULL));
+    }
+    if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
+      tc_fence_after();
+      store_row_bf16<D>(tmem + lane_off + COL_DQ, p.scale,
+                        p.dq + (((long long)b * p.N + qrow) * p.Hq + h) * D, qrow < p.N);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace bwd
+}  // namespace attn
+
+// ------------------------------------------------------------------ host
+extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N) {
+  if (B < 1 || Hq < 1 || N < 1) return 0;
+  const size_t npad = ((size_t)N + attn::BM - 1) / attn::BM * attn::BM;
+  return 2 * (size_t)B * Hq * npad * sizeof(float);
+}
+
+extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, void *dq, void *dk,
+                                void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                                int causal, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  using namespace attn;
+  using namespace attn::bwd;
+  if (B < 0 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  auto misaligned = [](const void *ptr, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+  };
+  if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+      misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
+      misaligned(lse, 4) || misaligned(workspace, 16))
+    return ATTN_ERR_ALIGNMENT;
+  const long long rows = (long long)B * N;
+  if (rows > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, Hq, N);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn_status st = prepare_device(dev);
+  if (st != ATTN_OK) return st;
+  {
+    static std::mutex mu;
+    static bool ready[MAX_DEVICES];
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      if (!opt_in_smem(attn_bwd_dkdv_kernel<64>, BCfg<64>::A_SMEM) ||
+          !opt_in_smem(attn_bwd_dkdv_kernel<128>, BCfg<128>::A_SMEM) ||
+          !opt_in_smem(attn_bwd_dq_kernel<64>, BCfg<64>::B_SMEM) ||
+          !opt_in_smem(attn_bwd_dq_kernel<128>, BCfg<128>::B_SMEM))
+        return ATTN_ERR_CUDA;
+      ready[dev] = true;
+    }
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return ATTN_ERR_CUDA;
+  CUtensorMap mq, mdo, mk, mv;
+  if (!make_map(enc, &mq, q, Hq, rows, d) || !make_map(enc, &mdo, dout, Hq, rows, d) ||
+      !make_map(enc, &mk, k, Hkv, rows, d) || !make_map(enc, &mv, v, Hkv, rows, d))
+    return ATTN_ERR_INVALID_ARG;
+
+  BwdParams p{};
+  p.dq = reinterpret_cast<__nv_bfloat16 *>(dq);
+  p.dk = reinterpret_cast<__nv_bfloat16 *>(dk);
+  p.dv = reinterpret_cast<__nv_bfloat16 *>(dv);
+  p.o = reinterpret_cast<const __nv_bfloat16 *>(o);
+  p.dout = reinterpret_cast<const __nv_bfloat16 *>(dout);
+  p.lse = lse;
+  p.nblk = (N + BM - 1) / BM;
+  p.Npad = p.nblk * BM;
+  p.lse2 = reinterpret_cast<float *>(workspace);
+  p.dsum = p.lse2 + (size_t)B * Hq * p.Npad;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_timeout_ns();
+
+  const unsigned row_blocks = (unsigned)(((long long)B * Hq * p.Npad + 7) / 8);
+  const unsigned kv_units = (unsigned)((long long)B * Hkv * p.nblk);
+  const unsigned q_units = (unsigned)((long long)B * Hq * p.nblk);
+  if (d == 64) {
+    bwd_rows_kernel<64><<<row_blocks, 256, 0, stream>>>(p);
+    attn_bwd_dkdv_kernel<64><<<kv_units, BWD_THREADS, BCfg<64>::A_SMEM, stream>>>(mq, mdo, mk, mv, p);
+    attn_bwd_dq_kernel<64><<<q_units, BWD_THREADS, BCfg<64>::B_SMEM, stream>>>(mq, mdo, mk, mv, p);
+  } else {
+    bwd_rows_kernel<128><<<row_blocks, 256, 0, stream>>>(p);
+    attn_bwd_dkdv_kernel<128><<<kv_units, BWD_THREADS, BCfg<128>::A_SMEM, stream>>>(mq, mdo, mk, mv, p);
+    attn_bwd_dq_kernel<128><<<q_units, BWD_THREADS, BCfg<128>::B_SMEM, stream>>>(mq, mdo, mk, mv, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}

@@ -1787,3 +1787,5 @@ extern "C" attn_status attn_selftest_timeout(int timeout_us, cudaStream_t stream
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return attn_get_status(stream);
 }
+
+#include "attn_bwd.cuh"

@@ -160,3 +160,29 @@ def test_paged_misaligned_table_rejected(lib):
 
 def test_paged_status_string(lib):
     assert pkg.attn_status_string(7) == "ATTN_ERR_BAD_PAGE_TABLE"
+
+
+def call_bwd(**kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000,
+                dk=0x8000, dv=0x9000, B=2, Hq=8, Hkv=2, N=256, d=128, scale=0.088, causal=1,
+                workspace=0xA000, workspace_bytes=1 << 20, stream=0)
+    args.update(kw)
+    return pkg.attn_bwd(check=False, **args)
+
+
+@pytest.mark.parametrize("kw", [dict(d=256), dict(d=32), dict(Hq=6, Hkv=4), dict(scale=0.0),
+                                dict(dq=None), dict(lse=None), dict(dout=None),
+                                dict(workspace=None), dict(workspace_bytes=16),
+                                dict(N=1 << 30, B=4)])
+def test_bwd_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert call_bwd(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(dq=0x7008), dict(dout=0x5004), dict(workspace=0xA004),
+                                dict(lse=0x6002)])
+def test_bwd_misaligned_pointers_rejected(lib, kw):
+    assert call_bwd(**kw) == pkg.ATTN_ERR_ALIGNMENT
+
+
+def test_bwd_workspace_size():
+    assert pkg.attn_bwd_workspace_bytes(2, 8, 300) == 2 * 2 * 8 * 384 * 4
