@@ -342,6 +342,35 @@ def run_decode_paged(pkg, dev, flush, steps, hbm_gbs, page_size=16):
             "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None}
 
 
+def run_backward(pkg, dev, flush, steps):
+    """Backward of the GQA prefill workload (B2 Hq32 Hkv8 N4096 d128 causal):
+    dQ, dK, dV from the forward's O and LSE.  TFLOP/s under the usual
+    convention of 2.5x the forward's FLOPs (five products of the forward's
+    size; the kernels here compute seven, recomputing S and dP in both)."""
+    import torch
+    B, Hq, Hkv, N, d = 2, 32, 8, 4096, 128
+    g = torch.Generator().manual_seed(2004)
+    q = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
+    do = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16).to(dev)
+    o, lse = pkg.attention(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    n = pkg.attn_bwd_workspace_bytes(B, Hq, N)
+    ws = torch.empty(((n + 15) // 16 * 4,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: pkg.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
+                                True, ws, stream=stream.cuda_stream)
+    t = statistics.median(time_steps(step, steps, 3, flush, stream))
+    st = pkg.attn_get_status(stream.cuda_stream)
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"backward run: {pkg.attn_status_string(st)}")
+    fwd_flops = 4.0 * B * Hq * N * N * d / 2
+    return {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} causal",
+            "tflops": round(2.5 * fwd_flops / (t / 1e3) / 1e12, 2), "ms_per_step": round(t, 5),
+            "flop_convention": "2.5 x forward"}
+
+
 def run_e2e(pkg, W, wl, inp, dev, steps):
     """Same metric through the public C ABI with host buffers: every step
     copies Q, K, V from pinned host memory, runs attn_fwd and reads O and LSE
@@ -473,6 +502,7 @@ def native(args):
                                             peaks.get("hbm_gbs"))
         per_workload["decode_paged"] = run_decode_paged(pkg, dev, flush, min(args.steps, 20),
                                                         peaks.get("hbm_gbs"))
+        per_workload["backward"] = run_backward(pkg, dev, flush, min(args.steps, 20))
 
     base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -559,7 +589,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows-per-head", type=int, default=24)
-    ap.add_argument("--extra", choices=["window", "decode", "decode_paged"], default=None,
+    ap.add_argument("--extra", choices=["window", "decode", "decode_paged", "backward"],
+                    default=None,
                     help="time only this extra path (one JSON line; for profiling)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -578,6 +609,8 @@ def extra_only(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.extra == "window":
         out = run_window(pkg, dev, flush, args.steps)
+    elif args.extra == "backward":
+        out = run_backward(pkg, dev, flush, args.steps)
     elif args.extra == "decode_paged":
         out = run_decode_paged(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
     else:
