@@ -23,7 +23,10 @@
 namespace attn {
 namespace bwd {
 
-constexpr int BWD_THREADS = 192;   // producer, MMA issuer, 4 softmax warps
+// producer, MMA issuer, 8 softmax warps (two per TMEM lane quarter, one per
+// half of the 128 columns of a score tile)
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_SM_WARPS = 8;
 
 struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;
@@ -119,11 +122,25 @@ __device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
     mbar_init(c.bar(B_EMPTY0 + s), 1);
   }
   mbar_init(c.bar(B_S_FULL), 1);
-  mbar_init(c.bar(B_P_FULL), 4);
+  mbar_init(c.bar(B_P_FULL), BWD_SM_WARPS);
   mbar_init(c.bar(B_DONE), 1);
   mbar_init(c.bar(B_DRAIN), 1);
   c.words[1] = 0u;
   mbar_init_fence();
+}
+
+// A (bf16 pairs in TMEM) times B (N-major shared-memory tile) over K = 128,
+// accumulating into d_tmem, when the two halves of A (K 0-63 and 64-127)
+// sit at a_tmem and a_tmem + 64: each softmax warp writes the bf16 values of
+// its half over the first columns of the scores it read itself.
+template <int D>
+__device__ __forceinline__ void issue_pv_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+           desc_add(bdesc, kk * 2048), IDESC, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // 32 columns of a softmax-warp row from two fp32 tiles in TMEM.
@@ -276,8 +293,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // dV += P^T dO, dK += dS^T Q (dO, Q as N-major B operands)
         const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
         const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
-        issue_pv<D, false>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, 0, s > 0);
-        issue_pv<D, false>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, 0, s > 0);
+        issue_pv_halves<D>(tmem + COL_DV, tmem + COL_ST, do_mn, s > 0);
+        issue_pv_halves<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, s > 0);
         tc_commit(ctl.bar(B_EMPTY0 + slot));
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
@@ -286,8 +303,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // softmax warps: thread = key row jb*128 + row of TMEM lane quarter warp%4
+    // softmax warps: thread = key row jb*128 + row of TMEM lane quarter warp%4,
+    // query columns 64 hf .. 64 hf + 63
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int row = wq * 32 + lane;
     const int key = jb * BM + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -306,13 +325,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const float *dsum = lse2 + 128;
       const bool diag = p.causal && ib == jb;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * hf + 32 * ch;
         float sv[32], dp[32];
-        ld_pair32(tmem + lane_off + COL_ST + 32 * ch, tmem + lane_off + COL_DPT + 32 * ch, sv, dp);
+        ld_pair32(tmem + lane_off + COL_ST + c0, tmem + lane_off + COL_DPT + c0, sv, dp);
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const int qc = 32 * ch + x;
+          const int qc = c0 + x;
           float p0 = ex2_approx(sv[x] * c - lse2[qc]);
           float p1 = ex2_approx(sv[x + 1] * c - lse2[qc + 1]);
           if (diag) {   // query ib*128 + qc sees key iff query >= key
@@ -322,9 +342,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           pw[x >> 1] = pack_bf16x2(p0, p1);
           dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum[qc]), p1 * (dp[x + 1] - dsum[qc + 1]));
         }
-        // bf16 P^T and dS^T over scores this warp has already read
-        tmem_st16(tmem + lane_off + COL_ST + 16 * ch, pw);
-        tmem_st16(tmem + lane_off + COL_DPT + 16 * ch, dw);
+        // bf16 P^T and dS^T over scores this warp has already read (the
+        // first 32 of its 64 columns)
+        tmem_st16(tmem + lane_off + COL_ST + 64 * hf + 16 * ch, pw);
+        tmem_st16(tmem + lane_off + COL_DPT + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -333,9 +354,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
       const bool live = key < p.N;
-      const long long off = (((long long)b * p.N + key) * p.Hkv + kvh) * D;
-      store_row_bf16<D>(tmem + lane_off + COL_DV, 1.f, p.dv + off, live);
-      store_row_bf16<D>(tmem + lane_off + COL_DK, p.scale, p.dk + off, live);
+      const long long off = (((long long)b * p.N + key) * p.Hkv + kvh) * D + hf * (D / 2);
+      store_row_bf16<D / 2>(tmem + lane_off + COL_DV + hf * (D / 2), 1.f, p.dv + off, live);
+      store_row_bf16<D / 2>(tmem + lane_off + COL_DK + hf * (D / 2), p.scale, p.dk + off, live);
     }
   }
   tc_fence_before();
@@ -446,8 +467,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           break;
         tc_fence_after();
         // dQ += dS K (K as the N-major B operand)
-        issue_pv<D, false>(tmem + COL_DQ, tmem + COL_DP, smem_desc_sw128(k_s, CHUNK_BYTES, 1024),
-                           0, 0, s > 0);
+        issue_pv_halves<D>(tmem + COL_DQ, tmem + COL_DP, smem_desc_sw128(k_s, CHUNK_BYTES, 1024),
+                           s > 0);
         tc_commit(ctl.bar(B_EMPTY0 + slot));
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
@@ -456,8 +477,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // softmax warps: thread = query row ib*128 + row
+    // softmax warps: thread = query row ib*128 + row, key columns 64 hf .. +63
     const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int row = wq * 32 + lane;
     const int qrow = ib * BM + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -471,13 +493,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_after();
       const bool edge = (s * BM + BM > p.N) || (p.causal && s == ib);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * hf + 32 * ch;
         float sv[32], dp[32];
-        ld_pair32(tmem + lane_off + COL_S + 32 * ch, tmem + lane_off + COL_DP + 32 * ch, sv, dp);
+        ld_pair32(tmem + lane_off + COL_S + c0, tmem + lane_off + COL_DP + c0, sv, dp);
         uint32_t dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
-          const int k0 = s * BM + 32 * ch + x;
+          const int k0 = s * BM + c0 + x;
           float p0 = ex2_approx(sv[x] * c - lse2);
           float p1 = ex2_approx(sv[x + 1] * c - lse2);
           if (edge) {   // keys past the sequence, or after the query (causal)
@@ -486,7 +509,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           }
           dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum), p1 * (dp[x + 1] - dsum));
         }
-        tmem_st16(tmem + lane_off + COL_DP + 16 * ch, dw);
+        tmem_st16(tmem + lane_off + COL_DP + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -494,8 +517,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
-      store_row_bf16<D>(tmem + lane_off + COL_DQ, p.scale,
-                        p.dq + (((long long)b * p.N + qrow) * p.Hq + h) * D, qrow < p.N);
+      store_row_bf16<D / 2>(tmem + lane_off + COL_DQ + hf * (D / 2), p.scale,
+                            p.dq + (((long long)b * p.N + qrow) * p.Hq + h) * D + hf * (D / 2),
+                            qrow < p.N);
     }
   }
   tc_fence_before();
