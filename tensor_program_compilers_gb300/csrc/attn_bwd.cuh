@@ -70,8 +70,10 @@ enum : int {
   B_FULL1,
   B_EMPTY0,            // ring slot s consumed (MMA commit)
   B_EMPTY1,
-  B_S_FULL,            // the step's two score-shaped products are in TMEM
-  B_P_FULL,            // the softmax warps wrote P / dS (4 arrivals)
+  B_S_FULL0,           // column half h of the step's two score-shaped products is
+  B_S_FULL1,           //   in TMEM, h < 2
+  B_P_FULL0,           // the 4 softmax warps of column half h wrote P / dS
+  B_P_FULL1,
   B_DONE,              // the accumulators are final
   B_DRAIN,             // abort drain of the MMA issuer
   B_COUNT
@@ -121,26 +123,45 @@ __device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
     mbar_init(c.bar(B_FULL0 + s), 1);
     mbar_init(c.bar(B_EMPTY0 + s), 1);
   }
-  mbar_init(c.bar(B_S_FULL), 1);
-  mbar_init(c.bar(B_P_FULL), BWD_SM_WARPS);
+  for (int h = 0; h < 2; ++h) {
+    mbar_init(c.bar(B_S_FULL0 + h), 1);
+    mbar_init(c.bar(B_P_FULL0 + h), BWD_SM_WARPS / 2);
+  }
   mbar_init(c.bar(B_DONE), 1);
   mbar_init(c.bar(B_DRAIN), 1);
   c.words[1] = 0u;
   mbar_init_fence();
 }
 
-// A (bf16 pairs in TMEM) times B (N-major shared-memory tile) over K = 128,
-// accumulating into d_tmem, when the two halves of A (K 0-63 and 64-127)
-// sit at a_tmem and a_tmem + 64: each softmax warp writes the bf16 values of
-// its half over the first columns of the scores it read itself.
+// Column half h of a score-shaped product: A (128 rows, K-major) times rows
+// 64 h .. 64 h + 63 of B (K-major; 64 rows = 8 KB into each swizzle chunk),
+// N = 64, into TMEM columns d_tmem + 64 h.  Each half is committed on its
+// own so that the softmax warps of half 0 start while half 1 is computed.
 template <int D>
-__device__ __forceinline__ void issue_pv_halves(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                bool accumulate) {
+__device__ __forceinline__ void issue_half_s(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             int h) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(64, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
+    mma_ss(d_tmem + 64u * (uint32_t)h, desc_add(adesc, koff),
+           desc_add(bdesc, koff + (uint32_t)h * 64u * 128u), IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+
+// K-half h of A (bf16 pairs in TMEM at a_tmem + 64 h: each softmax warp
+// writes its half over the first columns of the scores it read itself)
+// times rows 64 h .. 64 h + 63 of B (N-major shared-memory tile), N = D,
+// accumulated into d_tmem (overwritten by half 0 unless accumulate).
+template <int D>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              int h, bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
-           desc_add(bdesc, kk * 2048), IDESC, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts(d_tmem, a_tmem + 64u * (uint32_t)h + 8u * (uint32_t)kk,
+           desc_add(bdesc, (4 * h + kk) * 2048), IDESC,
+           (accumulate || h > 0 || kk > 0) ? 1u : 0u);
 }
 
 // 32 columns of a softmax-warp row from two fp32 tiles in TMEM.
@@ -281,20 +302,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t q_s = base + C::A_OFF_RING + slot * C::A_SLOT;
         const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
         const uint64_t dodesc = smem_desc_sw128(q_s + C::TILE, 16, 1024);
-        // S^T = K Q^T and dP^T = V dO^T (the previous step's dV, dK products,
-        // issued earlier by this thread, have read P^T, dS^T before these
-        // overwrite them: one thread's MMAs run in issue order)
-        issue_qk<D>(tmem + COL_ST, kdesc, qdesc);
-        issue_qk<D>(tmem + COL_DPT, vdesc, dodesc);
-        tc_commit(ctl.bar(B_S_FULL));
-        if (!(ok = wait_bounded(ctl.bar(B_P_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
-          break;
-        tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q (dO, Q as N-major B operands)
+        // S^T = K Q^T and dP^T = V dO^T, by query halves (the previous
+        // step's dV, dK products, issued earlier by this thread, have read
+        // P^T, dS^T before these overwrite them: one thread's MMAs run in
+        // issue order)
+        for (int h = 0; h < 2; ++h) {
+          issue_half_s<D>(tmem + COL_ST, kdesc, qdesc, h);
+          issue_half_s<D>(tmem + COL_DPT, vdesc, dodesc, h);
+          tc_commit(ctl.bar(B_S_FULL0 + h));
+        }
+        // dV += P^T dO, dK += dS^T Q (dO, Q as N-major B operands), by
+        // query halves as their softmax warps finish
         const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
         const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
-        issue_pv_halves<D>(tmem + COL_DV, tmem + COL_ST, do_mn, s > 0);
-        issue_pv_halves<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, s > 0);
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!(ok = wait_bounded(ctl.bar(B_P_FULL0 + h), (uint32_t)s & 1u, abort_flag,
+                                  p.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, h, s > 0);
+          issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, h, s > 0);
+        }
+        if (!ok) break;
         tc_commit(ctl.bar(B_EMPTY0 + slot));
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
@@ -314,7 +343,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
       const int slot = s & 1;
-      if (!(ok = wait_warp(ctl.bar(B_S_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)) ||
+      if (!(ok = wait_warp(ctl.bar(B_S_FULL0 + hf), (uint32_t)s & 1u, abort_flag,
+                           p.timeout_ns)) ||
           !(ok = wait_warp(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
                            p.timeout_ns)))
         break;
@@ -349,7 +379,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(ctl.bar(B_P_FULL));
+      warp_arrive(ctl.bar(B_P_FULL0 + hf));
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
@@ -460,15 +490,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t k_s = base + C::B_OFF_RING + slot * C::B_SLOT;
         const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
         const uint64_t vdesc = smem_desc_sw128(k_s + C::TILE, 16, 1024);
-        issue_qk<D>(tmem + COL_S, qdesc, kdesc);     // S = Q K^T
-        issue_qk<D>(tmem + COL_DP, dodesc, vdesc);   // dP = dO V^T
-        tc_commit(ctl.bar(B_S_FULL));
-        if (!(ok = wait_bounded(ctl.bar(B_P_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
-          break;
-        tc_fence_after();
-        // dQ += dS K (K as the N-major B operand)
-        issue_pv_halves<D>(tmem + COL_DQ, tmem + COL_DP, smem_desc_sw128(k_s, CHUNK_BYTES, 1024),
-                           s > 0);
+        for (int h = 0; h < 2; ++h) {   // S = Q K^T, dP = dO V^T, by key halves
+          issue_half_s<D>(tmem + COL_S, qdesc, kdesc, h);
+          issue_half_s<D>(tmem + COL_DP, dodesc, vdesc, h);
+          tc_commit(ctl.bar(B_S_FULL0 + h));
+        }
+        // dQ += dS K (K as the N-major B operand), by key halves
+        const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!(ok = wait_bounded(ctl.bar(B_P_FULL0 + h), (uint32_t)s & 1u, abort_flag,
+                                  p.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, h, s > 0);
+        }
+        if (!ok) break;
         tc_commit(ctl.bar(B_EMPTY0 + slot));
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
@@ -489,7 +525,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const float dsum = p.dsum[prow];
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
-      if (!(ok = wait_warp(ctl.bar(B_S_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
+      if (!(ok = wait_warp(ctl.bar(B_S_FULL0 + hf), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        break;
       tc_fence_after();
       const bool edge = (s * BM + BM > p.N) || (p.causal && s == ib);
 #pragma unroll 1
@@ -513,7 +550,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(ctl.bar(B_P_FULL));
+      warp_arrive(ctl.bar(B_P_FULL0 + hf));
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
