@@ -360,7 +360,7 @@ def run_backward(pkg, dev, flush, steps):
     ws = torch.empty(((n + 15) // 16 * 4,), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     step = lambda: pkg.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
-                                True, ws, stream=stream.cuda_stream)
+                                True, workspace=ws, stream=stream.cuda_stream)
     t = statistics.median(time_steps(step, steps, 3, flush, stream))
     st = pkg.attn_get_status(stream.cuda_stream)
     if st != pkg.ATTN_OK:

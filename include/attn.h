@@ -217,7 +217,7 @@ attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v, 
                                    cudaStream_t stream);
 
 /*
- * attn_bwd -- gradients of attn_fwd (fixed batches): dq, dk, dv of
+ * attn_bwd -- gradients of attn_fwd (fixed or packed batches): dq, dk, dv of
  * O = softmax(scale Q K^T + mask) V for the output gradient dout (tang,
  * section 3 "Gradients are comprehensions"; section 6: the flash backward
  * identity D_i = sum_j P_ij dP_ij = dO_i . O_i):
@@ -225,20 +225,25 @@ attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v, 
  *   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q
  * (dK, dV summed over the query heads of each kv head).
  *
- *   q, o, dout, dq: device bf16 [B, N, Hq, d];  k, v, dk, dv: [B, N, Hkv, d]
- *              (16-byte aligned);  lse: the forward's fp32 [B, Hq, N].
+ *   q, o, dout, dq, k, v, dk, dv: device bf16 in the layouts of attn_fwd
+ *              (fixed [B, N, H, d], packed [T, H, d]; 16-byte aligned);
+ *   lse      : the forward's fp32 LSE in its layout ([B, Hq, N] or [Hq, T]).
+ *   N, cu_seqlens: as attn_fwd (packed: N = T, cu_seqlens device int32[B+1];
+ *              bad offsets are reported as ATTN_ERR_BAD_SEQLENS).
  *   d        : 64 or 128.
  *   workspace: caller-owned device memory of at least
- *              attn_bwd_workspace_bytes(B, Hq, N) bytes, 16-byte aligned
- *              (per-row D and LSE log2(e)); nothing else is allocated.
+ *              attn_bwd_workspace_bytes(B, Hq, N, cu_seqlens != NULL) bytes,
+ *              16-byte aligned (per-row D and LSE log2(e), sequence
+ *              offsets); nothing else is allocated.
  * Other arguments, ownership and errors as attn_fwd; too small a workspace
  * is ATTN_ERR_INVALID_ARG.  dq, dk, dv are overwritten (no accumulation).
  */
-size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int packed);
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
-                     int Hq, int Hkv, int N, int d, float scale, int causal, void *workspace,
-                     size_t workspace_bytes, cudaStream_t stream);
+                     int Hq, int Hkv, int N, int d, float scale, int causal,
+                     const int *cu_seqlens, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
 
 /*
  * attn_get_status -- synchronises `stream`, then reads and clears the

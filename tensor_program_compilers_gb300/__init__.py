@@ -105,9 +105,9 @@ def _load():
         lib.attn_decode_paged_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.attn_bwd.restype = i
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
-                                 ctypes.c_float, i, vp, ctypes.c_size_t, vp]
+                                 ctypes.c_float, i, vp, vp, ctypes.c_size_t, vp]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
@@ -233,21 +233,22 @@ def attn_fwd_decode_paged(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Nq, d, scale,
     return rc
 
 
-def attn_bwd_workspace_bytes(B, Hq, N) -> int:
-    """Workspace bytes ``attn_bwd`` needs (two fp32 rows per (batch, head))."""
-    return int(_load().attn_bwd_workspace_bytes(int(B), int(Hq), int(N)))
+def attn_bwd_workspace_bytes(B, Hq, N, packed=False) -> int:
+    """Workspace bytes ``attn_bwd`` needs (per-row D and LSE, sequence offsets)."""
+    return int(_load().attn_bwd_workspace_bytes(int(B), int(Hq), int(N), int(bool(packed))))
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
-             workspace=None, workspace_bytes=None, stream=None, check=True) -> int:
+             cu_seqlens=None, workspace=None, workspace_bytes=None, stream=None,
+             check=True) -> int:
     """Call the C ``attn_bwd``: dq, dk, dv of the forward's O for output
-    gradient dout (fixed batch layouts; lse from the forward)."""
+    gradient dout (the forward's layouts and LSE; packed with cu_seqlens)."""
     if workspace_bytes is None:
         workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
             workspace.numel() * workspace.element_size()
     rc = _load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                           _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(N), int(d),
-                          float(scale), int(bool(causal)), _ptr(workspace),
+                          float(scale), int(bool(causal)), _ptr(cu_seqlens), _ptr(workspace),
                           int(workspace_bytes), _stream(stream))
     if check and rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
@@ -255,17 +256,24 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
 
 
 def attention_backward(q, k, v, o, lse, dout, causal: bool, scale: Optional[float] = None,
-                       stream=None):
+                       cu_seqlens=None, stream=None):
     """Allocate dq, dk, dv and the workspace (torch, on q's device) and run
-    ``attn_bwd`` for a fixed batch q [B, N, Hq, d], k/v [B, N, Hkv, d]."""
+    ``attn_bwd``: fixed batch q [B, N, Hq, d], k/v [B, N, Hkv, d], or packed
+    q [T, Hq, d], k/v [T, Hkv, d] with cu_seqlens (int32 [B+1], device)."""
     import torch
-    B, N, Hq, d = q.shape
-    Hkv = k.shape[2]
+    d = q.shape[-1]
+    if cu_seqlens is None:
+        B, N, Hq, _ = q.shape
+        Hkv = k.shape[2]
+    else:
+        N, Hq, _ = q.shape
+        Hkv = k.shape[1]
+        B = cu_seqlens.numel() - 1
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    n = attn_bwd_workspace_bytes(B, Hq, N)
+    n = attn_bwd_workspace_bytes(B, Hq, N, packed=cu_seqlens is not None)
     ws = torch.empty(((max(n, 16) + 15) // 16 * 4,), dtype=torch.float32, device=q.device)
-    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, ws,
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, ws,
              stream=stream)
     return dq, dk, dv
 

@@ -18,7 +18,7 @@
 // Both recompute the scores, so no partial sums cross CTAs.  Per step the
 // softmax warps turn the fp32 tiles into bf16 P^T / dS^T (dS) written over
 // the scores they came from; the MMAs that follow read them from tensor
-// memory.  Fixed batches, d = 64 or 128.
+// memory.  Fixed and packed batches, d = 64 or 128.
 
 namespace attn {
 namespace bwd {
@@ -28,16 +28,79 @@ namespace bwd {
 constexpr int BWD_THREADS = 320;
 constexpr int BWD_SM_WARPS = 8;
 
+// Sequences: fixed batch (cu == nullptr) sequence b holds token rows
+// b N .. b N + N - 1; packed, rows cu[b] .. cu[b+1] - 1.  In the padded row
+// space each sequence starts at pstart[b] (whole 128-row blocks); per-row
+// values live in [H, rows_pad] arrays with rows_pad = nb_max * 128.
 struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;
   const __nv_bfloat16 *o, *dout;
-  const float *lse;      // [B, Hq, N] (natural log)
-  float *lse2;           // [B Hq, Npad]: LSE log2(e); +inf on padding rows
-  float *dsum;           // [B Hq, Npad]: D = rowsum(dO o O); 0 on padding rows
-  int B, Hq, Hkv, N, Npad, group, nblk, causal;
+  const float *lse;      // the forward's LSE: fixed [B, Hq, N], packed [Hq, T]
+  const int *cu;         // packed: cu_seqlens[B+1]; fixed: nullptr
+  int *pstart;           // [B+1] padded start of each sequence (set-up pass)
+  float *lse2;           // [Hq, rows_pad]: LSE log2(e); +inf on padding rows
+  float *dsum;           // [Hq, rows_pad]: D = rowsum(dO o O); 0 on padding rows
+  int B, Hq, Hkv, N, T, nb_max, group, causal;
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  __device__ int rows_pad() const { return nb_max * BM; }
+  __device__ int seq_start(int b) const { return cu ? __ldg(cu + b) : b * N; }
+  __device__ int seq_len(int b) const { return cu ? __ldg(cu + b + 1) - __ldg(cu + b) : N; }
+  __device__ long long lse_index(int b, int h, int i) const {
+    return cu ? (long long)h * T + __ldg(cu + b) + i : ((long long)b * Hq + h) * N + i;
+  }
 };
+
+// Set-up (one thread): padded sequence starts; inconsistent cu_seqlens are
+// reported and then no sequence has rows (every unit exits).
+__global__ void bwd_setup_kernel(const BwdParams p) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  bool good = !p.cu || (__ldg(p.cu) == 0 && __ldg(p.cu + p.B) == p.T);
+  int acc = 0;
+  for (int b = 0; b < p.B; ++b) {
+    p.pstart[b] = acc;
+    const int L = p.seq_len(b);
+    if (L < 0) good = false;
+    acc += good ? (L + BM - 1) / BM * BM : 0;
+  }
+  p.pstart[p.B] = acc;
+  if (!good || acc > p.nb_max * BM) {
+    record_status(ATTN_ERR_BAD_SEQLENS);
+    for (int b = 0; b <= p.B; ++b) p.pstart[b] = 0;
+  }
+}
+
+// The sequence holding padded row r (r < pstart[B]): the last b with
+// pstart[b] <= r, by binary search.
+__device__ __forceinline__ int seq_of_padded_row(const BwdParams &p, int r) {
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.pstart[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// A work unit of the dK/dV kernel (kv head, key block) or of the dQ kernel
+// (query head, query block): unit u covers padded block u % nb_max of head
+// u / nb_max; blocks past the last sequence do nothing.
+struct BUnit {
+  bool valid;
+  int head, seq, blk, start, len, nblk;
+};
+__device__ __forceinline__ BUnit bwd_unit(const BwdParams &p, int u) {
+  BUnit t{};
+  t.head = u / p.nb_max;
+  const int r = (u % p.nb_max) * BM;
+  if (r >= p.pstart[p.B]) return t;
+  t.seq = seq_of_padded_row(p, r);
+  t.blk = (r - p.pstart[t.seq]) / BM;
+  t.start = p.seq_start(t.seq);
+  t.len = p.seq_len(t.seq);
+  t.nblk = (t.len + BM - 1) / BM;
+  t.valid = t.blk < t.nblk;
+  return t;
+}
 
 template <int D>
 struct BCfg {
@@ -80,17 +143,19 @@ enum : int {
 };
 
 // ------------------------------------------------------------------ row pass
-// One warp per (batch, head, row): D = sum_c dO o O, LSE log2(e); rows past
-// N (up to Npad) get D = 0 and +inf, which zeroes their P in the kernels.
+// One warp per (head, padded row): D = sum_c dO o O, LSE log2(e); padding
+// rows of a sequence get D = 0 and +inf, which zeroes their P in the kernels.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // bh Npad + i
-  if (row >= (long long)p.B * p.Hq * p.Npad) return;
-  const int i = (int)(row % p.Npad);
-  const long long bh = row / p.Npad;
-  const int b = (int)(bh / p.Hq), h = (int)(bh % p.Hq);
-  if (i >= p.N) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // h rows_pad + r
+  if (row >= (long long)p.Hq * p.rows_pad()) return;
+  const int h = (int)(row / p.rows_pad());
+  const int r = (int)(row % p.rows_pad());
+  if (r >= p.pstart[p.B]) return;
+  const int b = seq_of_padded_row(p, r);
+  const int i = r - p.pstart[b];
+  if (i >= p.seq_len(b)) {
     if (lane == 0) {
       p.lse2[row] = INFINITY;
       p.dsum[row] = 0.f;
@@ -98,7 +163,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
     return;
   }
   constexpr int PER = D / 32;
-  const long long off = (((long long)b * p.N + i) * p.Hq + h) * D + lane * PER;
+  const long long off = ((long long)(p.seq_start(b) + i) * p.Hq + h) * D + lane * PER;
   float acc = 0.f;
 #pragma unroll
   for (int x = 0; x < PER; ++x)
@@ -106,7 +171,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) {
     p.dsum[row] = acc;
-    p.lse2[row] = p.lse[((long long)b * p.Hq + h) * p.N + i] * 1.4426950408889634f;
+    p.lse2[row] = p.lse[p.lse_index(b, h, i)] * 1.4426950408889634f;
   }
 }
 
@@ -224,11 +289,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::A_OFF_CTL + 8 * B_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const int jb = blockIdx.x % p.nblk;
-  const int r = blockIdx.x / p.nblk;
-  const int kvh = r % p.Hkv, b = r / p.Hkv;
+  const BUnit un = bwd_unit(p, blockIdx.x);
+  if (!un.valid) return;   // uniform over the CTA, before any set-up
+  const int jb = un.blk, kvh = un.head, b = un.seq;
+  const int nblk = un.nblk, row0 = un.start, len = un.len;
   const int i0 = p.causal ? jb : 0;
-  const int steps = p.group * (p.nblk - i0);
+  const int steps = p.group * (nblk - i0);
   const uint32_t k_s = base, v_s = base + C::TILE;
 
   if (warp == 1) {
@@ -255,28 +321,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_arrive_expect_tx(ctl.bar(B_STATIC_FULL), 2 * C::TILE);
       for (int c = 0; c < C::CHUNKS; ++c) {
         tma_load_3d(k_s + c * CHUNK_BYTES, &tm_k, ctl.bar(B_STATIC_FULL), c * 64, kvh,
-                    b * p.N + jb * BM);
+                    row0 + jb * BM);
         tma_load_3d(v_s + c * CHUNK_BYTES, &tm_v, ctl.bar(B_STATIC_FULL), c * 64, kvh,
-                    b * p.N + jb * BM);
+                    row0 + jb * BM);
       }
       for (int s = 0; ok && s < steps; ++s) {
         const int slot = s & 1;
         if (s >= 2 && !(ok = wait_bounded(ctl.bar(B_EMPTY0 + slot), (uint32_t)((s - 2) >> 1) & 1u,
                                           abort_flag, p.timeout_ns)))
           break;
-        const int h = kvh * p.group + s / (p.nblk - i0);
-        const int ib = i0 + s % (p.nblk - i0);
+        const int h = kvh * p.group + s / (nblk - i0);
+        const int ib = i0 + s % (nblk - i0);
         const uint32_t dst = base + C::A_OFF_RING + slot * C::A_SLOT;
         mbar_arrive_expect_tx(ctl.bar(B_FULL0 + slot), 2 * C::TILE + 1024);
         for (int c = 0; c < C::CHUNKS; ++c) {
           tma_load_3d(dst + c * CHUNK_BYTES, &tm_q, ctl.bar(B_FULL0 + slot), c * 64, h,
-                      b * p.N + ib * BM);
+                      row0 + ib * BM);
           tma_load_3d(dst + C::TILE + c * CHUNK_BYTES, &tm_do, ctl.bar(B_FULL0 + slot), c * 64, h,
-                      b * p.N + ib * BM);
+                      row0 + ib * BM);
         }
-        const long long row0 = ((long long)b * p.Hq + h) * p.Npad + (long long)ib * BM;
-        bulk_load(dst + 2 * C::TILE, p.lse2 + row0, 512, ctl.bar(B_FULL0 + slot));
-        bulk_load(dst + 2 * C::TILE + 512, p.dsum + row0, 512, ctl.bar(B_FULL0 + slot));
+        const long long prow =
+            (long long)h * p.rows_pad() + p.pstart[b] + (long long)ib * BM;   // 512-B aligned
+        bulk_load(dst + 2 * C::TILE, p.lse2 + prow, 512, ctl.bar(B_FULL0 + slot));
+        bulk_load(dst + 2 * C::TILE + 512, p.dsum + prow, 512, ctl.bar(B_FULL0 + slot));
         ++issued;
       }
       if (*abort_flag) {   // drain: bounded waits for the copies issued
@@ -349,7 +416,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                            p.timeout_ns)))
         break;
       tc_fence_after();
-      const int ib = i0 + s % (p.nblk - i0);
+      const int ib = i0 + s % (nblk - i0);
       const float *lse2 =
           reinterpret_cast<const float *>(smem + C::A_OFF_RING + slot * C::A_SLOT + 2 * C::TILE);
       const float *dsum = lse2 + 128;
@@ -383,8 +450,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
-      const bool live = key < p.N;
-      const long long off = (((long long)b * p.N + key) * p.Hkv + kvh) * D + hf * (D / 2);
+      const bool live = key < len;
+      const long long off = ((long long)(row0 + key) * p.Hkv + kvh) * D + hf * (D / 2);
       store_row_bf16<D / 2>(tmem + lane_off + COL_DV + hf * (D / 2), 1.f, p.dv + off, live);
       store_row_bf16<D / 2>(tmem + lane_off + COL_DK + hf * (D / 2), p.scale, p.dk + off, live);
     }
@@ -417,11 +484,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::B_OFF_CTL + 8 * B_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const int ib = blockIdx.x % p.nblk;
-  const int r = blockIdx.x / p.nblk;
-  const int h = r % p.Hq, b = r / p.Hq;
+  const BUnit un = bwd_unit(p, blockIdx.x);
+  if (!un.valid) return;   // uniform over the CTA, before any set-up
+  const int ib = un.blk, h = un.head, b = un.seq;
+  const int row0 = un.start, len = un.len;
   const int kvh = h / p.group;
-  const int steps = p.causal ? ib + 1 : p.nblk;
+  const int steps = p.causal ? ib + 1 : un.nblk;
   const uint32_t q_s = base, do_s = base + C::TILE;
 
   if (warp == 1) {
@@ -448,9 +516,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_arrive_expect_tx(ctl.bar(B_STATIC_FULL), 2 * C::TILE);
       for (int c = 0; c < C::CHUNKS; ++c) {
         tma_load_3d(q_s + c * CHUNK_BYTES, &tm_q, ctl.bar(B_STATIC_FULL), c * 64, h,
-                    b * p.N + ib * BM);
+                    row0 + ib * BM);
         tma_load_3d(do_s + c * CHUNK_BYTES, &tm_do, ctl.bar(B_STATIC_FULL), c * 64, h,
-                    b * p.N + ib * BM);
+                    row0 + ib * BM);
       }
       for (int s = 0; ok && s < steps; ++s) {
         const int slot = s & 1;
@@ -461,9 +529,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         mbar_arrive_expect_tx(ctl.bar(B_FULL0 + slot), 2 * C::TILE);
         for (int c = 0; c < C::CHUNKS; ++c) {
           tma_load_3d(dst + c * CHUNK_BYTES, &tm_k, ctl.bar(B_FULL0 + slot), c * 64, kvh,
-                      b * p.N + s * BM);
+                      row0 + s * BM);
           tma_load_3d(dst + C::TILE + c * CHUNK_BYTES, &tm_v, ctl.bar(B_FULL0 + slot), c * 64,
-                      kvh, b * p.N + s * BM);
+                      kvh, row0 + s * BM);
         }
         ++issued;
       }
@@ -520,7 +588,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int qrow = ib * BM + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float c = p.scale_log2;
-    const long long prow = ((long long)b * p.Hq + h) * p.Npad + qrow;
+    const long long prow = (long long)h * p.rows_pad() + p.pstart[b] + qrow;
     const float lse2 = p.lse2[prow];   // +inf on padding rows: P = 0
     const float dsum = p.dsum[prow];
     bool ok = true;
@@ -528,7 +596,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (!(ok = wait_warp(ctl.bar(B_S_FULL0 + hf), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
         break;
       tc_fence_after();
-      const bool edge = (s * BM + BM > p.N) || (p.causal && s == ib);
+      const bool edge = (s * BM + BM > len) || (p.causal && s == ib);
 #pragma unroll 1
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * hf + 32 * ch;
@@ -541,8 +609,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           float p0 = ex2_approx(sv[x] * c - lse2);
           float p1 = ex2_approx(sv[x + 1] * c - lse2);
           if (edge) {   // keys past the sequence, or after the query (causal)
-            if (k0 >= p.N || (p.causal && k0 > qrow)) p0 = 0.f;
-            if (k0 + 1 >= p.N || (p.causal && k0 + 1 > qrow)) p1 = 0.f;
+            if (k0 >= len || (p.causal && k0 > qrow)) p0 = 0.f;
+            if (k0 + 1 >= len || (p.causal && k0 + 1 > qrow)) p1 = 0.f;
           }
           dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum), p1 * (dp[x + 1] - dsum));
         }
@@ -555,8 +623,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
       store_row_bf16<D / 2>(tmem + lane_off + COL_DQ + hf * (D / 2), p.scale,
-                            p.dq + (((long long)b * p.N + qrow) * p.Hq + h) * D + hf * (D / 2),
-                            qrow < p.N);
+                            p.dq + ((long long)(row0 + qrow) * p.Hq + h) * D + hf * (D / 2),
+                            qrow < len);
     }
   }
   tc_fence_before();
@@ -571,17 +639,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }  // namespace attn
 
 // ------------------------------------------------------------------ host
-extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N) {
+namespace attn {
+namespace bwd {
+// Padded 128-row blocks of all sequences: B ceil(N / 128) for a fixed batch
+// is at most ceil(rows / 128) + B, which also bounds a packed batch.
+static long long bwd_nb_max(int B, long long rows) { return (rows + BM - 1) / BM + B; }
+}  // namespace bwd
+}  // namespace attn
+
+extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int packed) {
   if (B < 1 || Hq < 1 || N < 1) return 0;
-  const size_t npad = ((size_t)N + attn::BM - 1) / attn::BM * attn::BM;
-  return 2 * (size_t)B * Hq * npad * sizeof(float);
+  const long long rows = packed ? (long long)N : (long long)B * N;
+  const size_t rows_pad = (size_t)attn::bwd::bwd_nb_max(B, rows) * attn::BM;
+  return 2 * (size_t)Hq * rows_pad * sizeof(float) + ((size_t)B + 1) * sizeof(int);
 }
 
 extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                                 const void *dout, const float *lse, void *dq, void *dk,
                                 void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
-                                int causal, void *workspace, size_t workspace_bytes,
-                                cudaStream_t stream) {
+                                int causal, const int *cu_seqlens, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
   using namespace attn;
   using namespace attn::bwd;
   if (B < 0 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -594,11 +671,13 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   };
   if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
       misaligned(dout, 16) || misaligned(dq, 16) || misaligned(dk, 16) || misaligned(dv, 16) ||
-      misaligned(lse, 4) || misaligned(workspace, 16))
+      misaligned(lse, 4) || misaligned(workspace, 16) || misaligned(cu_seqlens, 4))
     return ATTN_ERR_ALIGNMENT;
-  const long long rows = (long long)B * N;
+  const long long rows = cu_seqlens ? (long long)N : (long long)B * N;
   if (rows > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_workspace_bytes(B, Hq, N);
+  const long long nb_max = bwd_nb_max(B, rows);
+  if (nb_max * BM * (long long)Hq > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, Hq, N, cu_seqlens ? 1 : 0);
   if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -632,23 +711,26 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   p.o = reinterpret_cast<const __nv_bfloat16 *>(o);
   p.dout = reinterpret_cast<const __nv_bfloat16 *>(dout);
   p.lse = lse;
-  p.nblk = (N + BM - 1) / BM;
-  p.Npad = p.nblk * BM;
+  p.cu = cu_seqlens;
+  p.nb_max = (int)nb_max;
   p.lse2 = reinterpret_cast<float *>(workspace);
-  p.dsum = p.lse2 + (size_t)B * Hq * p.Npad;
+  p.dsum = p.lse2 + (size_t)Hq * nb_max * BM;
+  p.pstart = reinterpret_cast<int *>(p.dsum + (size_t)Hq * nb_max * BM);
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
-  p.N = N;
+  p.N = cu_seqlens ? 0 : N;
+  p.T = (int)rows;
   p.group = Hq / Hkv;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
 
-  const unsigned row_blocks = (unsigned)(((long long)B * Hq * p.Npad + 7) / 8);
-  const unsigned kv_units = (unsigned)((long long)B * Hkv * p.nblk);
-  const unsigned q_units = (unsigned)((long long)B * Hq * p.nblk);
+  const unsigned row_blocks = (unsigned)(((long long)Hq * nb_max * BM + 7) / 8);
+  const unsigned kv_units = (unsigned)((long long)Hkv * nb_max);
+  const unsigned q_units = (unsigned)((long long)Hq * nb_max);
+  bwd_setup_kernel<<<1, 32, 0, stream>>>(p);
   if (d == 64) {
     bwd_rows_kernel<64><<<row_blocks, 256, 0, stream>>>(p);
     attn_bwd_dkdv_kernel<64><<<kv_units, BWD_THREADS, BCfg<64>::A_SMEM, stream>>>(mq, mdo, mk, mv, p);

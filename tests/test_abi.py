@@ -165,7 +165,7 @@ def test_paged_status_string(lib):
 def call_bwd(**kw):
     args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000,
                 dk=0x8000, dv=0x9000, B=2, Hq=8, Hkv=2, N=256, d=128, scale=0.088, causal=1,
-                workspace=0xA000, workspace_bytes=1 << 20, stream=0)
+                cu_seqlens=None, workspace=0xA000, workspace_bytes=1 << 20, stream=0)
     args.update(kw)
     return pkg.attn_bwd(check=False, **args)
 
@@ -179,10 +179,12 @@ def test_bwd_invalid_arguments_rejected_without_gpu(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [dict(dq=0x7008), dict(dout=0x5004), dict(workspace=0xA004),
-                                dict(lse=0x6002)])
+                                dict(lse=0x6002), dict(cu_seqlens=0xB002)])
 def test_bwd_misaligned_pointers_rejected(lib, kw):
     assert call_bwd(**kw) == pkg.ATTN_ERR_ALIGNMENT
 
 
 def test_bwd_workspace_size():
-    assert pkg.attn_bwd_workspace_bytes(2, 8, 300) == 2 * 2 * 8 * 384 * 4
+    # padded blocks: ceil(rows / 128) + B; two fp32 values per (head, padded row); B + 1 ints
+    assert pkg.attn_bwd_workspace_bytes(2, 8, 300) == 2 * 8 * (5 + 2) * 128 * 4 + 3 * 4
+    assert pkg.attn_bwd_workspace_bytes(3, 4, 1000, packed=True) == 2 * 4 * (8 + 3) * 128 * 4 + 16

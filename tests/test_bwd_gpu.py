@@ -40,7 +40,8 @@ def run_bwd(q, k, v, g, causal):
     gv = torch.full_like(dv_, float("nan"))
     n = pkg.attn_bwd_workspace_bytes(B, Hq, N)
     ws = torch.full(((n + 15) // 16 * 4,), float("nan"), dtype=torch.float32, device=dev)
-    pkg.attn_bwd(dq_, dk_, dv_, o, dg, lse, gq, gk, gv, B, Hq, Hkv, N, d, d ** -0.5, causal, ws)
+    pkg.attn_bwd(dq_, dk_, dv_, o, dg, lse, gq, gk, gv, B, Hq, Hkv, N, d, d ** -0.5, causal,
+                 workspace=ws)
     st = pkg.attn_get_status()
     assert st == pkg.ATTN_OK, pkg.attn_status_string(st)
     return [t.float().cpu().numpy() for t in (gq, gk, gv)]
@@ -106,5 +107,44 @@ def test_bwd_small_workspace_rejected():
     t = torch.zeros((B, N, H, d), dtype=torch.bfloat16, device=dev)
     lse = torch.zeros((B, H, N), dtype=torch.float32, device=dev)
     ws = torch.empty((16,), dtype=torch.float32, device=dev)
-    rc = pkg.attn_bwd(t, t, t, t, t, lse, t, t, t, B, H, H, N, d, 0.125, True, ws, check=False)
+    rc = pkg.attn_bwd(t, t, t, t, t, lse, t, t, t, B, H, H, N, d, 0.125, True, workspace=ws,
+                      check=False)
     assert rc == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_packed(d, causal):
+    lens = [1, 127, 128, 129, 300, 0, 513, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, Hq, Hkv = int(cu[-1]), 4, 2
+    q, k, v = rand((T, Hq, d), 41 + d, 2.0), rand((T, Hkv, d), 42 + d), rand((T, Hkv, d), 43 + d)
+    g = rand((T, Hq, d), 44 + d)
+    dev = torch.device("cuda:0")
+    dcu = torch.tensor(cu, device=dev)
+    dq_, dk_, dv_, dg = (t.to(dev) for t in (q, k, v, g))
+    o, lse = pkg.attention(dq_, dk_, dv_, causal=causal, cu_seqlens=dcu)
+    grads = pkg.attention_backward(dq_, dk_, dv_, o, lse, dg, causal, cu_seqlens=dcu)
+    assert pkg.attn_get_status() == pkg.ATTN_OK
+    refs = oracle.attn_bwd_oracle(q, k, v, g, len(lens), Hq, Hkv, T, d, d ** -0.5, causal,
+                                  cu_seqlens=cu)
+    for name, m, r in zip(("dq", "dk", "dv"), grads, refs):
+        m = m.float().cpu().numpy()
+        assert np.isfinite(m).all()
+        err = np.abs(m - r)
+        assert err.max() <= REL_MAX * max(np.abs(r).max(), 1e-3), (name, err.max())
+        assert err.mean() <= REL_MEAN * max(np.abs(r).mean(), 1e-3), (name, err.mean())
+
+
+def test_bwd_packed_bad_offsets_reported():
+    T, H, d = 300, 2, 64
+    dev = torch.device("cuda:0")
+    t = rand((T, H, d), 51).to(dev)
+    lse = torch.zeros((H, T), dtype=torch.float32, device=dev)
+    out = torch.full_like(t, float("nan"))
+    bad = torch.tensor([0, 200, 100], dtype=torch.int32, device=dev)   # decreasing
+    n = pkg.attn_bwd_workspace_bytes(2, H, T, packed=True)
+    ws = torch.empty(((n + 15) // 16 * 4,), dtype=torch.float32, device=dev)
+    pkg.attn_bwd(t, t, t, t, t, lse, out, out, out, 2, H, H, T, d, 0.125, True, bad, ws)
+    assert pkg.attn_get_status() == pkg.ATTN_ERR_BAD_SEQLENS
+    assert torch.isnan(out.float()).all()
