@@ -1312,6 +1312,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+}  // namespace attn
+
+#include "attn_fwd2.cuh"
+
+namespace attn {
+
 // One block waits on a barrier that nobody signals, with a short limit: the
 // wait runs out and records ATTN_ERR_TIMEOUT.  Used to test that path.
 __global__ void selftest_timeout_kernel(unsigned long long timeout_ns) {
@@ -1412,6 +1418,7 @@ static bool opt_in_smem(K kernel, uint32_t bytes) {
 // Per device: compute capability check and the shared-memory opt-in of the
 // kernel instantiations, done once.
 static int g_sm_count[MAX_DEVICES];
+static bool g_two_tiles_ok[MAX_DEVICES];
 
 // Scratch of attn_fwd_decode_static: a fixed device array (the library
 // allocates nothing); its address on each device is looked up once, when
@@ -1450,8 +1457,16 @@ static attn_status prepare_device(int dev) {
       !opt_in_smem(attn_fwd_kernel<256, 2>, Cfg<256>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<64, 3>, Cfg<64>::SMEM_BYTES) ||
       !opt_in_smem(attn_fwd_kernel<128, 3>, Cfg<128>::SMEM_BYTES) ||
-      !opt_in_smem(attn_fwd_kernel<256, 3>, Cfg<256>::SMEM_BYTES))
+      !opt_in_smem(attn_fwd_kernel<256, 3>, Cfg<256>::SMEM_BYTES) ||
+      !opt_in_smem(two::attn_fwd2_kernel<64>, two::Cfg2<64>::SMEM_BYTES) ||
+      !opt_in_smem(two::attn_fwd2_kernel<128>, two::Cfg2<128>::SMEM_BYTES))
     return ATTN_ERR_CUDA;
+  // the two-tile kernel's register split needs its launch share
+  cudaFuncAttributes fa64, fa128;
+  if (cudaFuncGetAttributes(&fa64, two::attn_fwd2_kernel<64>) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa128, two::attn_fwd2_kernel<128>) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  g_two_tiles_ok[dev] = fa64.numRegs >= two::REGS_NEEDED && fa128.numRegs >= two::REGS_NEEDED;
   if (cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch) != cudaSuccess)
     return ATTN_ERR_CUDA;
   state[dev] = 1;
@@ -1532,7 +1547,11 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
   p.cap_k2 = cap > 0.f ? scale / cap : 0.f;
   p.alibi = slopes;
   const bool mod = cap > 0.f || slopes != nullptr;
-  p.unit_rows = BM;
+  // Two query tiles per CTA (head dims 64, 128) unless a window or a score
+  // modifier asks for the one-tile kernel.
+  const bool two_tiles =
+      g_two_tiles_ok[dev] && !mod && d <= 128 && p.wl >= N && (causal || p.wr >= N);
+  p.unit_rows = two_tiles ? two::UNIT_ROWS : BM;
   p.num_units = (N + p.unit_rows - 1) / p.unit_rows;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -1550,6 +1569,15 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
   const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
 
   const unsigned gr = (unsigned)grid;
+  if (two_tiles) {
+    if (d == 64)
+      two::attn_fwd2_kernel<64><<<gr, two::THREADS2, two::Cfg2<64>::SMEM_BYTES, stream>>>(
+          mq, mk, mv, p);
+    else
+      two::attn_fwd2_kernel<128><<<gr, two::THREADS2, two::Cfg2<128>::SMEM_BYTES, stream>>>(
+          mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
   switch (d * 2 + (mod ? 1 : 0)) {
     case 128: attn_fwd_kernel<64, 0><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;
     case 129: attn_fwd_kernel<64, 1><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mq, mk, mv, p); break;

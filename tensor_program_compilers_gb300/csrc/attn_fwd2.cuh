@@ -1,0 +1,485 @@
+// attn_fwd2.cuh -- the attention forward with two query tiles per CTA, for
+// head dims 64 and 128 without a key window or score modifier.  Included by
+// attn_fwd.cu, whose helpers (waits, tile decoding, softmax pieces, MMA
+// issue) it uses.
+//
+// A work unit is 256 query rows of one (sequence, query head): tile A is rows
+// 0..127 of the unit, tile B rows 128..255.  Both tiles walk the same key
+// tiles, so each K_j and V_j is loaded once for 256 rows.  Every softmax
+// thread owns one whole query row (all 128 keys of a key tile), so no two
+// warps share a row; while the softmax warps of one tile work on P, the
+// tensor core runs the other tile's products.  The computation per row is the
+// one attn_fwd.cu describes (online softmax with a lazily moved reference
+// maximum; tang, section 2.3, Table 1 "FlashAttention forward"), with O
+// divided by the exact fp32 row sum.
+//
+// Warp roles (384 threads):
+//   warps 0-3  softmax of tile A: lane t of warp w owns query row 32 w + t
+//              (TMEM lane 32 w + t)
+//   warps 4-7  softmax of tile B (TMEM lane quarter w % 4)
+//   warp 8     TMA producer: Q_A, Q_B of the unit, then K_0, V_0, K_1, V_1, ...
+//   warp 9     TMEM allocator and MMA issuer (one thread)
+//   warps 10, 11 idle (they complete the third warpgroup)
+//
+// Tensor memory (512 columns): S_A [0, 128), S_B [128, 256),
+// O_A [256, 256 + d), O_B [256 + d, 256 + 2d).  P_X (bf16 pairs, keys 2c and
+// 2c + 1 in column c) is written over columns [0, 64) of S_X.
+//
+// MMA order (one thread; the tensor core runs one thread's MMAs in issue
+// order): QK_A(0), QK_B(0), then for each key step j
+//   PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
+// QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X(j) from it, and
+// the commit that signals S_X(j+1) also covers PV_X(j): a softmax warp that
+// sees S_X(j+1) may rescale O_X at once.
+
+namespace attn {
+namespace two {
+
+constexpr int THREADS2 = 384;   // three warpgroups
+constexpr int WARP_PROD = 8, WARP_MMA = 9;   // warps 10, 11 only complete the third warpgroup
+// Register split (setmaxnreg): the kernel is built for 168 registers a thread
+// (384 threads; three warps share each SM sub-partition); the third
+// warpgroup gives part of its share to the softmax warpgroups:
+// 2 x 128 x 208 + 128 x 72 = 62,464 <= 384 x 168 = 64,512.  The host checks
+// the built register count against this before it uses the kernel.
+constexpr int REGS_SOFTMAX = 208, REGS_OTHER = 72;
+constexpr int REGS_NEEDED = (2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER + THREADS2 - 1) / THREADS2;
+constexpr int UNIT_ROWS = 2 * BM;
+constexpr int UNIT_INTS = 10;   // valid, seq_start, len, unit, h, nA, nB, lse lo/hi
+
+template <int D>
+struct Cfg2 {
+  static constexpr int CHUNKS = D / 64;
+  static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;   // one 128-row Q, K or V tile
+  static constexpr int QB = 2;                                    // Q buffers (two tiles each)
+  static constexpr int STAGES = D == 64 ? 8 : 3;                  // K/V ring slots
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_KV = 2 * TILE_BYTES * QB;
+  static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
+  static constexpr uint32_t CTL_BYTES = 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment
+  static constexpr uint32_t COL_O = 256;                               // O_X at COL_O + D X
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(COL_O + 2 * D <= TMEM_COLS, "tensor memory");
+};
+
+enum : int {
+  T_Q_FULL0 = 0,   // Q buffer b (both tiles) loaded, b < 2
+  T_Q_FULL1,
+  T_Q_EMPTY0,      // Q buffer b no longer read (MMA issuer commit)
+  T_Q_EMPTY1,
+  T_S_FULL0,       // S_X written (commit; also covers PV_X of the previous step), X < 2
+  T_S_FULL1,
+  T_P_FULL0,       // P_X written over S_X (the tile's four softmax warps)
+  T_P_FULL1,
+  T_PV_DONE0,      // PV_X completed (commit)
+  T_PV_DONE1,
+  T_O_FREE0,       // O_X read by the epilogue (four warps)
+  T_O_FREE1,
+  T_INFO_FULL0,                            // unit-info entry e written (producer)
+  T_INFO_EMPTY0 = T_INFO_FULL0 + INFO_SLOTS,   // entry e consumed
+  T_DRAIN = T_INFO_EMPTY0 + INFO_SLOTS,    // teardown drain of the MMA issuer
+  T_RING                                   // K/V ring: full[0..STAGES), empty[0..STAGES)
+};
+
+struct Ctl2 {
+  uint32_t bar0;     // shared address of barrier 0 (8 bytes apart)
+  uint32_t *words;   // [0] TMEM base, [1] abort flag
+  int *info;         // INFO_SLOTS entries of UNIT_INTS ints
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+};
+
+struct UnitInfo {
+  int valid, seq_start, len, unit, h, n[2];
+  long long lse_base;
+};
+
+// Key tiles of the two tiles of unit u of a sequence of len rows: causal
+// rows see keys up to their own position (tile A's last key tile is 2u, tile
+// B's 2u + 1); a tile that starts past the sequence has none.
+__device__ __forceinline__ void unit_steps(int causal, int u, int len, int &nA, int &nB) {
+  const int r0 = UNIT_ROWS * u;
+  const int kt = (len + BN - 1) / BN;
+  nA = r0 < len ? (causal ? min(kt, 2 * u + 1) : kt) : 0;
+  nB = r0 + BM < len ? (causal ? min(kt, 2 * u + 2) : kt) : 0;
+}
+
+__device__ __forceinline__ bool read_unit(const Ctl2 &c, int k, UnitInfo &t,
+                                          volatile uint32_t *abort_flag,
+                                          unsigned long long timeout_ns) {
+  const int e = k % INFO_SLOTS;
+  if (!wait_bounded(c.bar(T_INFO_FULL0 + e), (uint32_t)(k / INFO_SLOTS) & 1u, abort_flag,
+                    timeout_ns))
+    return false;
+  const volatile int *src = c.info + e * UNIT_INTS;
+  t.valid = src[0];
+  t.seq_start = src[1];
+  t.len = src[2];
+  t.unit = src[3];
+  t.h = src[4];
+  t.n[0] = src[5];
+  t.n[1] = src[6];
+  t.lse_base = (long long)(unsigned)src[7] | ((long long)src[8] << 32);
+  return true;
+}
+
+// p = 2^(h c - m c) for the row's 128 scores (two halves) into pk0, pk1;
+// returns the sum of the fp32 values.
+__device__ __forceinline__ float exp_row(const float (&h0)[HB], const float (&h1)[HB],
+                                         float c, float m, uint32_t (&pk0)[HB / 2],
+                                         uint32_t (&pk1)[HB / 2]) {
+  const uint64_t c2 = f2_pack(c, c);
+  const float nmc = (m == -INFINITY) ? 0.f : -m * c;
+  const uint64_t nm2 = f2_pack(nmc, nmc);
+  uint64_t acc[4] = {0, 0, 0, 0}, unused[4] = {0, 0, 0, 0};
+  exp_half<false>(h0, c2, nm2, pk0, acc, unused);
+  exp_half<false>(h1, c2, nm2, pk1, acc, unused);
+  return sum_acc(acc);
+}
+
+// ================================================================ kernel
+template <int D>
+__global__ void __launch_bounds__(THREADS2, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg2<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t base_s = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_CTL);
+  Ctl2 ctl;
+  ctl.bar0 = smem_u32(bars);
+  ctl.words = reinterpret_cast<uint32_t *>(bars + T_RING + 2 * C::STAGES);
+  ctl.info = reinterpret_cast<int *>(ctl.words + 4);
+  static_assert((T_RING + 2 * C::STAGES) * 8 + 16 + INFO_SLOTS * UNIT_INTS * 4 <= C::CTL_BYTES,
+                "control block");
+  volatile uint32_t *abort_flag = ctl.words + 1;
+  const uint32_t q_s = base_s + C::OFF_Q;
+  const uint32_t kv_s = base_s + C::OFF_KV;
+  constexpr uint32_t INFO_CONSUMERS = 1 + 8;   // the MMA issuer, the softmax warps
+
+  if (warp == WARP_MMA) {
+    if (lane == 0) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(ctl.bar(T_Q_FULL0 + b), 1);
+        mbar_init(ctl.bar(T_Q_EMPTY0 + b), 1);
+        mbar_init(ctl.bar(T_S_FULL0 + b), 1);
+        mbar_init(ctl.bar(T_P_FULL0 + b), 4);
+        mbar_init(ctl.bar(T_PV_DONE0 + b), 1);
+        mbar_init(ctl.bar(T_O_FREE0 + b), 4);
+      }
+      for (int e = 0; e < INFO_SLOTS; ++e) {
+        mbar_init(ctl.bar(T_INFO_FULL0 + e), 1);
+        mbar_init(ctl.bar(T_INFO_EMPTY0 + e), INFO_CONSUMERS);
+      }
+      mbar_init(ctl.bar(T_DRAIN), 1);
+      for (int s = 0; s < C::STAGES; ++s) {
+        mbar_init(ctl.bar(T_RING + s), 1);
+        mbar_init(ctl.bar(T_RING + C::STAGES + s), 1);
+      }
+      ctl.words[1] = 0u;
+      mbar_init_fence();
+    }
+    __syncwarp();
+    tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
+    tmem_relinquish();
+  } else if (warp == WARP_PROD && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.words[0];
+
+  if (warp >= 8) {
+   setmaxnreg_dec<REGS_OTHER>();
+   if (warp == WARP_PROD) {
+    // ---------------- producer: decode units, publish them, load Q and K/V
+    long long pos = 0;   // global ring position
+    int q_loads = 0;
+    bool ok = true;
+    long long round = 0;
+    for (int k = 0; ok; ++k) {
+      // round r covers units [r G, (r+1) G), odd rounds backwards (longest
+      // units first overall, so each CTA's total evens out)
+      const long long G = gridDim.x;
+      const Tile t =
+          decode_tile(p, round * G + ((round & 1) ? G - 1 - blockIdx.x : blockIdx.x), false);
+      ++round;
+      int nA = 0, nB = 0;
+      if (t.valid) unit_steps(p.causal, t.unit, t.len, nA, nB);
+      if (lane == 0) {
+        const int e = k % INFO_SLOTS;
+        ok = wait_bounded(ctl.bar(T_INFO_EMPTY0 + e), ((uint32_t)(k / INFO_SLOTS) & 1u) ^ 1u,
+                          abort_flag, p.timeout_ns);
+        if (ok) {
+          int *dst = ctl.info + e * UNIT_INTS;
+          dst[0] = t.valid;
+          dst[1] = t.seq_start;
+          dst[2] = t.len;
+          dst[3] = t.unit;
+          dst[4] = t.h;
+          dst[5] = nA;
+          dst[6] = nB;
+          dst[7] = (int)(unsigned)(t.lse_base & 0xFFFFFFFFll);
+          dst[8] = (int)(t.lse_base >> 32);
+          mbar_arrive(ctl.bar(T_INFO_FULL0 + e));   // release: the entry is visible
+        }
+        if (ok && t.valid) {
+          const int qb = k % C::QB;
+          const int kvh = t.h / p.group;
+          const int row0 = t.seq_start + UNIT_ROWS * t.unit;
+          if (k >= C::QB)
+            ok = wait_bounded(ctl.bar(T_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
+                              abort_flag, p.timeout_ns);
+          if (ok) {
+            const int tiles = nB > 0 ? 2 : 1;
+            ++q_loads;
+            mbar_arrive_expect_tx(ctl.bar(T_Q_FULL0 + qb), C::TILE_BYTES * tiles);
+            for (int x = 0; x < tiles; ++x)
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_3d(q_s + (2 * qb + x) * C::TILE_BYTES + c * CHUNK_BYTES, &tm_q,
+                            ctl.bar(T_Q_FULL0 + qb), c * 64, t.h, row0 + BM * x);
+          }
+          // K_0, V_0, K_1, V_1, ...
+          const int n = max(nA, nB);
+          for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
+            const int slot = (int)(pos % C::STAGES);
+            if (!(ok = wait_bounded(ctl.bar(T_RING + C::STAGES + slot),
+                                    ((uint32_t)(pos / C::STAGES) & 1u) ^ 1u, abort_flag,
+                                    p.timeout_ns)))
+              break;
+            mbar_arrive_expect_tx(ctl.bar(T_RING + slot), C::TILE_BYTES);
+            const uint32_t dst = kv_s + slot * C::TILE_BYTES;
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * CHUNK_BYTES, (item & 1) ? &tm_v : &tm_k,
+                          ctl.bar(T_RING + slot), c * 64, kvh, t.seq_start + (item >> 1) * BN);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && t.valid;
+    }
+    if (lane == 0 && *abort_flag) {
+      // drain: wait (bounded) for the copies this thread issued
+      for (int b = 0; b < C::QB && b < q_loads; ++b) {
+        const int last = b + C::QB * ((q_loads - 1 - b) / C::QB);
+        wait_drain(ctl.bar(T_Q_FULL0 + b), (uint32_t)(last / C::QB) & 1u, p.timeout_ns);
+      }
+      for (int s = 0; s < C::STAGES && s < pos; ++s) {
+        const long long last = s + C::STAGES * ((pos - 1 - s) / C::STAGES);
+        wait_drain(ctl.bar(T_RING + s), (uint32_t)(last / C::STAGES) & 1u, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+   } else if (warp == WARP_MMA) {
+    // ---------------- MMA issuer (one thread)
+    if (lane == 0) {
+      const uint64_t kdesc0 = smem_desc_sw128(kv_s, 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(kv_s, CHUNK_BYTES, 1024);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
+      long long base = 0;            // ring position of the unit's first load (K_0)
+      long long npv[2] = {0, 0};     // PV_X issued so far (P_FULL_X phases)
+      int nunits[2] = {0, 0};        // units in which tile X had work (O_FREE_X phases)
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        UnitInfo t;
+        if (!(ok = read_unit(ctl, k, t, abort_flag, p.timeout_ns))) break;
+        mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
+        if (!t.valid) break;
+        const int qb = k % C::QB;
+        if (!(ok = wait_bounded(ctl.bar(T_Q_FULL0 + qb), (uint32_t)(k / C::QB) & 1u,
+                                abort_flag, p.timeout_ns)))
+          break;
+        const uint64_t qdesc[2] = {smem_desc_sw128(q_s + 2 * qb * C::TILE_BYTES, 16, 1024),
+                                   smem_desc_sw128(q_s + (2 * qb + 1) * C::TILE_BYTES, 16, 1024)};
+        const int n = max(t.n[0], t.n[1]);
+        // K_j at ring position base + 2j, V_j at base + 2j + 1; the first
+        // tile to use a slot waits for it, the last one releases it
+        auto ring_wait = [&](long long ps) -> bool {
+          return wait_bounded(ctl.bar(T_RING + (int)(ps % C::STAGES)),
+                              (uint32_t)(ps / C::STAGES) & 1u, abort_flag, p.timeout_ns);
+        };
+        auto ring_release = [&](long long ps) {
+          tc_commit(ctl.bar(T_RING + C::STAGES + (int)(ps % C::STAGES)));
+        };
+        auto qk = [&](int x, int j) {
+          const long long ps = base + 2 * j;
+          issue_qk<D>(tmem + 128u * (uint32_t)x, qdesc[x],
+                      desc_add(kdesc0, (uint32_t)(ps % C::STAGES) * C::TILE_BYTES));
+          tc_commit(ctl.bar(T_S_FULL0 + x));
+        };
+        if (!(ok = ring_wait(base))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (t.n[x] > 0) qk(x, 0);
+        ring_release(base);
+        for (int j = 0; ok && j < n; ++j) {
+          bool v_ready = false, k_ready = false;
+          const long long pv_pos = base + 2 * j + 1, qk_pos = base + 2 * j + 2;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (j >= t.n[x]) continue;
+            // PV_X(j): O_X (+)= P_X(j) V_j; a unit's first overwrites O_X
+            if (j == 0 && nunits[x] > 0 &&
+                !(ok = wait_bounded(ctl.bar(T_O_FREE0 + x), (uint32_t)(nunits[x] - 1) & 1u,
+                                    abort_flag, p.timeout_ns)))
+              break;
+            if (!(ok = wait_bounded(ctl.bar(T_P_FULL0 + x), (uint32_t)npv[x] & 1u, abort_flag,
+                                    p.timeout_ns)))
+              break;
+            if (!v_ready && !(ok = ring_wait(pv_pos))) break;
+            v_ready = true;
+            tc_fence_after();
+            const uint64_t vdesc =
+                desc_add(vdesc0, (uint32_t)(pv_pos % C::STAGES) * C::TILE_BYTES);
+            const uint32_t s_x = tmem + 128u * (uint32_t)x;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(tmem + C::COL_O + (uint32_t)(D * x), s_x + kk * 8,
+                     desc_add(vdesc, kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(ctl.bar(T_PV_DONE0 + x));
+            ++npv[x];
+            if (x == 1 || j >= t.n[1]) ring_release(pv_pos);   // V_j's last use
+            // QK_X(j+1)
+            if (j + 1 < t.n[x]) {
+              if (!k_ready && !(ok = ring_wait(qk_pos))) break;
+              k_ready = true;
+              tc_fence_after();
+              qk(x, j + 1);
+              if (x == 1 || j + 1 >= t.n[1]) ring_release(qk_pos);   // K_{j+1}'s last use
+            }
+          }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (t.n[x] > 0) ++nunits[x];
+        tc_commit(ctl.bar(T_Q_EMPTY0 + qb));   // Q buffer free once its QKs are done
+        base += 2 * n;
+      }
+      tc_commit(ctl.bar(T_DRAIN));   // no MMA may be in flight at teardown
+      wait_drain(ctl.bar(T_DRAIN), 0, p.timeout_ns);
+    }
+    __syncwarp();
+   }
+  } else {
+    setmaxnreg_inc<REGS_SOFTMAX>();
+    // ---------------- softmax warps: tile x = warp / 4, lane quarter warp % 4
+    const int x = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t s_t = tmem + lane_off + 128u * (uint32_t)x;
+    const uint32_t o_t = tmem + lane_off + C::COL_O + (uint32_t)(D * x);
+    const float c = p.scale_log2;
+    long long g = 0;   // key steps of tile x so far (S_FULL, P_FULL, PV_DONE phases)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      UnitInfo t;
+      ok = __all_sync(0xffffffffu, read_unit(ctl, k, t, abort_flag, p.timeout_ns));
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
+      if (!t.valid) break;
+      const int nx = t.n[x];
+      if (nx == 0) continue;
+      const int r0 = UNIT_ROWS * t.unit + BM * x;   // the tile's first row
+      const int q_idx = r0 + row;
+      const int lim = p.causal ? min(t.len, q_idx + 1) : t.len;   // visible keys [0, lim)
+      float m = -INFINITY, l = 0.f;
+      bool s_ready = false;   // early test of this step's S
+      for (int j = 0; j < nx; ++j, ++g) {
+        if (!__all_sync(0xffffffffu, s_ready) &&
+            !(ok = wait_warp(ctl.bar(T_S_FULL0 + x), (uint32_t)g & 1u, abort_flag,
+                             p.timeout_ns)))
+          break;
+        tc_fence_after();
+        const int kb = j * BN;
+        const bool masked = kb + BN > t.len || (p.causal && kb + BN - 1 > r0);
+        float h0[HB], h1[HB];
+        load_half(s_t, h0);
+        load_half(s_t + HB, h1);
+        if (masked) {
+          mask_half(h0, kb, 0, lim);
+          mask_half(h1, kb + HB, 0, lim);
+        }
+        uint32_t pk0[HB / 2], pk1[HB / 2];
+        float alpha = 1.f, sum;
+        bool moved = false;
+        if (__any_sync(0xffffffffu, m == -INFINITY)) {
+          // a row without a reference yet (its first visible keys): the
+          // tile's row maximum first
+          const float m_new = fmaxf(m, fmaxf(max_half(h0), max_half(h1)));
+          if (m_new != m) {
+            alpha = (m == -INFINITY) ? 0.f : ex2_approx((m - m_new) * c);
+            m = m_new;
+            l *= alpha;
+            moved = true;
+          }
+          sum = exp_row(h0, h1, c, m, pk0, pk1);
+        } else {
+          sum = exp_row(h0, h1, c, m, pk0, pk1);
+          const bool need = !(sum <= P_SUM_LIMIT);
+          if (__any_sync(0xffffffffu, need)) {
+            // the reference must move: the scores again (S_x is intact
+            // until P is stored), their maximum, the exponentials again
+            load_half(s_t, h0);
+            load_half(s_t + HB, h1);
+            if (masked) {
+              mask_half(h0, kb, 0, lim);
+              mask_half(h1, kb + HB, 0, lim);
+            }
+            if (need) {
+              const float m_new = fmaxf(m, fmaxf(max_half(h0), max_half(h1)));
+              if (m_new != m) {
+                alpha = ex2_approx((m - m_new) * c);
+                m = m_new;
+                l *= alpha;
+                moved = true;
+              }
+            }
+            sum = exp_row(h0, h1, c, m, pk0, pk1);
+          }
+        }
+        // O_x holds P_x(j-1) V_{j-1} (the commit of S_x(j) covers that PV)
+        if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o<D>(o_t, alpha);
+        tmem_st32(s_t, pk0);
+        tmem_st32(s_t + HB / 2, pk1);
+        l += sum;
+        s_ready = j + 1 < nx && mbar_test_wait(ctl.bar(T_S_FULL0 + x), (uint32_t)(g + 1) & 1u);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(ctl.bar(T_P_FULL0 + x));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, LSE; then O_x is free for the next unit
+      ok = wait_warp(ctl.bar(T_PV_DONE0 + x), (uint32_t)(g - 1) & 1u, abort_flag, p.timeout_ns);
+      if (!ok) break;
+      tc_fence_after();
+      const bool live = q_idx < t.len;
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      store_cols<D>(o_t, l > 0.f ? 1.f / l : 0.f,
+                    p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D, live);
+      if (live) p.lse[t.lse_base + q_idx] = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
+      tc_fence_before();
+      warp_arrive(ctl.bar(T_O_FREE0 + x));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace two
+}  // namespace attn

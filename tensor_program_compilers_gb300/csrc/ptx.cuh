@@ -89,6 +89,18 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
 }
 
 // ---------------------------------------------------------------- tcgen05
+// Per-warpgroup register budget (all threads of the warpgroup execute it):
+// dec gives registers back to the CTA's pool, inc waits until the pool has
+// them.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                "r"(ncols)
