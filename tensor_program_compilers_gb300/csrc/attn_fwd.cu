@@ -1,13 +1,15 @@
 // attn_fwd.cu -- fused attention forward for sm_103a (GB300) and its C ABI.
 //
-// A CTA owns one 128-row query tile of one (sequence, query head) and walks
-// the key tiles of that sequence:
+// A CTA works on 128-row query tiles of one (sequence, query head) at a time
+// (one tile, or two in the two-tile kernel) and walks the key tiles of that
+// sequence:
 //
 //   for each 128-key tile j (causal: only j <= the diagonal tile)
 //     S    = Q K_j^T                       tcgen05.mma, bf16 -> fp32 in TMEM
 //     m'   = max(m, rowmax S)              online-softmax monoid state (m, l)
 //     P    = 2^(S*c - m'*c), c = scale*log2(e), rounded to bf16 into TMEM
-//     l    = l * 2^((m - m')*c) + rowsum P      (of the rounded P)
+//     l    = l * 2^((m - m')*c) + rowsum P      (two sums: of the fp32 P for
+//                                               the LSE, of the rounded P for O)
 //     O    = O * 2^((m - m')*c) + P V_j    tcgen05.mma, P read from TMEM
 //   O / l -> bf16, LSE = m*scale + ln(l)
 //
@@ -23,20 +25,25 @@
 //  * masked keys read -inf, the identity of max (tang, section 2.1, guarded
 //    views), so fully masked tiles are skipped rather than computed.
 //
-// Warp roles (224 threads):
-//   warp 0     TMA producer: Q once, then K_0, K_1, V_0, K_2, V_1, ... into a
-//              ring of shared-memory slots (128-byte swizzle)
+// Two kernels share this file's pieces.  attn_fwd2.cuh holds the one used
+// for head dims 64 and 128 without a key window or score modifier: two
+// 128-row query tiles per CTA, one softmax thread per row.  The kernel below
+// serves everything else (d = 256, windows, soft cap, ALiBi, decode, paged
+// caches): one 128-row query tile per CTA.  Its warp roles (352 threads):
+//   warp 0     TMA producer: Q, then K_0, K_1, V_0, K_2, V_1, ... into a ring
+//              of shared-memory slots (128-byte swizzle)
 //   warp 1     TMEM allocator and QK^T issuer (one thread); at d = 256 also
 //              the PV issuer, keeping the order QK_{j+1}, PV_j
-//   warps 2-5  softmax warpgroup: thread t owns query row t (TMEM lane t)
-//   warp 6     PV issuer (one thread), d <= 128
-// Each issuing thread shares its SM sub-partition with a busy softmax warp,
-// so the issue loops keep their instruction counts small.
+//   warps 2-9  softmax: warp w handles the rows of TMEM lane quarter w % 4
+//              and keys 64 h .. 64 h + 63 of each key tile, h = (w - 2) / 4;
+//              the two warps of a lane quarter share one reference maximum
+//   warp 10    PV issuer (one thread), d <= 128
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S     [0, 128)          fp32 scores of the current key tile
 //   P_b   [128 + 64 b, +64) bf16 probabilities (two per column), b < 2
 //   O     [256, 256 + d)    fp32 accumulator
+//   L     [256 + d, +16)    row sums of the rounded P (tensor core), d <= 128
 // QK_{j+1} is issued as soon as the softmax warps have read S_j into
 // registers, so it runs while they compute P_j.
 
@@ -79,11 +86,34 @@ __device__ __forceinline__ void trace_ev(int slot, int role, long long step, int
     g_trace[slot][role][step][ev] = c;
   }
 }
+__device__ __forceinline__ unsigned trace_clock() {
+  unsigned c;
+  asm volatile("mov.u32 %0, %%clock;" : "=r"(c));
+  return c;
+}
+__device__ __forceinline__ void trace_put(int slot, int role, long long step, int ev, unsigned c) {
+  if (slot >= 0 && step >= 0 && step < TRACE_STEPS) g_trace[slot][role][step][ev] = c;
+}
 #define ATTN_TRACE_SLOT() trace_slot()
 #define ATTN_TRACE_EV(role, step, ev) trace_ev(tslot, role, step, ev)
+// stamp now, store later (so that the store does not precede a release)
+#define ATTN_TRACE_CLK(v) ((v) = trace_clock())
+#define ATTN_TRACE_PUT(role, step, ev, v) trace_put(tslot, role, step, ev, v)
+// stamps kept in shared memory (events 0..7 of steps 0..15), copied out at the end
+#define ATTN_TRACE_SM(buf, step, ev) \
+  do { if ((step) < 16) (buf)[(step) * 8 + (ev)] = trace_clock(); } while (0)
+#define ATTN_TRACE_SM_FLUSH(buf, role)                                           \
+  do {                                                                           \
+    for (int s_ = 0; s_ < 16; ++s_)                                              \
+      for (int e_ = 0; e_ < 8; ++e_) trace_put(tslot, role, s_, e_, (buf)[s_ * 8 + e_]); \
+  } while (0)
 #else
 #define ATTN_TRACE_SLOT() (-1)
 #define ATTN_TRACE_EV(role, step, ev) ((void)tslot)
+#define ATTN_TRACE_CLK(v) ((void)(v))
+#define ATTN_TRACE_PUT(role, step, ev, v) ((void)tslot)
+#define ATTN_TRACE_SM(buf, step, ev) ((void)(buf))
+#define ATTN_TRACE_SM_FLUSH(buf, role) ((void)(buf))
 #endif
 
 constexpr int BM = 128;            // query rows per tile (one per TMEM lane)
@@ -218,6 +248,34 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile uint32_t *abort_flag,
                                              unsigned long long timeout_ns) {
   return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, timeout_ns);
+}
+
+// Bounded wait by polling (mbarrier.test_wait in a loop), for barriers that
+// other threads complete with plain arrivals: a thread suspended in try_wait
+// on such a barrier was measured to resume several hundred cycles after the
+// phase completed; a polling thread sees it within one shared-memory round
+// trip.
+__device__ __forceinline__ bool wait_poll_slow(uint32_t bar, uint32_t parity,
+                                            volatile uint32_t *abort_flag,
+                                            unsigned long long timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns || it > (1u << 30)) {
+        *abort_flag = 1u;
+        record_status(ATTN_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity,
+                                          volatile uint32_t *abort_flag,
+                                          unsigned long long timeout_ns) {
+  return mbar_test_wait(bar, parity) || wait_poll_slow(bar, parity, abort_flag, timeout_ns);
 }
 
 // One arrival per warp (count barriers in warps): after every lane's prior

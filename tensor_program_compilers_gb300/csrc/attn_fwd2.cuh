@@ -10,16 +10,20 @@
 // warps share a row; while the softmax warps of one tile work on P, the
 // tensor core runs the other tile's products.  The computation per row is the
 // one attn_fwd.cu describes (online softmax with a lazily moved reference
-// maximum; tang, section 2.3, Table 1 "FlashAttention forward"), with O
-// divided by the exact fp32 row sum.
+// maximum; tang, section 2.3, Table 1 "FlashAttention forward").  O is
+// divided by the sum of the bf16-rounded weights exactly as P.V uses them
+// (so a row whose weight sits on one key returns that key's value), the LSE
+// taken from the sum of the fp32 weights.  The rounded sum is formed after P
+// is handed to the MMA issuer, off the path to it.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of tile A: lane t of warp w owns query row 32 w + t
 //              (TMEM lane 32 w + t)
 //   warps 4-7  softmax of tile B (TMEM lane quarter w % 4)
 //   warp 8     TMA producer: Q_A, Q_B of the unit, then K_0, V_0, K_1, V_1, ...
 //   warp 9     TMEM allocator and MMA issuer (one thread)
-//   warps 10, 11 idle (they complete the third warpgroup)
+//   warps 10, 11 idle (they complete the third warpgroup, which hands part of
+//              its registers to the softmax warpgroups)
 //
 // Tensor memory (512 columns): S_A [0, 128), S_B [128, 256),
 // O_A [256, 256 + d), O_B [256 + d, 256 + 2d).  P_X (bf16 pairs, keys 2c and
@@ -36,7 +40,9 @@ namespace attn {
 namespace two {
 
 constexpr int THREADS2 = 384;   // three warpgroups
-constexpr int WARP_PROD = 8, WARP_MMA = 9;   // warps 10, 11 only complete the third warpgroup
+// Warpgroups 0 and 1: the softmax of tiles A and B; warpgroup 2: producer
+// and MMA issuer (warps 10, 11 only complete it).
+constexpr int SM_WARP0 = 0, WARP_PROD = 8, WARP_MMA = 9;
 // Register split (setmaxnreg): the kernel is built for 168 registers a thread
 // (384 threads; three warps share each SM sub-partition); the third
 // warpgroup gives part of its share to the softmax warpgroups:
@@ -124,10 +130,10 @@ __device__ __forceinline__ bool read_unit(const Ctl2 &c, int k, UnitInfo &t,
   return true;
 }
 
-// p = 2^(h c - m c) for the row's 128 scores (two halves) into pk0, pk1;
-// returns the sum of the fp32 values.
-__device__ __forceinline__ float exp_row(const float (&h0)[HB], const float (&h1)[HB],
-                                         float c, float m, uint32_t (&pk0)[HB / 2],
+// p = 2^(h c - m c) for the row's 128 scores (two halves) into pk0, pk1
+// (bf16 pairs); returns the sum of the fp32 values.
+__device__ __forceinline__ float exp_row(const float (&h0)[HB], const float (&h1)[HB], float c,
+                                         float m, uint32_t (&pk0)[HB / 2],
                                          uint32_t (&pk1)[HB / 2]) {
   const uint64_t c2 = f2_pack(c, c);
   const float nmc = (m == -INFINITY) ? 0.f : -m * c;
@@ -136,6 +142,89 @@ __device__ __forceinline__ float exp_row(const float (&h0)[HB], const float (&h1
   exp_half<false>(h0, c2, nm2, pk0, acc, unused);
   exp_half<false>(h1, c2, nm2, pk1, acc, unused);
   return sum_acc(acc);
+}
+
+// Sum of the row's 128 bf16 weights exactly as P.V uses them.
+__device__ __forceinline__ float sum_rounded(const uint32_t (&pk0)[HB / 2],
+                                             const uint32_t (&pk1)[HB / 2]) {
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int x = 0; x < HB / 2; x += 2) {
+    add_bf16x2_f32(a[0], a[1], pk0[x]);
+    add_bf16x2_f32(a[2], a[3], pk0[x + 1]);
+    add_bf16x2_f32(a[4], a[5], pk1[x]);
+    add_bf16x2_f32(a[6], a[7], pk1[x + 1]);
+  }
+  return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
+// K/V ring slot of position ps: wait until loaded / release after the MMAs
+// issued so far (by this thread) complete.
+template <int STAGES>
+__device__ __forceinline__ bool ring_wait(const Ctl2 &ctl, long long ps,
+                                          volatile uint32_t *abort_flag,
+                                          unsigned long long timeout_ns) {
+  return wait_bounded(ctl.bar(T_RING + (int)(ps % STAGES)), (uint32_t)(ps / STAGES) & 1u,
+                      abort_flag, timeout_ns);
+}
+template <int STAGES>
+__device__ __forceinline__ void ring_release(const Ctl2 &ctl, long long ps) {
+  tc_commit(ctl.bar(T_RING + STAGES + (int)(ps % STAGES)));
+}
+
+struct IssueState {
+  long long npv;   // PV_X issued so far (P_FULL_X phases)
+  int nunits;      // units in which tile X had work (O_FREE_X phases)
+};
+
+// Tile X's share of key step j of a unit: PV_X(j) (O_X (+)= P_X(j) V_j; the
+// unit's first overwrites O_X, after the previous epilogue has read it), then
+// QK_X(j+1).  K_j sits at ring position base + 2j, V_j at base + 2j + 1; the
+// first tile to use a slot waits for it (v_ready, k_ready), the last one
+// releases it (tile B whenever it uses the slot).
+template <int D, int X>
+__device__ __forceinline__ bool pv_then_qk(const Ctl2 &ctl, volatile uint32_t *abort_flag,
+                                           unsigned long long timeout_ns, uint32_t tmem,
+                                           uint64_t kdesc0, uint64_t vdesc0, uint64_t qdesc,
+                                           long long base, int j, int nA, int nB,
+                                           IssueState &st, bool &v_ready, bool &k_ready,
+                                           volatile unsigned *trb) {
+  using C = Cfg2<D>;
+  constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
+  (void)trb;
+  const int nx = X ? nB : nA;
+  if (j >= nx) return true;
+  const long long pv_pos = base + 2 * j + 1, qk_pos = base + 2 * j + 2;
+  if (j == 0 && st.nunits > 0 &&
+      !wait_poll(ctl.bar(T_O_FREE0 + X), (uint32_t)(st.nunits - 1) & 1u, abort_flag, timeout_ns))
+    return false;
+  ATTN_TRACE_SM(trb, st.npv, 6 + X);
+  if (!wait_poll(ctl.bar(T_P_FULL0 + X), (uint32_t)st.npv & 1u, abort_flag, timeout_ns))
+    return false;
+  ATTN_TRACE_SM(trb, st.npv, 3 * X);
+  if (!v_ready && !ring_wait<C::STAGES>(ctl, pv_pos, abort_flag, timeout_ns)) return false;
+  v_ready = true;
+  tc_fence_after();
+  const uint64_t vdesc = desc_add(vdesc0, (uint32_t)(pv_pos % C::STAGES) * C::TILE_BYTES);
+  const uint32_t s_x = tmem + 128u * X;
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_ts(tmem + C::COL_O + (uint32_t)(D * X), s_x + kk * 8, desc_add(vdesc, kk * 2048),
+           IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+  tc_commit(ctl.bar(T_PV_DONE0 + X));
+  ATTN_TRACE_SM(trb, st.npv, 3 * X + 1);
+  ++st.npv;
+  if (X == 1 || j >= nB) ring_release<C::STAGES>(ctl, pv_pos);   // V_j's last use
+  if (j + 1 < nx) {   // QK_X(j+1)
+    if (!k_ready && !ring_wait<C::STAGES>(ctl, qk_pos, abort_flag, timeout_ns)) return false;
+    k_ready = true;
+    tc_fence_after();
+    issue_qk<D>(s_x, qdesc, desc_add(kdesc0, (uint32_t)(qk_pos % C::STAGES) * C::TILE_BYTES));
+    tc_commit(ctl.bar(T_S_FULL0 + X));
+    ATTN_TRACE_SM(trb, st.npv, 3 * X + 2);
+    if (X == 1 || j + 1 >= nB) ring_release<C::STAGES>(ctl, qk_pos);   // K_{j+1}'s last use
+  }
+  return true;
 }
 
 // ================================================================ kernel
@@ -155,12 +244,14 @@ __global__ void __launch_bounds__(THREADS2, 1)
   ctl.bar0 = smem_u32(bars);
   ctl.words = reinterpret_cast<uint32_t *>(bars + T_RING + 2 * C::STAGES);
   ctl.info = reinterpret_cast<int *>(ctl.words + 4);
-  static_assert((T_RING + 2 * C::STAGES) * 8 + 16 + INFO_SLOTS * UNIT_INTS * 4 <= C::CTL_BYTES,
-                "control block");
+  static_assert((T_RING + 2 * C::STAGES) * 8 + 16 + INFO_SLOTS * UNIT_INTS * 4 <= 512 &&
+                    512 + 16 * 8 * 4 <= C::CTL_BYTES,
+                "control block (the last 512 bytes hold trace stamps in trace builds)");
   volatile uint32_t *abort_flag = ctl.words + 1;
   const uint32_t q_s = base_s + C::OFF_Q;
   const uint32_t kv_s = base_s + C::OFF_KV;
   constexpr uint32_t INFO_CONSUMERS = 1 + 8;   // the MMA issuer, the softmax warps
+  const int tslot = ATTN_TRACE_SLOT();          // -1 unless built for tracing
 
   if (warp == WARP_MMA) {
     if (lane == 0) {
@@ -197,7 +288,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.words[0];
 
-  if (warp >= 8) {
+  if (warp < SM_WARP0 || warp >= SM_WARP0 + 8) {
    setmaxnreg_dec<REGS_OTHER>();
    if (warp == WARP_PROD) {
     // ---------------- producer: decode units, publish them, load Q and K/V
@@ -282,10 +373,11 @@ __global__ void __launch_bounds__(THREADS2, 1)
     if (lane == 0) {
       const uint64_t kdesc0 = smem_desc_sw128(kv_s, 16, 1024);
       const uint64_t vdesc0 = smem_desc_sw128(kv_s, CHUNK_BYTES, 1024);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
+      // trace builds: issuer stamps in the spare end of the control block
+      volatile unsigned *trb = reinterpret_cast<volatile unsigned *>(smem + C::OFF_CTL + 512);
+      (void)trb;
       long long base = 0;            // ring position of the unit's first load (K_0)
-      long long npv[2] = {0, 0};     // PV_X issued so far (P_FULL_X phases)
-      int nunits[2] = {0, 0};        // units in which tile X had work (O_FREE_X phases)
+      IssueState st0{0, 0}, st1{0, 0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         UnitInfo t;
@@ -296,83 +388,45 @@ __global__ void __launch_bounds__(THREADS2, 1)
         if (!(ok = wait_bounded(ctl.bar(T_Q_FULL0 + qb), (uint32_t)(k / C::QB) & 1u,
                                 abort_flag, p.timeout_ns)))
           break;
-        const uint64_t qdesc[2] = {smem_desc_sw128(q_s + 2 * qb * C::TILE_BYTES, 16, 1024),
-                                   smem_desc_sw128(q_s + (2 * qb + 1) * C::TILE_BYTES, 16, 1024)};
-        const int n = max(t.n[0], t.n[1]);
-        // K_j at ring position base + 2j, V_j at base + 2j + 1; the first
-        // tile to use a slot waits for it, the last one releases it
-        auto ring_wait = [&](long long ps) -> bool {
-          return wait_bounded(ctl.bar(T_RING + (int)(ps % C::STAGES)),
-                              (uint32_t)(ps / C::STAGES) & 1u, abort_flag, p.timeout_ns);
-        };
-        auto ring_release = [&](long long ps) {
-          tc_commit(ctl.bar(T_RING + C::STAGES + (int)(ps % C::STAGES)));
-        };
-        auto qk = [&](int x, int j) {
-          const long long ps = base + 2 * j;
-          issue_qk<D>(tmem + 128u * (uint32_t)x, qdesc[x],
-                      desc_add(kdesc0, (uint32_t)(ps % C::STAGES) * C::TILE_BYTES));
-          tc_commit(ctl.bar(T_S_FULL0 + x));
-        };
-        if (!(ok = ring_wait(base))) break;
+        const uint64_t qd0 = smem_desc_sw128(q_s + 2 * qb * C::TILE_BYTES, 16, 1024);
+        const uint64_t qd1 = smem_desc_sw128(q_s + (2 * qb + 1) * C::TILE_BYTES, 16, 1024);
+        const int nA = t.n[0], nB = t.n[1];
+        const int n = max(nA, nB);
+        if (!(ok = ring_wait<C::STAGES>(ctl, base, abort_flag, p.timeout_ns))) break;
         tc_fence_after();
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-          if (t.n[x] > 0) qk(x, 0);
-        ring_release(base);
+        const uint64_t kd = desc_add(kdesc0, (uint32_t)(base % C::STAGES) * C::TILE_BYTES);
+        if (nA > 0) {
+          issue_qk<D>(tmem, qd0, kd);
+          tc_commit(ctl.bar(T_S_FULL0));
+        }
+        if (nB > 0) {
+          issue_qk<D>(tmem + 128u, qd1, kd);
+          tc_commit(ctl.bar(T_S_FULL1));
+        }
+        ring_release<C::STAGES>(ctl, base);
         for (int j = 0; ok && j < n; ++j) {
           bool v_ready = false, k_ready = false;
-          const long long pv_pos = base + 2 * j + 1, qk_pos = base + 2 * j + 2;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (j >= t.n[x]) continue;
-            // PV_X(j): O_X (+)= P_X(j) V_j; a unit's first overwrites O_X
-            if (j == 0 && nunits[x] > 0 &&
-                !(ok = wait_bounded(ctl.bar(T_O_FREE0 + x), (uint32_t)(nunits[x] - 1) & 1u,
-                                    abort_flag, p.timeout_ns)))
-              break;
-            if (!(ok = wait_bounded(ctl.bar(T_P_FULL0 + x), (uint32_t)npv[x] & 1u, abort_flag,
-                                    p.timeout_ns)))
-              break;
-            if (!v_ready && !(ok = ring_wait(pv_pos))) break;
-            v_ready = true;
-            tc_fence_after();
-            const uint64_t vdesc =
-                desc_add(vdesc0, (uint32_t)(pv_pos % C::STAGES) * C::TILE_BYTES);
-            const uint32_t s_x = tmem + 128u * (uint32_t)x;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(tmem + C::COL_O + (uint32_t)(D * x), s_x + kk * 8,
-                     desc_add(vdesc, kk * 2048), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(ctl.bar(T_PV_DONE0 + x));
-            ++npv[x];
-            if (x == 1 || j >= t.n[1]) ring_release(pv_pos);   // V_j's last use
-            // QK_X(j+1)
-            if (j + 1 < t.n[x]) {
-              if (!k_ready && !(ok = ring_wait(qk_pos))) break;
-              k_ready = true;
-              tc_fence_after();
-              qk(x, j + 1);
-              if (x == 1 || j + 1 >= t.n[1]) ring_release(qk_pos);   // K_{j+1}'s last use
-            }
-          }
+          ok = pv_then_qk<D, 0>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd0, base, j,
+                                nA, nB, st0, v_ready, k_ready, trb) &&
+               pv_then_qk<D, 1>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd1, base, j,
+                                nA, nB, st1, v_ready, k_ready, trb);
         }
         if (!ok) break;
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-          if (t.n[x] > 0) ++nunits[x];
+        if (nA > 0) ++st0.nunits;
+        if (nB > 0) ++st1.nunits;
         tc_commit(ctl.bar(T_Q_EMPTY0 + qb));   // Q buffer free once its QKs are done
         base += 2 * n;
       }
       tc_commit(ctl.bar(T_DRAIN));   // no MMA may be in flight at teardown
       wait_drain(ctl.bar(T_DRAIN), 0, p.timeout_ns);
+      ATTN_TRACE_SM_FLUSH(trb, 0);
     }
     __syncwarp();
    }
   } else {
     setmaxnreg_inc<REGS_SOFTMAX>();
     // ---------------- softmax warps: tile x = warp / 4, lane quarter warp % 4
-    const int x = warp >> 2;
+    const int x = (warp - SM_WARP0) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -388,18 +442,22 @@ __global__ void __launch_bounds__(THREADS2, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
       if (!t.valid) break;
-      const int nx = t.n[x];
+      const int nx = x ? t.n[1] : t.n[0];
       if (nx == 0) continue;
       const int r0 = UNIT_ROWS * t.unit + BM * x;   // the tile's first row
       const int q_idx = r0 + row;
       const int lim = p.causal ? min(t.len, q_idx + 1) : t.len;   // visible keys [0, lim)
-      float m = -INFINITY, l = 0.f;
+      // reference max (raw score units); row sums of the fp32 weights (for the
+      // LSE) and of the bf16-rounded ones (for O)
+      float m = -INFINITY, l = 0.f, lr = 0.f;
       bool s_ready = false;   // early test of this step's S
       for (int j = 0; j < nx; ++j, ++g) {
         if (!__all_sync(0xffffffffu, s_ready) &&
             !(ok = wait_warp(ctl.bar(T_S_FULL0 + x), (uint32_t)g & 1u, abort_flag,
                              p.timeout_ns)))
           break;
+        unsigned tr_s = 0, tr_e = 0, tr_w = 0;   // trace stamps, stored after the arrival
+        ATTN_TRACE_CLK(tr_s);
         tc_fence_after();
         const int kb = j * BN;
         const bool masked = kb + BN > t.len || (p.causal && kb + BN - 1 > r0);
@@ -413,41 +471,36 @@ __global__ void __launch_bounds__(THREADS2, 1)
         uint32_t pk0[HB / 2], pk1[HB / 2];
         float alpha = 1.f, sum;
         bool moved = false;
-        if (__any_sync(0xffffffffu, m == -INFINITY)) {
-          // a row without a reference yet (its first visible keys): the
-          // tile's row maximum first
-          const float m_new = fmaxf(m, fmaxf(max_half(h0), max_half(h1)));
-          if (m_new != m) {
-            alpha = (m == -INFINITY) ? 0.f : ex2_approx((m - m_new) * c);
-            m = m_new;
-            l *= alpha;
-            moved = true;
+        // A row without a reference yet (its first visible keys) takes the
+        // tile's maximum first; the others exponentiate against their
+        // reference, and only if some row's sum leaves range do the scores
+        // come again (S_x is intact until P is stored) for a second pass with
+        // the maximum.  One copy of the exponential loop serves both passes.
+        bool want = m == -INFINITY, again = false;
+        for (;;) {
+          if (want) {
+            const float m_new = fmaxf(m, fmaxf(max_half(h0), max_half(h1)));
+            if (m_new != m) {
+              alpha = (m == -INFINITY) ? 0.f : ex2_approx((m - m_new) * c);
+              m = m_new;
+              l *= alpha;
+              lr *= alpha;
+              moved = true;
+            }
           }
-          sum = exp_row(h0, h1, c, m, pk0, pk1);
-        } else {
           sum = exp_row(h0, h1, c, m, pk0, pk1);
           const bool need = !(sum <= P_SUM_LIMIT);
-          if (__any_sync(0xffffffffu, need)) {
-            // the reference must move: the scores again (S_x is intact
-            // until P is stored), their maximum, the exponentials again
-            load_half(s_t, h0);
-            load_half(s_t + HB, h1);
-            if (masked) {
-              mask_half(h0, kb, 0, lim);
-              mask_half(h1, kb + HB, 0, lim);
-            }
-            if (need) {
-              const float m_new = fmaxf(m, fmaxf(max_half(h0), max_half(h1)));
-              if (m_new != m) {
-                alpha = ex2_approx((m - m_new) * c);
-                m = m_new;
-                l *= alpha;
-                moved = true;
-              }
-            }
-            sum = exp_row(h0, h1, c, m, pk0, pk1);
+          if (again || !__any_sync(0xffffffffu, need)) break;
+          again = true;
+          want = need;
+          load_half(s_t, h0);
+          load_half(s_t + HB, h1);
+          if (masked) {
+            mask_half(h0, kb, 0, lim);
+            mask_half(h1, kb + HB, 0, lim);
           }
         }
+        ATTN_TRACE_CLK(tr_e);
         // O_x holds P_x(j-1) V_{j-1} (the commit of S_x(j) covers that PV)
         if (j > 0 && __any_sync(0xffffffffu, moved)) rescale_o<D>(o_t, alpha);
         tmem_st32(s_t, pk0);
@@ -455,8 +508,17 @@ __global__ void __launch_bounds__(THREADS2, 1)
         l += sum;
         s_ready = j + 1 < nx && mbar_test_wait(ctl.bar(T_S_FULL0 + x), (uint32_t)(g + 1) & 1u);
         tmem_wait_st();
+        ATTN_TRACE_CLK(tr_w);
         tc_fence_before();
         warp_arrive(ctl.bar(T_P_FULL0 + x));
+        // the rounded sum, off the path to P: the warp would wait for S now
+        lr += sum_rounded(pk0, pk1);
+        if (lane == 0) {
+          ATTN_TRACE_EV(2 + warp - SM_WARP0, g, 2);
+          ATTN_TRACE_PUT(2 + warp - SM_WARP0, g, 0, tr_s);
+          ATTN_TRACE_PUT(2 + warp - SM_WARP0, g, 1, tr_e);
+          ATTN_TRACE_PUT(2 + warp - SM_WARP0, g, 3, tr_w);
+        }
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE; then O_x is free for the next unit
@@ -465,7 +527,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
       tc_fence_after();
       const bool live = q_idx < t.len;
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      store_cols<D>(o_t, l > 0.f ? 1.f / l : 0.f,
+      store_cols<D>(o_t, lr > 0.f ? 1.f / lr : 0.f,
                     p.o + ((long long)(t.seq_start + q_idx) * p.Hq + t.h) * (long long)D, live);
       if (live) p.lse[t.lse_base + q_idx] = l > 0.f ? m_use * p.scale + logf(l) : -INFINITY;
       tc_fence_before();

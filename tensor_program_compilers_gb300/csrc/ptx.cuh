@@ -291,6 +291,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 // The two bf16 halves of a packed pair widened to fp32, as a packed fp32 pair.
+// a0 += low bf16 of w, a1 += high bf16 of w (mixed-precision adds: the bf16
+// operand widens exactly, one rounding per add).  Volatile: callers place
+// these after a barrier arrival on purpose, off the path to it.
+__device__ __forceinline__ void add_bf16x2_f32(float &a0, float &a1, uint32_t w) {
+  asm volatile(
+      "{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint64_t bf16x2_widen(uint32_t v) {
   return ((uint64_t)(v & 0xFFFF0000u) << 32) | (uint64_t)(v << 16);
 }
