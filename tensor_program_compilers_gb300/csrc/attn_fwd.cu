@@ -1648,10 +1648,14 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
 }
 
 namespace attn {
-// Key splits of a decode launch: about two units per SM, whole key tiles.
+// Key splits of a decode launch: at most one unit per SM, whole key tiles.
 static void decode_splits(int B, int Hkv, int Nk, int sms, int &splits, int &chunk) {
+  // At most one round of units: as many splits as keep every (sequence, kv
+  // head) on whole SMs.  Measured (B 16, Hkv 8, Nk 8192 on 152 SMs): one
+  // split 5.33 TB/s, two 4.84, three 4.77 -- the merge pass and the second
+  // round's tail cost more than the idle SMs of a single round.
   const long long per = (long long)B * Hkv;
-  long long want = (2LL * sms + per - 1) / per;
+  long long want = sms / per;
   const int tiles = (Nk + BN - 1) / BN;
   if (want > tiles) want = tiles;
   if (want < 1) want = 1;

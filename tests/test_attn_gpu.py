@@ -328,14 +328,16 @@ def test_workload_ragged_sampled():
     print(_workload_check(W.RAGGED, rows_per_head=64))
 
 
-@pytest.mark.parametrize("key", ["ragged", "gqa"])
+@pytest.mark.parametrize("key", ["ragged", "gqa", "d256"])
 def test_workload_every_row_fp32(key):
-    """Every output row of the two large d = 128 workloads, against the same
-    definition computed in fp32 with PyTorch on the GPU (cuBLAS products, TF32
-    off; its own error, ~1e-6, is far below the tolerance).  The fp64 oracle
-    checks sampled rows; the worst rows of the peaked ragged batch are rare
-    (a sample of 2,048 of its 2.7 M rows can miss them), so this checks all."""
+    """Every output row of the large workloads (d256: of its first four heads),
+    against the same definition computed in fp32 with PyTorch on the GPU
+    (cuBLAS products, TF32 off; its own error, ~1e-6, is far below the
+    tolerance).  The fp64 oracle checks sampled rows; the worst rows of the
+    peaked ragged batch are rare (a sample of 2,048 of its 2.7 M rows can miss
+    them), so this checks all."""
     wl = W.BY_KEY[key]
+    heads = range(4) if key == "d256" else range(wl.Hq)
     inp = W.make_inputs(wl)
     r = Run(inp.q, inp.k, inp.v, wl.B, wl.Hq, wl.Hkv, inp.n_arg, wl.d, wl.scale, wl.causal,
             cu=None if inp.cu_seqlens is None else inp.cu_seqlens.numpy())
@@ -351,7 +353,7 @@ def test_workload_every_row_fp32(key):
     a = 0
     for L in lens:
         mask = torch.ones(L, L, dtype=torch.bool, device=q.device).triu(1)
-        for h in range(wl.Hq):
+        for h in heads:
             s = (q[a:a + L, h].float() @ k[a:a + L, h // g].float().T) * wl.scale
             if wl.causal:
                 s = s.masked_fill(mask, float("-inf"))
