@@ -237,6 +237,49 @@ def run_workload(pkg, W, wl, seed, steps, warmup, dev, flush, sample_clocks=Fals
                 tensors=(q, k, v, o, lse, cu), step=step)
 
 
+# One exp2 per visible score; MUFU ex2 issues 32 lanes per clock per SM
+# (measured on this GPU with a dependent-free ex2 loop), at the 2.07 GHz
+# maximum SM clock on 152 SMs.
+MUFU_EX2_PER_S = 32 * 152 * 2.07e9
+
+
+def launch_floor_us(dev, flush):
+    """CUDA-event time of the smallest kernel launch (a one-element fill),
+    the floor under any launch of the short workloads.  Timed as the
+    workloads are: behind the L2 flush, so that the launch is queued before
+    the GPU reaches it and host overhead stays out of the interval."""
+    import torch
+    x = torch.empty(1, device=dev)
+    for _ in range(10):
+        x.zero_()
+    ts = []
+    for _ in range(30):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        a.record()
+        x.zero_()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return round(statistics.median(ts), 2)
+
+
+def secondary_rooflines(wl, rr, ms, hbm_gbs, floor_us):
+    """The bounds that matter for the short workloads: the minimum HBM bytes
+    (Q, K, V read once, O and LSE written once) against the copy bandwidth,
+    the exponentials (one per visible score, FLOPs / 4d) against the MUFU
+    rate, and the time against the launch floor."""
+    inp = rr["inp"]
+    rows = inp.total_rows
+    nbytes = rows * (2 * wl.Hq + 2 * wl.Hkv) * wl.d * 2 + rows * wl.Hq * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    ex2 = rr["flops"] / (4 * wl.d) / (ms / 1e3)
+    return {"us": round(ms * 1e3, 2), "launch_floor_us": floor_us, "min_bytes": nbytes,
+            "hbm_gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
+            "exp2_per_s": float(f"{ex2:.4g}"), "frac_of_mufu": round(ex2 / MUFU_EX2_PER_S, 4)}
+
+
 def time_steps(step, steps, warmup, flush, stream):
     """CUDA-event times (ms) of `steps` calls of step(), L2 flushed before each."""
     import torch
@@ -488,6 +531,7 @@ def native(args):
 
     per_workload = {}
     if not args.no_per_workload:
+        floor_us = launch_floor_us(dev, flush)
         for key, other in W.BY_KEY.items():
             if key == args.workload:
                 continue
@@ -495,7 +539,9 @@ def native(args):
             ms = rr["total_ms"] / len(rr["per_ms"])
             tf = rr["flops"] / (ms / 1e3) / 1e12
             per_workload[key] = {"workload": other.name, "tflops": round(tf, 2),
-                                 "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peak, 4)}
+                                 "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peak, 4),
+                                 **secondary_rooflines(other, rr, ms, peaks.get("hbm_gbs"),
+                                                       floor_us)}
             del rr
         per_workload["window"] = run_window(pkg, dev, flush, min(args.steps, 20))
         per_workload["decode"] = run_decode(pkg, dev, flush, min(args.steps, 20),

@@ -82,16 +82,31 @@ __device__ __forceinline__ int seq_of_padded_row(const BwdParams &p, int r) {
 }
 
 // A work unit of the dK/dV kernel (kv head, key block) or of the dQ kernel
-// (query head, query block): unit u covers padded block u % nb_max of head
-// u / nb_max; blocks past the last sequence do nothing.
+// (query head, query block).  Heads run fastest, and the blocks come longest
+// first so that the last CTAs the hardware schedules are the short ones:
+// causal key blocks of the dK/dV kernel see fewer query blocks the later they
+// sit in their sequence (ascending block order), query blocks of the dQ
+// kernel see more (desc: descending).  Fixed batches order blocks by their
+// index within the sequence across all sequences; packed batches by their
+// place in the padded row space.  Blocks past the last sequence do nothing.
 struct BUnit {
   bool valid;
   int head, seq, blk, start, len, nblk;
 };
-__device__ __forceinline__ BUnit bwd_unit(const BwdParams &p, int u) {
+__device__ __forceinline__ BUnit bwd_unit(const BwdParams &p, int u, int heads, bool desc) {
   BUnit t{};
-  t.head = u / p.nb_max;
-  const int r = (u % p.nb_max) * BM;
+  t.head = u % heads;
+  const int v = u / heads;   // the block's rank in the order above
+  int r;                     // padded row of the block's first row
+  if (!p.cu) {
+    const int nb = (p.N + BM - 1) / BM;
+    if (v >= nb * p.B) return t;
+    const int blk = v / p.B;
+    r = p.pstart[v % p.B] + (desc ? nb - 1 - blk : blk) * BM;
+  } else {
+    if (v >= p.nb_max) return t;
+    r = (desc ? p.nb_max - 1 - v : v) * BM;
+  }
   if (r >= p.pstart[p.B]) return t;
   t.seq = seq_of_padded_row(p, r);
   t.blk = (r - p.pstart[t.seq]) / BM;
@@ -289,7 +304,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::A_OFF_CTL + 8 * B_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const BUnit un = bwd_unit(p, blockIdx.x);
+  const BUnit un = bwd_unit(p, blockIdx.x, p.Hkv, false);
   if (!un.valid) return;   // uniform over the CTA, before any set-up
   const int jb = un.blk, kvh = un.head, b = un.seq;
   const int nblk = un.nblk, row0 = un.start, len = un.len;
@@ -484,7 +499,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::B_OFF_CTL + 8 * B_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const BUnit un = bwd_unit(p, blockIdx.x);
+  const BUnit un = bwd_unit(p, blockIdx.x, p.Hq, p.causal != 0);
   if (!un.valid) return;   // uniform over the CTA, before any set-up
   const int ib = un.blk, h = un.head, b = un.seq;
   const int row0 = un.start, len = un.len;
