@@ -18,7 +18,9 @@
 // Both recompute the scores, so no partial sums cross CTAs.  Per step the
 // softmax warps turn the fp32 tiles into bf16 P^T / dS^T (dS) written over
 // the scores they came from; the MMAs that follow read them from tensor
-// memory.  Fixed and packed batches, d = 64 or 128.
+// memory.  The softmax works in two phases (P, then dS), and the next step's
+// score product is issued between them, so it runs while dS is formed.
+// Fixed and packed batches, d = 64 or 128.
 
 namespace attn {
 namespace bwd {
@@ -148,12 +150,12 @@ enum : int {
   B_FULL1,
   B_EMPTY0,            // ring slot s consumed (MMA commit)
   B_EMPTY1,
-  B_S_FULL0,           // column half h of the step's two score-shaped products is
-  B_S_FULL1,           //   in TMEM, h < 2
-  B_P_FULL0,           // the 4 softmax warps of column half h wrote P / dS
-  B_P_FULL1,
   B_DONE,              // the accumulators are final
   B_DRAIN,             // abort drain of the MMA issuer
+  B_ST_FULL,           // the step's S^T (dK/dV kernel) or S (dQ kernel) in TMEM
+  B_DPT_FULL,          // the step's dP^T or dP in TMEM
+  B_PT_FULL,           // all softmax warps: P^T written over S^T (dK/dV), or S read (dQ)
+  B_DST_FULL,          // all softmax warps: dS^T (dS) written over dP^T (dP)
   B_COUNT
 };
 
@@ -203,30 +205,14 @@ __device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
     mbar_init(c.bar(B_FULL0 + s), 1);
     mbar_init(c.bar(B_EMPTY0 + s), 1);
   }
-  for (int h = 0; h < 2; ++h) {
-    mbar_init(c.bar(B_S_FULL0 + h), 1);
-    mbar_init(c.bar(B_P_FULL0 + h), BWD_SM_WARPS / 2);
-  }
   mbar_init(c.bar(B_DONE), 1);
   mbar_init(c.bar(B_DRAIN), 1);
+  mbar_init(c.bar(B_ST_FULL), 1);
+  mbar_init(c.bar(B_DPT_FULL), 1);
+  mbar_init(c.bar(B_PT_FULL), BWD_SM_WARPS);
+  mbar_init(c.bar(B_DST_FULL), BWD_SM_WARPS);
   c.words[1] = 0u;
   mbar_init_fence();
-}
-
-// Column half h of a score-shaped product: A (128 rows, K-major) times rows
-// 64 h .. 64 h + 63 of B (K-major; 64 rows = 8 KB into each swizzle chunk),
-// N = 64, into TMEM columns d_tmem + 64 h.  Each half is committed on its
-// own so that the softmax warps of half 0 start while half 1 is computed.
-template <int D>
-__device__ __forceinline__ void issue_half_s(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             int h) {
-  constexpr uint32_t IDESC = idesc_bf16_f32(64, 0);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t koff = (kk >> 2) * CHUNK_BYTES + (kk & 3) * 32;
-    mma_ss(d_tmem + 64u * (uint32_t)h, desc_add(adesc, koff),
-           desc_add(bdesc, koff + (uint32_t)h * 64u * 128u), IDESC, kk > 0 ? 1u : 0u);
-  }
 }
 
 // K-half h of A (bf16 pairs in TMEM at a_tmem + 64 h: each softmax warp
@@ -242,22 +228,6 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
     mma_ts(d_tmem, a_tmem + 64u * (uint32_t)h + 8u * (uint32_t)kk,
            desc_add(bdesc, (4 * h + kk) * 2048), IDESC,
            (accumulate || h > 0 || kk > 0) ? 1u : 0u);
-}
-
-// 32 columns of a softmax-warp row from two fp32 tiles in TMEM.
-__device__ __forceinline__ void ld_pair32(uint32_t ta, uint32_t tb, float (&a)[32],
-                                          float (&b)[32]) {
-  uint32_t ua[32], ub[32];
-  tmem_ld32(ta, ua);
-  tmem_ld32(tb, ub);
-  tmem_wait_ld();
-  reg_fence32(ua);
-  reg_fence32(ub);
-#pragma unroll
-  for (int x = 0; x < 32; ++x) {
-    a[x] = __uint_as_float(ua[x]);
-    b[x] = __uint_as_float(ub[x]);
-  }
 }
 
 // Epilogue of one accumulator row: NCOLS fp32 columns * mul -> bf16, 16-byte
@@ -375,38 +345,50 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
       const uint64_t vdesc = smem_desc_sw128(v_s, 16, 1024);
       bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      // Per step s: S^T(s) and dP^T(s) in full; dV += P^T(s) dO once the
+      // softmax warps have written P^T; then S^T(s+1) (S^T's columns are
+      // free once dV(s) has read P^T: one thread's MMAs run in issue order)
+      // while the softmax warps form dS^T(s); dK += dS^T(s) Q; then
+      // dP^T(s+1).  So the next scores are computed while dS is formed.
+      const uint32_t ring = base + C::A_OFF_RING;
+      if (ok && steps > 0 &&
+          (ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+        tc_fence_after();
+        issue_qk<D>(tmem + COL_ST, kdesc, smem_desc_sw128(ring, 16, 1024));
+        tc_commit(ctl.bar(B_ST_FULL));
+        issue_qk<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(ring + C::TILE, 16, 1024));
+        tc_commit(ctl.bar(B_DPT_FULL));
+      }
       for (int s = 0; ok && s < steps; ++s) {
         const int slot = s & 1;
-        if (!(ok = wait_bounded(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
-                                p.timeout_ns)))
-          break;
-        tc_fence_after();
-        const uint32_t q_s = base + C::A_OFF_RING + slot * C::A_SLOT;
-        const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
-        const uint64_t dodesc = smem_desc_sw128(q_s + C::TILE, 16, 1024);
-        // S^T = K Q^T and dP^T = V dO^T, by query halves (the previous
-        // step's dV, dK products, issued earlier by this thread, have read
-        // P^T, dS^T before these overwrite them: one thread's MMAs run in
-        // issue order)
-        for (int h = 0; h < 2; ++h) {
-          issue_half_s<D>(tmem + COL_ST, kdesc, qdesc, h);
-          issue_half_s<D>(tmem + COL_DPT, vdesc, dodesc, h);
-          tc_commit(ctl.bar(B_S_FULL0 + h));
-        }
-        // dV += P^T dO, dK += dS^T Q (dO, Q as N-major B operands), by
-        // query halves as their softmax warps finish
+        const uint32_t q_s = ring + slot * C::A_SLOT;
+        const uint32_t q_n = ring + (slot ^ 1) * C::A_SLOT;   // the next step's slot
         const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
         const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = wait_bounded(ctl.bar(B_P_FULL0 + h), (uint32_t)s & 1u, abort_flag,
-                                  p.timeout_ns)))
+        if (!(ok = wait_bounded(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
+        issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
+        const bool more = s + 1 < steps;
+        if (more) {
+          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
+                                  abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, h, s > 0);
-          issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, h, s > 0);
+          issue_qk<D>(tmem + COL_ST, kdesc, smem_desc_sw128(q_n, 16, 1024));
+          tc_commit(ctl.bar(B_ST_FULL));
         }
-        if (!ok) break;
-        tc_commit(ctl.bar(B_EMPTY0 + slot));
+        if (!(ok = wait_bounded(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, s > 0);
+        issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 1, s > 0);
+        tc_commit(ctl.bar(B_EMPTY0 + slot));   // Q(s), dO(s) and their rows are read
+        if (more) {
+          issue_qk<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(q_n + C::TILE, 16, 1024));
+          tc_commit(ctl.bar(B_DPT_FULL));
+        }
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
       tc_commit(ctl.bar(B_DRAIN));
@@ -425,8 +407,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
       const int slot = s & 1;
-      if (!(ok = wait_warp(ctl.bar(B_S_FULL0 + hf), (uint32_t)s & 1u, abort_flag,
-                           p.timeout_ns)) ||
+      if (!(ok = wait_warp(ctl.bar(B_ST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)) ||
           !(ok = wait_warp(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
                            p.timeout_ns)))
         break;
@@ -436,32 +417,58 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           reinterpret_cast<const float *>(smem + C::A_OFF_RING + slot * C::A_SLOT + 2 * C::TILE);
       const float *dsum = lse2 + 128;
       const bool diag = p.causal && ib == jb;
-#pragma unroll 1
+      // phase 1: P^T = 2^(S^T c - LSE2) for this warp's 64 query columns,
+      // bf16 over the first 32 of them; the bf16 P stays in registers for
+      // phase 2 (dS uses P as the dV product does)
+      uint32_t pw[2][16];
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * hf + 32 * ch;
-        float sv[32], dp[32];
-        ld_pair32(tmem + lane_off + COL_ST + c0, tmem + lane_off + COL_DPT + c0, sv, dp);
-        uint32_t pw[16], dw[16];
+        uint32_t us[32];
+        tmem_ld32(tmem + lane_off + COL_ST + c0, us);
+        tmem_wait_ld();
+        reg_fence32(us);
 #pragma unroll
         for (int x = 0; x < 32; x += 2) {
           const int qc = c0 + x;
-          float p0 = ex2_approx(sv[x] * c - lse2[qc]);
-          float p1 = ex2_approx(sv[x + 1] * c - lse2[qc + 1]);
+          float p0 = ex2_approx(__uint_as_float(us[x]) * c - lse2[qc]);
+          float p1 = ex2_approx(__uint_as_float(us[x + 1]) * c - lse2[qc + 1]);
           if (diag) {   // query ib*128 + qc sees key iff query >= key
             if (ib * BM + qc < key) p0 = 0.f;
             if (ib * BM + qc + 1 < key) p1 = 0.f;
           }
-          pw[x >> 1] = pack_bf16x2(p0, p1);
-          dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum[qc]), p1 * (dp[x + 1] - dsum[qc + 1]));
+          pw[ch][x >> 1] = pack_bf16x2(p0, p1);
         }
-        // bf16 P^T and dS^T over scores this warp has already read (the
-        // first 32 of its 64 columns)
-        tmem_st16(tmem + lane_off + COL_ST + 64 * hf + 16 * ch, pw);
+        tmem_st16(tmem + lane_off + COL_ST + 64 * hf + 16 * ch, pw[ch]);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(ctl.bar(B_PT_FULL));
+      // phase 2: dS^T = P^T o (dP^T - D), bf16 over the first 32 columns
+      if (!(ok = wait_warp(ctl.bar(B_DPT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * hf + 32 * ch;
+        uint32_t ud[32];
+        tmem_ld32(tmem + lane_off + COL_DPT + c0, ud);
+        tmem_wait_ld();
+        reg_fence32(ud);
+        uint32_t dw[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const int qc = c0 + x;
+          const uint32_t w = pw[ch][x >> 1];
+          dw[x >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (__uint_as_float(ud[x]) - dsum[qc]),
+                                   __uint_as_float(w & 0xFFFF0000u) *
+                                       (__uint_as_float(ud[x + 1]) - dsum[qc + 1]));
+        }
         tmem_st16(tmem + lane_off + COL_DPT + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(ctl.bar(B_P_FULL0 + hf));
+      warp_arrive(ctl.bar(B_DST_FULL));
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
@@ -564,31 +571,45 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
       const uint64_t dodesc = smem_desc_sw128(do_s, 16, 1024);
       bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      // Per step s: S(s) and dP(s) in full; S(s+1) as soon as the softmax
+      // warps have read S(s) (P is no operand here); dQ += dS(s) K once they
+      // have written dS over dP(s); then dP(s+1) (dP's columns are free once
+      // dQ(s) has read dS: one thread's MMAs run in issue order).
+      const uint32_t ring = base + C::B_OFF_RING;
+      if (ok && steps > 0 &&
+          (ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+        tc_fence_after();
+        issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(ring, 16, 1024));
+        tc_commit(ctl.bar(B_ST_FULL));
+        issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(ring + C::TILE, 16, 1024));
+        tc_commit(ctl.bar(B_DPT_FULL));
+      }
       for (int s = 0; ok && s < steps; ++s) {
         const int slot = s & 1;
-        if (!(ok = wait_bounded(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
-                                p.timeout_ns)))
+        const uint32_t k_s = ring + slot * C::B_SLOT;
+        const uint32_t k_n = ring + (slot ^ 1) * C::B_SLOT;   // the next step's slot
+        const bool more = s + 1 < steps;
+        if (!(ok = wait_bounded(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
-        tc_fence_after();
-        const uint32_t k_s = base + C::B_OFF_RING + slot * C::B_SLOT;
-        const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
-        const uint64_t vdesc = smem_desc_sw128(k_s + C::TILE, 16, 1024);
-        for (int h = 0; h < 2; ++h) {   // S = Q K^T, dP = dO V^T, by key halves
-          issue_half_s<D>(tmem + COL_S, qdesc, kdesc, h);
-          issue_half_s<D>(tmem + COL_DP, dodesc, vdesc, h);
-          tc_commit(ctl.bar(B_S_FULL0 + h));
-        }
-        // dQ += dS K (K as the N-major B operand), by key halves
-        const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = wait_bounded(ctl.bar(B_P_FULL0 + h), (uint32_t)s & 1u, abort_flag,
-                                  p.timeout_ns)))
+        if (more) {
+          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
+                                  abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, h, s > 0);
+          issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(k_n, 16, 1024));
+          tc_commit(ctl.bar(B_ST_FULL));
         }
-        if (!ok) break;
-        tc_commit(ctl.bar(B_EMPTY0 + slot));
+        if (!(ok = wait_bounded(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
+        issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 0, s > 0);
+        issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 1, s > 0);
+        tc_commit(ctl.bar(B_EMPTY0 + slot));   // K(s), V(s) are read
+        if (more) {
+          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(k_n + C::TILE, 16, 1024));
+          tc_commit(ctl.bar(B_DPT_FULL));
+        }
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
       tc_commit(ctl.bar(B_DRAIN));
@@ -608,32 +629,57 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const float dsum = p.dsum[prow];
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
-      if (!(ok = wait_warp(ctl.bar(B_S_FULL0 + hf), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+      if (!(ok = wait_warp(ctl.bar(B_ST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
         break;
       tc_fence_after();
       const bool edge = (s * BM + BM > len) || (p.causal && s == ib);
-#pragma unroll 1
+      // phase 1: this warp's 64 scores into registers, S released at once
+      // (the next S is computed while P and dS are formed), then P
+      float pv[64];
+      {
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + lane_off + COL_S + 64 * hf, u0);
+        tmem_ld32(tmem + lane_off + COL_S + 64 * hf + 32, u1);
+        tmem_wait_ld();
+        reg_fence32(u0);
+        reg_fence32(u1);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          pv[x] = __uint_as_float(u0[x]);
+          pv[32 + x] = __uint_as_float(u1[x]);
+        }
+      }
+      tc_fence_before();
+      warp_arrive(ctl.bar(B_PT_FULL));
+#pragma unroll
+      for (int x = 0; x < 64; ++x) {
+        const int k0 = s * BM + 64 * hf + x;
+        float pe = ex2_approx(pv[x] * c - lse2);
+        if (edge && (k0 >= len || (p.causal && k0 > qrow)))   // past the sequence, or causal
+          pe = 0.f;
+        pv[x] = pe;
+      }
+      // phase 2: dS = P o (dP - D), bf16 over the first 32 of the 64 columns
+      if (!(ok = wait_warp(ctl.bar(B_DPT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        break;
+      tc_fence_after();
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * hf + 32 * ch;
-        float sv[32], dp[32];
-        ld_pair32(tmem + lane_off + COL_S + c0, tmem + lane_off + COL_DP + c0, sv, dp);
+        uint32_t ud[32];
+        tmem_ld32(tmem + lane_off + COL_DP + c0, ud);
+        tmem_wait_ld();
+        reg_fence32(ud);
         uint32_t dw[16];
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int k0 = s * BM + c0 + x;
-          float p0 = ex2_approx(sv[x] * c - lse2);
-          float p1 = ex2_approx(sv[x + 1] * c - lse2);
-          if (edge) {   // keys past the sequence, or after the query (causal)
-            if (k0 >= len || (p.causal && k0 > qrow)) p0 = 0.f;
-            if (k0 + 1 >= len || (p.causal && k0 + 1 > qrow)) p1 = 0.f;
-          }
-          dw[x >> 1] = pack_bf16x2(p0 * (dp[x] - dsum), p1 * (dp[x + 1] - dsum));
-        }
+        for (int x = 0; x < 32; x += 2)
+          dw[x >> 1] = pack_bf16x2(pv[32 * ch + x] * (__uint_as_float(ud[x]) - dsum),
+                                   pv[32 * ch + x + 1] * (__uint_as_float(ud[x + 1]) - dsum));
         tmem_st16(tmem + lane_off + COL_DP + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(ctl.bar(B_P_FULL0 + hf));
+      warp_arrive(ctl.bar(B_DST_FULL));
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
