@@ -160,35 +160,47 @@ enum : int {
 };
 
 // ------------------------------------------------------------------ row pass
-// One warp per (head, padded row): D = sum_c dO o O, LSE log2(e); padding
-// rows of a sequence get D = 0 and +inf, which zeroes their P in the kernels.
+// Eight lanes per (head, padded row), 16-byte loads: D = sum_c dO o O and
+// LSE log2(e); padding rows of a sequence get D = 0 and +inf, which zeroes
+// their P in the kernels.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // h rows_pad + r
-  if (row >= (long long)p.Hq * p.rows_pad()) return;
-  const int h = (int)(row / p.rows_pad());
-  const int r = (int)(row % p.rows_pad());
-  if (r >= p.pstart[p.B]) return;
-  const int b = seq_of_padded_row(p, r);
+  const int lane = threadIdx.x & 31, seg = lane & 7;
+  const long long row = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);   // h rows_pad + r
+  bool live = row < (long long)p.Hq * p.rows_pad();
+  const int h = live ? (int)(row / p.rows_pad()) : 0;
+  const int r = live ? (int)(row % p.rows_pad()) : 0;
+  live = live && r < p.pstart[p.B];
+  const int b = live ? seq_of_padded_row(p, r) : 0;
   const int i = r - p.pstart[b];
-  if (i >= p.seq_len(b)) {
-    if (lane == 0) {
+  const bool pad = live && i >= p.seq_len(b);
+  live = live && !pad;
+  constexpr int PER = D / 8;   // elements per lane: PER / 8 loads of 16 bytes
+  float acc = 0.f;
+  if (live) {
+    const long long off = ((long long)(p.seq_start(b) + i) * p.Hq + h) * D + seg * PER;
+    const uint4 *po = reinterpret_cast<const uint4 *>(p.o + off);
+    const uint4 *pd = reinterpret_cast<const uint4 *>(p.dout + off);
+#pragma unroll
+    for (int x = 0; x < PER / 8; ++x) {
+      const uint4 a = __ldg(po + x), c = __ldg(pd + x);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        acc += __uint_as_float(wa[y] << 16) * __uint_as_float(wc[y] << 16);
+        acc += __uint_as_float(wa[y] & 0xFFFF0000u) * __uint_as_float(wc[y] & 0xFFFF0000u);
+      }
+    }
+  }
+  for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (seg == 0) {
+    if (pad) {
       p.lse2[row] = INFINITY;
       p.dsum[row] = 0.f;
+    } else if (live) {
+      p.dsum[row] = acc;
+      p.lse2[row] = p.lse[p.lse_index(b, h, i)] * 1.4426950408889634f;
     }
-    return;
-  }
-  constexpr int PER = D / 32;
-  const long long off = ((long long)(p.seq_start(b) + i) * p.Hq + h) * D + lane * PER;
-  float acc = 0.f;
-#pragma unroll
-  for (int x = 0; x < PER; ++x)
-    acc += __bfloat162float(p.o[off + x]) * __bfloat162float(p.dout[off + x]);
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    p.dsum[row] = acc;
-    p.lse2[row] = p.lse[p.lse_index(b, h, i)] * 1.4426950408889634f;
   }
 }
 
@@ -788,7 +800,7 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
 
-  const unsigned row_blocks = (unsigned)(((long long)Hq * nb_max * BM + 7) / 8);
+  const unsigned row_blocks = (unsigned)(((long long)Hq * nb_max * BM + 31) / 32);
   const unsigned kv_units = (unsigned)((long long)Hkv * nb_max);
   const unsigned q_units = (unsigned)((long long)Hq * nb_max);
   bwd_setup_kernel<<<1, 32, 0, stream>>>(p);
