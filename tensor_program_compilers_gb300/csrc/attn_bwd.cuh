@@ -440,16 +440,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tmem_ld32(tmem + lane_off + COL_ST + c0, us);
         tmem_wait_ld();
         reg_fence32(us);
+        // the mask test is taken out of the loop (only the diagonal block
+        // needs it; inside the loop it cost more than the exponentials)
+        if (!diag) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int qc = c0 + x;
-          float p0 = ex2_approx(__uint_as_float(us[x]) * c - lse2[qc]);
-          float p1 = ex2_approx(__uint_as_float(us[x + 1]) * c - lse2[qc + 1]);
-          if (diag) {   // query ib*128 + qc sees key iff query >= key
+          for (int x = 0; x < 32; x += 4) {
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c0 + x);
+            pw[ch][x >> 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x]) * c - l4.x),
+                                         ex2_approx(__uint_as_float(us[x + 1]) * c - l4.y));
+            pw[ch][(x >> 1) + 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x + 2]) * c - l4.z),
+                                               ex2_approx(__uint_as_float(us[x + 3]) * c - l4.w));
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const int qc = c0 + x;
+            float p0 = ex2_approx(__uint_as_float(us[x]) * c - lse2[qc]);
+            float p1 = ex2_approx(__uint_as_float(us[x + 1]) * c - lse2[qc + 1]);
+            // query ib*128 + qc sees key iff query >= key
             if (ib * BM + qc < key) p0 = 0.f;
             if (ib * BM + qc + 1 < key) p1 = 0.f;
+            pw[ch][x >> 1] = pack_bf16x2(p0, p1);
           }
-          pw[ch][x >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tmem + lane_off + COL_ST + 64 * hf + 16 * ch, pw[ch]);
       }
@@ -469,12 +481,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         reg_fence32(ud);
         uint32_t dw[16];
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const int qc = c0 + x;
-          const uint32_t w = pw[ch][x >> 1];
-          dw[x >> 1] = pack_bf16x2(__uint_as_float(w << 16) * (__uint_as_float(ud[x]) - dsum[qc]),
-                                   __uint_as_float(w & 0xFFFF0000u) *
-                                       (__uint_as_float(ud[x + 1]) - dsum[qc + 1]));
+        for (int x = 0; x < 32; x += 4) {
+          const float4 d4 = *reinterpret_cast<const float4 *>(dsum + c0 + x);
+          const uint32_t w0 = pw[ch][x >> 1], w1 = pw[ch][(x >> 1) + 1];
+          float a0, a1, a2, a3;
+          f2_unpack(f2_mul(bf16x2_widen(w0),
+                           f2_add(f2_pack(__uint_as_float(ud[x]), __uint_as_float(ud[x + 1])),
+                                  f2_pack(-d4.x, -d4.y))), a0, a1);
+          f2_unpack(f2_mul(bf16x2_widen(w1),
+                           f2_add(f2_pack(__uint_as_float(ud[x + 2]), __uint_as_float(ud[x + 3])),
+                                  f2_pack(-d4.z, -d4.w))), a2, a3);
+          dw[x >> 1] = pack_bf16x2(a0, a1);
+          dw[(x >> 1) + 1] = pack_bf16x2(a2, a3);
         }
         tmem_st16(tmem + lane_off + COL_DPT + 64 * hf + 16 * ch, dw);
       }
@@ -663,13 +681,25 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       tc_fence_before();
       warp_arrive(ctl.bar(B_PT_FULL));
+      // the mask test is taken out of the loop (only the last block of a
+      // sequence and the causal diagonal need it)
+      if (!edge) {
+        const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-      for (int x = 0; x < 64; ++x) {
-        const int k0 = s * BM + 64 * hf + x;
-        float pe = ex2_approx(pv[x] * c - lse2);
-        if (edge && (k0 >= len || (p.causal && k0 > qrow)))   // past the sequence, or causal
-          pe = 0.f;
-        pv[x] = pe;
+        for (int x = 0; x < 64; x += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(pv[x], pv[x + 1]), c2, nl2), a0, a1);
+          pv[x] = ex2_approx(a0);
+          pv[x + 1] = ex2_approx(a1);
+        }
+      } else {
+#pragma unroll
+        for (int x = 0; x < 64; ++x) {
+          const int k0 = s * BM + 64 * hf + x;
+          float pe = ex2_approx(pv[x] * c - lse2);
+          if (k0 >= len || (p.causal && k0 > qrow)) pe = 0.f;   // past the sequence, or causal
+          pv[x] = pe;
+        }
       }
       // phase 2: dS = P o (dP - D), bf16 over the first 32 of the 64 columns
       if (!(ok = wait_warp(ctl.bar(B_DPT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
@@ -683,10 +713,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tmem_wait_ld();
         reg_fence32(ud);
         uint32_t dw[16];
+        const uint64_t nd2 = f2_pack(-dsum, -dsum);
 #pragma unroll
-        for (int x = 0; x < 32; x += 2)
-          dw[x >> 1] = pack_bf16x2(pv[32 * ch + x] * (__uint_as_float(ud[x]) - dsum),
-                                   pv[32 * ch + x + 1] * (__uint_as_float(ud[x + 1]) - dsum));
+        for (int x = 0; x < 32; x += 2) {
+          float a0, a1;
+          f2_unpack(f2_mul(f2_pack(pv[32 * ch + x], pv[32 * ch + x + 1]),
+                           f2_add(f2_pack(__uint_as_float(ud[x]), __uint_as_float(ud[x + 1])), nd2)),
+                    a0, a1);
+          dw[x >> 1] = pack_bf16x2(a0, a1);
+        }
         tmem_st16(tmem + lane_off + COL_DP + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
