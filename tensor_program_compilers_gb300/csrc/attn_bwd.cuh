@@ -128,10 +128,13 @@ struct BCfg {
   static constexpr uint32_t A_SLOT = 2 * TILE + 1024;
   static constexpr uint32_t A_OFF_RING = 2 * TILE;
   static constexpr uint32_t A_OFF_CTL = A_OFF_RING + STAGES * A_SLOT;
-  // dQ kernel: Q, dO, then STAGES x {K, V}
-  static constexpr uint32_t B_SLOT = 2 * TILE;
-  static constexpr uint32_t B_OFF_RING = 2 * TILE;
-  static constexpr uint32_t B_OFF_CTL = B_OFF_RING + STAGES * B_SLOT;
+  // dQ kernel: Q, dO, then a ring of K_STAGES K tiles and one of V_STAGES V
+  // tiles (K is held from S to the dQ product, V only for dP, so K gets the
+  // deeper ring: its load for a step starts two steps ahead)
+  static constexpr int K_STAGES = 3, V_STAGES = 2;
+  static constexpr uint32_t B_OFF_K = 2 * TILE;
+  static constexpr uint32_t B_OFF_V = B_OFF_K + K_STAGES * TILE;
+  static constexpr uint32_t B_OFF_CTL = B_OFF_V + V_STAGES * TILE;
   static constexpr uint32_t CTL_BYTES = 256;
   // at least 116 KB so that one CTA holds an SM (and all of its tensor memory)
   static constexpr uint32_t MIN_SMEM = 116u << 10;
@@ -156,7 +159,9 @@ enum : int {
   B_DPT_FULL,          // the step's dP^T or dP in TMEM
   B_PT_FULL,           // all softmax warps: P^T written over S^T (dK/dV), or S read (dQ)
   B_DST_FULL,          // all softmax warps: dS^T (dS) written over dP^T (dP)
-  B_COUNT
+  B_KFULL0,            // dQ kernel: K ring slot s loaded, s < 3 (B_FULL0/1 and
+  B_KEMPTY0 = B_KFULL0 + 3,   // B_EMPTY0/1 serve its V ring); K slot s consumed
+  B_COUNT = B_KEMPTY0 + 3
 };
 
 // ------------------------------------------------------------------ row pass
@@ -223,6 +228,10 @@ __device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
   mbar_init(c.bar(B_DPT_FULL), 1);
   mbar_init(c.bar(B_PT_FULL), BWD_SM_WARPS);
   mbar_init(c.bar(B_DST_FULL), BWD_SM_WARPS);
+  for (int s = 0; s < 3; ++s) {
+    mbar_init(c.bar(B_KFULL0 + s), 1);
+    mbar_init(c.bar(B_KEMPTY0 + s), 1);
+  }
   c.words[1] = 0u;
   mbar_init_fence();
 }
@@ -572,26 +581,39 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tma_load_3d(do_s + c * CHUNK_BYTES, &tm_do, ctl.bar(B_STATIC_FULL), c * 64, h,
                     row0 + ib * BM);
       }
+      int issued_v = 0;
       for (int s = 0; ok && s < steps; ++s) {
-        const int slot = s & 1;
-        if (s >= 2 && !(ok = wait_bounded(ctl.bar(B_EMPTY0 + slot), (uint32_t)((s - 2) >> 1) & 1u,
-                                          abort_flag, p.timeout_ns)))
+        const int ks = s % C::K_STAGES, vs = s % C::V_STAGES;
+        if (s >= C::K_STAGES &&
+            !(ok = wait_bounded(ctl.bar(B_KEMPTY0 + ks), (uint32_t)(s / C::K_STAGES - 1) & 1u,
+                                abort_flag, p.timeout_ns)))
           break;
-        const uint32_t dst = base + C::B_OFF_RING + slot * C::B_SLOT;
-        mbar_arrive_expect_tx(ctl.bar(B_FULL0 + slot), 2 * C::TILE);
-        for (int c = 0; c < C::CHUNKS; ++c) {
-          tma_load_3d(dst + c * CHUNK_BYTES, &tm_k, ctl.bar(B_FULL0 + slot), c * 64, kvh,
+        const uint32_t kdst = base + C::B_OFF_K + ks * C::TILE;
+        mbar_arrive_expect_tx(ctl.bar(B_KFULL0 + ks), C::TILE);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(kdst + c * CHUNK_BYTES, &tm_k, ctl.bar(B_KFULL0 + ks), c * 64, kvh,
                       row0 + s * BM);
-          tma_load_3d(dst + C::TILE + c * CHUNK_BYTES, &tm_v, ctl.bar(B_FULL0 + slot), c * 64,
-                      kvh, row0 + s * BM);
-        }
         ++issued;
+        if (s >= C::V_STAGES &&
+            !(ok = wait_bounded(ctl.bar(B_EMPTY0 + vs), (uint32_t)(s / C::V_STAGES - 1) & 1u,
+                                abort_flag, p.timeout_ns)))
+          break;
+        const uint32_t vdst = base + C::B_OFF_V + vs * C::TILE;
+        mbar_arrive_expect_tx(ctl.bar(B_FULL0 + vs), C::TILE);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(vdst + c * CHUNK_BYTES, &tm_v, ctl.bar(B_FULL0 + vs), c * 64, kvh,
+                      row0 + s * BM);
+        ++issued_v;
       }
       if (*abort_flag) {
         wait_drain(ctl.bar(B_STATIC_FULL), 0, p.timeout_ns);
-        for (int s = 0; s < 2 && s < issued; ++s) {
-          const int last = s + 2 * ((issued - 1 - s) / 2);
-          wait_drain(ctl.bar(B_FULL0 + s), (uint32_t)(last >> 1) & 1u, p.timeout_ns);
+        for (int s = 0; s < C::K_STAGES && s < issued; ++s) {
+          const int last = s + C::K_STAGES * ((issued - 1 - s) / C::K_STAGES);
+          wait_drain(ctl.bar(B_KFULL0 + s), (uint32_t)(last / C::K_STAGES) & 1u, p.timeout_ns);
+        }
+        for (int s = 0; s < C::V_STAGES && s < issued_v; ++s) {
+          const int last = s + C::V_STAGES * ((issued_v - 1 - s) / C::V_STAGES);
+          wait_drain(ctl.bar(B_FULL0 + s), (uint32_t)(last / C::V_STAGES) & 1u, p.timeout_ns);
         }
       }
     }
@@ -604,41 +626,49 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // Per step s: S(s) and dP(s) in full; S(s+1) as soon as the softmax
       // warps have read S(s) (P is no operand here); dQ += dS(s) K once they
       // have written dS over dP(s); then dP(s+1) (dP's columns are free once
-      // dQ(s) has read dS: one thread's MMAs run in issue order).
-      const uint32_t ring = base + C::B_OFF_RING;
+      // dQ(s) has read dS: one thread's MMAs run in issue order).  A V slot
+      // is released when its dP product is done, a K slot after dQ.
+      const uint32_t kring = base + C::B_OFF_K, vring = base + C::B_OFF_V;
       if (ok && steps > 0 &&
-          (ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+          (ok = wait_bounded(ctl.bar(B_KFULL0), 0, abort_flag, p.timeout_ns))) {
         tc_fence_after();
-        issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(ring, 16, 1024));
+        issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring, 16, 1024));
         tc_commit(ctl.bar(B_ST_FULL));
-        issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(ring + C::TILE, 16, 1024));
-        tc_commit(ctl.bar(B_DPT_FULL));
+        if ((ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+          tc_fence_after();
+          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring, 16, 1024));
+          tc_commit(ctl.bar(B_DPT_FULL));
+          tc_commit(ctl.bar(B_EMPTY0));   // V(0) is read
+        }
       }
       for (int s = 0; ok && s < steps; ++s) {
-        const int slot = s & 1;
-        const uint32_t k_s = ring + slot * C::B_SLOT;
-        const uint32_t k_n = ring + (slot ^ 1) * C::B_SLOT;   // the next step's slot
+        const int ks = s % C::K_STAGES, kn = (s + 1) % C::K_STAGES, vn = (s + 1) % C::V_STAGES;
         const bool more = s + 1 < steps;
         if (!(ok = wait_bounded(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         if (more) {
-          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
+          if (!(ok = wait_bounded(ctl.bar(B_KFULL0 + kn), (uint32_t)((s + 1) / C::K_STAGES) & 1u,
                                   abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(k_n, 16, 1024));
+          issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring + kn * C::TILE, 16, 1024));
           tc_commit(ctl.bar(B_ST_FULL));
         }
         if (!(ok = wait_bounded(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
-        const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
+        const uint64_t k_mn = smem_desc_sw128(kring + ks * C::TILE, CHUNK_BYTES, 1024);
         issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 0, s > 0);
         issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 1, s > 0);
-        tc_commit(ctl.bar(B_EMPTY0 + slot));   // K(s), V(s) are read
+        tc_commit(ctl.bar(B_KEMPTY0 + ks));   // K(s) is read
         if (more) {
-          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(k_n + C::TILE, 16, 1024));
+          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + vn), (uint32_t)((s + 1) / C::V_STAGES) & 1u,
+                                  abort_flag, p.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
           tc_commit(ctl.bar(B_DPT_FULL));
+          tc_commit(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
         }
       }
       if (ok) tc_commit(ctl.bar(B_DONE));
