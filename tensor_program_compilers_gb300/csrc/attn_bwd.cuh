@@ -428,9 +428,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
       const int slot = s & 1;
-      if (!(ok = wait_warp(ctl.bar(B_ST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)) ||
-          !(ok = wait_warp(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
-                           p.timeout_ns)))
+      // the slot's rows (loaded long before) first, so that the wait on
+      // S^T, which is on the step's critical path, is the last one
+      if (!(ok = wait_warp(ctl.bar(B_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
+                           p.timeout_ns)) ||
+          !(ok = wait_warp(ctl.bar(B_ST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
         break;
       tc_fence_after();
       const int ib = i0 + s % (nblk - i0);
