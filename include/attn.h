@@ -247,8 +247,9 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
 
 /*
  * attn_get_status -- synchronises `stream`, then reads and clears the
- * current device's status word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT,
- * ATTN_ERR_BAD_SEQLENS, or ATTN_ERR_CUDA if the synchronisation failed.
+ * current device's status word (the first device-side error recorded since
+ * the last read).  Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_SEQLENS,
+ * ATTN_ERR_BAD_PAGE_TABLE, or ATTN_ERR_CUDA if the synchronisation failed.
  */
 attn_status attn_get_status(cudaStream_t stream);
 
