@@ -72,6 +72,8 @@ def load_library(path: str):
         ctypes.c_double, ctypes.c_int, ctypes.c_int,                         # scale causal nthreads
     ]
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_round_bf16.restype = None
+    lib.oracle_round_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
     return lib
 
 
@@ -85,6 +87,16 @@ def _load():
 
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
+
+
+def round_bf16(x, lib=None) -> np.ndarray:
+    """The oracle's rounding of doubles to the nearest bf16 value (ties to
+    even), as used by the ``round_p`` diagnostic; returned as float64."""
+    lib = lib or _load()
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(a)
+    lib.oracle_round_bf16(a.ctypes.data, out.ctypes.data, a.size)
+    return out
 
 
 def _bits(x) -> np.ndarray:

@@ -74,16 +74,30 @@ static double bf16_to_double(uint16_t b) {
   return (double)f;
 }
 
-/* double -> nearest bf16 value (ties to even), returned as a double.  Used
- * only by the round_p diagnostic; inputs are finite and non-negative. */
+/* double -> the nearest bf16 value (ties to the even significand), returned
+ * as a double.  One rounding, taken from the double itself (going through
+ * float first would round twice, which can settle a near-tie the wrong way).
+ * bf16 keeps 8 significant bits: in the binade [2^(e-1), 2^e) its values are
+ * the multiples of 2^(e-1-7); below 2^-126 (subnormals) the multiples of
+ * 2^-133.  Scaling x by a power of two is exact, and rint() rounds to the
+ * nearest integer with ties to even (the default rounding mode), so the
+ * scaled value rounds exactly as the definition asks; a result of 2^8 times
+ * the spacing is the next binade's first value, which is right too.  Used
+ * only by the round_p diagnostic; x is finite and below the largest bf16. */
 static double round_to_bf16(double x) {
-  float f = (float)x;
-  uint32_t u;
-  memcpy(&u, &f, sizeof u);
-  uint32_t lsb = (u >> 16) & 1u;
-  u = (u + 0x7FFFu + lsb) & 0xFFFF0000u;
-  memcpy(&f, &u, sizeof f);
-  return (double)f;
+  if (x == 0.0 || !isfinite(x)) return x;
+  const double ax = fabs(x);
+  int e;
+  (void)frexp(ax, &e);               /* ax = f * 2^e with f in [0.5, 1) */
+  int spacing_exp = (e - 1) - 7;
+  if (spacing_exp < -133) spacing_exp = -133;
+  const double y = ldexp(rint(ldexp(ax, -spacing_exp)), spacing_exp);
+  return x < 0.0 ? -y : y;
+}
+
+/* Test hook for the rounding above: y[i] = round_to_bf16(x[i]). */
+void oracle_round_bf16(const double *x, double *y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = round_to_bf16(x[i]);
 }
 
 /*

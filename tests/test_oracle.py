@@ -363,16 +363,74 @@ def test_matches_torch_softmax_fp64(causal):
     np.testing.assert_allclose(lse, torch.logsumexp(S, -1).numpy(), rtol=0, atol=1e-12)
 
 
-def test_round_p_diagnostic_is_close_but_not_equal():
-    B, N, H, d = 1, 96, 2, 32
-    q = rand_bf16((B, N, H, d), 95)
-    k = rand_bf16((B, N, H, d), 96)
-    v = rand_bf16((B, N, H, d), 97)
-    o1, l1 = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.2, True)
-    o2, l2 = attn_fwd_oracle(q, k, v, B, H, H, N, d, 0.2, True, round_p=True)
-    np.testing.assert_array_equal(l1, l2)      # LSE uses unrounded weights
-    diff = np.abs(o1 - o2).max()
-    assert 0 < diff < 2e-2
+def bf16_neighbours():
+    """Every pair of adjacent positive finite bf16 values (a, b), as doubles,
+    with whether a's significand is even.  bf16 bit patterns of one sign are
+    ordered like the values they encode, so adjacent patterns are adjacent
+    values; the pair (0x7F, 0x80) crosses from subnormals to normals and the
+    pairs whose lower value ends in 0x7F cross into the next binade."""
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)           # up to the largest finite
+    vals = (bits << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    return vals[:-1], vals[1:], (bits[:-1] & 1) == 0
+
+
+def round_bf16_pins_hold(lib=None) -> bool:
+    """Pins of the oracle's double -> bf16 rounding (round to nearest, ties to
+    even), from the definition alone: bf16 values are fixed points; an exact
+    midpoint goes to the neighbour with the even significand; a value a tiny
+    step off the midpoint goes to the nearer neighbour (truncation, rounding
+    half up, or rounding to float first all fail one of these); signs are
+    symmetric; values below half the smallest subnormal round to zero."""
+    a, b, a_even = bf16_neighbours()
+    r = lambda x: oracle.round_bf16(x, lib=lib)
+    ok = np.array_equal(r(a), a) and np.array_equal(r(b), b)
+    mid = (a + b) / 2                                  # exact in double
+    ok &= np.array_equal(r(mid), np.where(a_even, a, b))
+    eps = (b - a) * 2.0 ** -30                         # far below float's resolution here
+    ok &= np.array_equal(r(mid + eps), b) and np.array_equal(r(mid - eps), a)
+    ok &= np.array_equal(r(-(mid + eps)), -b) and np.array_equal(r(-mid), -np.where(a_even, a, b))
+    tiny = 2.0 ** -134                                 # half the smallest subnormal (a tie)
+    ok &= np.array_equal(r([tiny, tiny * 0.99, tiny * 1.01, 0.0]), [0.0, 0.0, 2.0 ** -133, 0.0])
+    return bool(ok)
+
+
+def test_round_bf16_is_nearest_even():
+    assert round_bf16_pins_hold()
+
+
+def test_round_p_rounds_each_weight_to_nearest_bf16():
+    """Through the round_p switch: a row that sees two keys with scores 0 and
+    s < 0 and one-hot values gets o[1] = bf16(e^s) / (1 + e^s) (the sum keeps
+    the unrounded weights).  The recovered weight must be a bf16 value no
+    farther from e^s than either of its bf16 neighbours."""
+    n = 64
+    svals = -np.linspace(0.01, 9.0, n)                  # one row per head
+    d = 8
+    q = torch.zeros((1, 2, n, d), dtype=torch.bfloat16)
+    q[..., 0] = 1.0
+    k = torch.zeros((1, 2, n, d))
+    k[0, 1, :, 0] = torch.tensor(svals)
+    k = k.to(torch.bfloat16)
+    s = k[0, 1, :, 0].double().numpy()                  # the scores as bf16 inputs give them
+    v = torch.zeros((1, 2, n, d), dtype=torch.bfloat16)
+    v[0, 0, :, 0] = 1.0
+    v[0, 1, :, 1] = 1.0
+    o, lse = attn_fwd_oracle(q, k, v, 1, n, n, 2, d, 1.0, False, round_p=True)
+    p = np.exp(s)
+    w = o[0, 1, :, 1] * (1.0 + p)                       # recovered rounded weight
+    np.testing.assert_allclose(o[0, 1, :, 0] * (1.0 + p), 1.0, rtol=1e-15)   # bf16(1) = 1
+    np.testing.assert_allclose(lse[0, :, 1], np.log1p(p), rtol=0, atol=1e-15)
+    # o * (1 + p) recovers the weight up to a couple of double roundings
+    wb = torch.tensor(w, dtype=torch.float64).to(torch.float32)
+    c = wb.double().numpy()
+    assert (np.abs(w - c) <= 1e-15 * c).all(), "not a float value"
+    bits = wb.view(torch.int32)
+    assert (bits & 0xFFFF).eq(0).all(), "not a bf16 value"
+    up = ((bits + 0x10000).view(torch.float32)).double().numpy()
+    down = ((bits - 0x10000).view(torch.float32)).double().numpy()
+    err = np.abs(c - p)
+    assert (err <= np.abs(up - p)).all() and (err <= np.abs(down - p)).all()
+    assert (c != p).all()                               # the switch did round
 
 
 def test_row_selection_matches_full():

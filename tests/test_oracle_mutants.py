@@ -49,6 +49,14 @@ MUTANTS = {
     "backward: causal bound off by one": ("const int64_t n = causal ? i + 1 : L;",
                                           "const int64_t n = causal ? i : L;"),
     "backward: P not normalised": ("      p[j] /= l;\n", ""),
+    "bf16 rounding truncates": ("ldexp(rint(ldexp(ax, -spacing_exp)), spacing_exp)",
+                                "ldexp(floor(ldexp(ax, -spacing_exp)), spacing_exp)"),
+    "bf16 rounding ties upward": ("ldexp(rint(ldexp(ax, -spacing_exp)), spacing_exp)",
+                                  "ldexp(floor(ldexp(ax, -spacing_exp) + 0.5), spacing_exp)"),
+    "bf16 rounding through float first": ("const double ax = fabs(x);",
+                                          "const double ax = (double)(float)fabs(x);"),
+    "bf16 spacing one bit too fine": ("int spacing_exp = (e - 1) - 7;",
+                                      "int spacing_exp = (e - 1) - 8;"),
     "q row of the kv head": ("const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)h * d;",
                              "const uint16_t *qrow = q + (q_start[s] + i) * qstride + (int64_t)kv * d;"),
 }
@@ -135,6 +143,10 @@ def _pins_pass(lib) -> bool:
         for mine, ref in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
             if not np.allclose(mine, ref.numpy(), atol=1e-12, rtol=0):
                 return False
+    # the round_p diagnostic's rounding to bf16
+    from test_oracle import round_bf16_pins_hold
+    if not round_bf16_pins_hold(lib):
+        return False
     # Q = 0 closed form
     q = torch.zeros((1, 9, 2, 4), dtype=torch.bfloat16)
     k = rand_bf16((1, 9, 2, 4), 5)
