@@ -153,6 +153,11 @@ attn_status attn_fwd_ex(const void *q, const void *k, const void *v, void *o, fl
  *
  * Other arguments and errors as attn_fwd; too small a workspace is
  * ATTN_ERR_INVALID_ARG.  The split count depends on the device's SM count.
+ *
+ * attn_decode_workspace_bytes returns 0 both when the problem needs no
+ * workspace (one split) and when it cannot size one (invalid arguments, an
+ * unsupported or unusable device); rely on the status that attn_fwd_decode
+ * (or attn_fwd_decode_static) returns for the actual error.
  */
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 attn_status attn_fwd_decode(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -196,8 +201,11 @@ attn_status attn_fwd_decode_paged(const void *q, const void *k_cache, const void
  * attn_fwd_decode_static -- attn_fwd_decode without a caller workspace and
  * without any allocation: the partial states live in a fixed 8 MiB device
  * array inside the library (one per device).  The pages have no
- * counterpart; this exists for callers that cannot provide or allocate
- * memory (for example inside a captured CUDA graph).
+ * counterpart.  It is for callers that can neither allocate device memory
+ * nor hand one over: a plug-in whose host program owns all device memory
+ * through its own allocator and lends it none, or a serving loop that
+ * allows no allocation once it runs, because cudaMalloc and cudaFree can
+ * synchronise the whole device and stall every other stream.
  *
  *   - Problems whose attn_decode_workspace_bytes() exceeds 8 MiB
  *     (8388608 bytes) are rejected with ATTN_ERR_INVALID_ARG.
@@ -246,12 +254,28 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      cudaStream_t stream);
 
 /*
- * attn_get_status -- synchronises `stream`, then reads and clears the
- * current device's status word (the first device-side error recorded since
- * the last read).  Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_SEQLENS,
- * ATTN_ERR_BAD_PAGE_TABLE, or ATTN_ERR_CUDA if the synchronisation failed.
+ * attn_get_status -- takes and clears the current device's status word (the
+ * first device-side error recorded since the last read) in one atomic
+ * exchange, ordered on `stream` after the work already queued there, then
+ * synchronises `stream` and returns the value taken: ATTN_OK,
+ * ATTN_ERR_TIMEOUT, ATTN_ERR_BAD_SEQLENS, ATTN_ERR_BAD_PAGE_TABLE, or
+ * ATTN_ERR_CUDA if the launch, the copy or the synchronisation failed.
+ * The word is one per device, shared by every stream: an error that a
+ * kernel on another stream records is returned by whichever read follows
+ * it (no error is lost between the read and the clear).  Calls from several
+ * host threads are serialised inside the library.
  */
 attn_status attn_get_status(cudaStream_t stream);
+
+/*
+ * attn_debug_one_tile -- diagnostic switch for tests: nonzero makes every
+ * later attn_fwd / attn_fwd_ex call in this process run the one-tile kernel
+ * (one 128-row query tile per CTA), which otherwise serves only d = 256,
+ * key windows, score modifiers, and devices whose register budget cannot
+ * take the two-tile kernel.  Results agree within the stated tolerances;
+ * only speed and rounding order differ.  Returns the previous setting.
+ */
+int attn_debug_one_tile(int on);
 
 /* attn_status_string -- a static, human-readable name for a status code. */
 const char *attn_status_string(attn_status s);

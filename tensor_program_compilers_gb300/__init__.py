@@ -42,7 +42,8 @@ ATTN_ERR_BAD_PAGE_TABLE = 7
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
             "attn_fwd_decode_paged", "attn_decode_paged_workspace_bytes",
             "attn_fwd_decode_static", "attn_bwd", "attn_bwd_workspace_bytes",
-            "attn_get_status", "attn_status_string", "attn_selftest_timeout"]
+            "attn_get_status", "attn_status_string", "attn_selftest_timeout",
+            "attn_debug_one_tile"]
 
 
 class AttnVariant(ctypes.Structure):
@@ -116,6 +117,8 @@ def _load():
         lib.attn_status_string.argtypes = [i]
         lib.attn_selftest_timeout.restype = i
         lib.attn_selftest_timeout.argtypes = [i, vp]
+        lib.attn_debug_one_tile.restype = i
+        lib.attn_debug_one_tile.argtypes = [i]
         _lib = lib
     return _lib
 
@@ -316,12 +319,19 @@ def decode(q, k, v, causal: bool = False, scale: Optional[float] = None, seqlens
 
 
 def attn_get_status(stream=None) -> int:
-    """Synchronise the stream and read/clear the device status word."""
+    """Take and clear the device status word (one atomic exchange ordered on
+    the stream), then synchronise the stream."""
     return _load().attn_get_status(_stream(stream))
 
 
 def attn_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
     return _load().attn_selftest_timeout(int(timeout_us), _stream(stream))
+
+
+def attn_debug_one_tile(on: bool) -> bool:
+    """Route every later forward through the one-tile kernel (tests); returns
+    the previous setting."""
+    return bool(_load().attn_debug_one_tile(1 if on else 0))
 
 
 def attention(q, k, v, causal: bool, scale: Optional[float] = None, cu_seqlens=None,

@@ -58,6 +58,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <mutex>
@@ -1477,6 +1478,8 @@ static bool opt_in_smem(K kernel, uint32_t bytes) {
 // kernel instantiations, done once.
 static int g_sm_count[MAX_DEVICES];
 static bool g_two_tiles_ok[MAX_DEVICES];
+// attn_debug_one_tile: run every forward through the one-tile kernel.
+static std::atomic<int> g_force_one_tile{0};
 
 // Scratch of attn_fwd_decode_static: a fixed device array (the library
 // allocates nothing); its address on each device is looked up once, when
@@ -1607,8 +1610,8 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
   const bool mod = cap > 0.f || slopes != nullptr;
   // Two query tiles per CTA (head dims 64, 128) unless a window or a score
   // modifier asks for the one-tile kernel.
-  const bool two_tiles =
-      g_two_tiles_ok[dev] && !mod && d <= 128 && p.wl >= N && (causal || p.wr >= N);
+  const bool two_tiles = g_two_tiles_ok[dev] && !g_force_one_tile.load() && !mod && d <= 128 &&
+                         p.wl >= N && (causal || p.wr >= N);
   p.unit_rows = two_tiles ? two::UNIT_ROWS : BM;
   p.num_units = (N + p.unit_rows - 1) / p.unit_rows;
   p.scale = scale;
@@ -1827,12 +1830,23 @@ extern "C" attn_status attn_fwd_decode_static(const void *q, const void *k, cons
                            nullptr, 0, true, nullptr, stream);
 }
 
+namespace attn {
+// The status word is taken and cleared in one atomic exchange on the device,
+// so an error that a kernel on another stream records at any moment is
+// either returned by this read or kept for the next one.
+__device__ int g_status_taken;
+__global__ void take_status_kernel() { g_status_taken = atomicExch(&g_status, 0); }
+}  // namespace attn
+
 extern "C" attn_status attn_get_status(cudaStream_t stream) {
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  static std::mutex mu;   // one g_status_taken per device, shared by all callers
+  std::lock_guard<std::mutex> lock(mu);
+  attn::take_status_kernel<<<1, 1, 0, stream>>>();
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   int value = 0;
-  const int zero = 0;
-  if (cudaMemcpyFromSymbol(&value, attn::g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (value != 0 && cudaMemcpyToSymbol(attn::g_status, &zero, sizeof(int)) != cudaSuccess)
+  if (cudaMemcpyFromSymbolAsync(&value, attn::g_status_taken, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return static_cast<attn_status>(value);
 }
@@ -1852,6 +1866,8 @@ extern "C" int attn_trace_read(unsigned *out) {
   return cudaMemcpyFromSymbol(out, attn::g_trace, sizeof(attn::g_trace)) != cudaSuccess;
 }
 #endif
+
+extern "C" int attn_debug_one_tile(int on) { return attn::g_force_one_tile.exchange(on ? 1 : 0); }
 
 extern "C" const char *attn_status_string(attn_status s) {
   switch (s) {

@@ -148,3 +148,98 @@ def test_bwd_packed_bad_offsets_reported():
     pkg.attn_bwd(t, t, t, t, t, lse, out, out, out, 2, H, H, T, d, 0.125, True, bad, ws)
     assert pkg.attn_get_status() == pkg.ATTN_ERR_BAD_SEQLENS
     assert torch.isnan(out.float()).all()
+
+
+def _oracle_async(pool, q, k, v, g, B, Hq, Hkv, N, d, causal, cu=None):
+    return pool.submit(oracle.attn_bwd_oracle, q, k, v, g, B, Hq, Hkv, N, d, d ** -0.5,
+                       causal, cu_seqlens=cu)
+
+
+def _check_grads(mine, refs, what):
+    for name, m, r in zip(("dq", "dk", "dv"), mine, refs):
+        assert np.isfinite(m).all(), f"{what} {name}: unwritten or non-finite"
+        err = np.abs(m - r)
+        msg = (f"{what} {name}: max|err|={err.max():.3e} (max|ref| {np.abs(r).max():.3e}) "
+               f"mean|err|={err.mean():.3e} (mean|ref| {np.abs(r).mean():.3e})")
+        assert err.max() <= REL_MAX * max(np.abs(r).max(), 1e-3), msg
+        assert err.mean() <= REL_MEAN * max(np.abs(r).mean(), 1e-3), msg
+
+
+def test_bwd_parity_long_sequences():
+    """Sequences as long as the benchmarked backward's (4096 rows): dK/dV
+    units that walk 32 query blocks of every query head of a four-head group,
+    dQ units that walk 32 key blocks; causal at N = 4096, non-causal at
+    N = 2048, and a packed batch whose first sequence is longer than 4096.
+    One kv head keeps the fp64 oracle to seconds; its three calls run
+    side by side (the C oracle releases the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
+    d, Hq, Hkv = 128, 4, 1
+    cases = []
+    for N, causal in ((4096, True), (2048, False)):
+        q, k, v = rand((1, N, Hq, d), 61 + N), rand((1, N, Hkv, d), 62 + N), rand((1, N, Hkv, d), 63 + N)
+        g = rand((1, N, Hq, d), 64 + N)
+        cases.append((f"N={N} causal={causal}", (q, k, v, g, 1, N, causal, None)))
+    lens = [4500, 300, 1, 129]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v, g = rand((T, Hq, d), 71, 2.0), rand((T, Hkv, d), 72), rand((T, Hkv, d), 73), rand((T, Hq, d), 74)
+    cases.append(("packed, first sequence 4500", (q, k, v, g, len(lens), T, True, cu)))
+    with ThreadPoolExecutor(len(cases)) as pool:
+        futs = [_oracle_async(pool, q_, k_, v_, g_, B_, Hq, Hkv, N_, d, c_, cu_)
+                for _, (q_, k_, v_, g_, B_, N_, c_, cu_) in cases]
+        dev = torch.device("cuda:0")
+        mines = []
+        for what, (q_, k_, v_, g_, B_, N_, c_, cu_) in cases:
+            if cu_ is None:
+                mines.append(run_bwd(q_, k_, v_, g_, c_))
+                continue
+            dcu = torch.tensor(cu_, device=dev)
+            tq, tk, tv, tg = (t.to(dev) for t in (q_, k_, v_, g_))
+            o, lse = pkg.attention(tq, tk, tv, causal=c_, cu_seqlens=dcu)
+            grads = pkg.attention_backward(tq, tk, tv, o, lse, tg, c_, cu_seqlens=dcu)
+            assert pkg.attn_get_status() == pkg.ATTN_OK
+            mines.append([t.float().cpu().numpy() for t in grads])
+        for (what, _), mine, fut in zip(cases, mines, futs):
+            _check_grads(mine, fut.result(), what)
+
+
+def test_bwd_benchmarked_shape_fp32():
+    """The benchmarked backward itself (B2 Hq32 Hkv8 N4096 d128 causal) against
+    the gradient formulas evaluated in fp32 with PyTorch on the GPU, head by
+    head (TF32 off; the reference's own error is far below the tolerance):
+    S = scale Q K^T (masked), P = softmax(S), dP = dO V^T, D = rowsum(P dP),
+    dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO, with
+    dK and dV summed over each kv head's four query heads."""
+    B, Hq, Hkv, N, d = 2, 32, 8, 4096, 128
+    gen = torch.Generator().manual_seed(2004)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (torch.randn(s, generator=gen).to(torch.bfloat16).to(dev)
+                   for s in ((B, N, Hq, d), (B, N, Hkv, d), (B, N, Hkv, d), (B, N, Hq, d)))
+    o, lse = pkg.attention(q, k, v, causal=True)
+    dq, dk, dv = pkg.attention_backward(q, k, v, o, lse, do, True)
+    assert pkg.attn_get_status() == pkg.ATTN_OK
+    scale = d ** -0.5
+    grp = Hq // Hkv
+    mask = torch.ones(N, N, dtype=torch.bool, device=dev).triu(1)
+    tf32 = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        rq = torch.empty((B, N, Hq, d), dtype=torch.float32, device=dev)
+        rk = torch.zeros((B, N, Hkv, d), dtype=torch.float32, device=dev)
+        rv = torch.zeros((B, N, Hkv, d), dtype=torch.float32, device=dev)
+        for b in range(B):
+            for h in range(Hq):
+                kv = h // grp
+                qh, kh, vh, gh = (q[b, :, h].float(), k[b, :, kv].float(), v[b, :, kv].float(),
+                                  do[b, :, h].float())
+                p = torch.softmax((qh @ kh.T * scale).masked_fill(mask, float("-inf")), -1)
+                dp = gh @ vh.T
+                ds = p * (dp - (p * dp).sum(-1, keepdim=True))
+                rq[b, :, h] = scale * (ds @ kh)
+                rk[b, :, kv] += scale * (ds.T @ qh)
+                rv[b, :, kv] += p.T @ gh
+                del p, dp, ds
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+    _check_grads([t.float().cpu().numpy() for t in (dq, dk, dv)],
+                 [t.cpu().numpy() for t in (rq, rk, rv)], "B2 Hq32 Hkv8 N4096 d128 causal")
