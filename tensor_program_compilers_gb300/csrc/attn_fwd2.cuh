@@ -21,20 +21,31 @@
 //              (TMEM lane 32 w + t)
 //   warps 4-7  softmax of tile B (TMEM lane quarter w % 4)
 //   warp 8     TMA producer: Q_A, Q_B of the unit, then K_0, V_0, K_1, V_1, ...
-//   warp 9     TMEM allocator and MMA issuer (one thread)
-//   warps 10, 11 idle (they complete the third warpgroup, which hands part of
-//              its registers to the softmax warpgroups)
+//   warp 9     TMEM allocator and MMA issuer: the whole warp runs the issue
+//              loop and one elected lane issues each tcgen05 instruction
+//   warp 10    K/V watcher: adds one arrival to P_FULL_X(j) once V_j (and
+//              K_{j+1}, if tile X computes S(j+1)) have landed, so that the
+//              MMA warp waits on nothing but P_FULL between its batches
+//   warp 11    idle (completes the third warpgroup, which hands part of its
+//              registers to the softmax warpgroups)
 //
 // Tensor memory (512 columns): S_A [0, 128), S_B [128, 256),
 // O_A [256, 256 + d), O_B [256 + d, 256 + 2d).  P_X (bf16 pairs, keys 2c and
 // 2c + 1 in column c) is written over columns [0, 64) of S_X.
 //
-// MMA order (one thread; the tensor core runs one thread's MMAs in issue
-// order): QK_A(0), QK_B(0), then for each key step j
+// MMA order (one warp; the tensor core runs its MMAs in issue order):
+// QK_A(0), QK_B(0), then for each key step j
 //   PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
 // QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X(j) from it, and
 // the commit that signals S_X(j+1) also covers PV_X(j): a softmax warp that
 // sees S_X(j+1) may rescale O_X at once.
+//
+// Measured on this GPU, a tcgen05.mma costs the issuing warp ~45 cycles
+// against the 64 the tensor core takes to run a 128 x 128 x 16 product, so the
+// issue loop holds only ~16 cycles of slack per MMA: one wait per batch (P),
+// the commits the consumers need, and a warp-uniform (elected-lane) issue,
+// which kept its rate beside the busy softmax warps of its sub-partition
+// where a single diverged lane fell far behind.
 
 namespace attn {
 namespace two {
@@ -42,13 +53,13 @@ namespace two {
 constexpr int THREADS2 = 384;   // three warpgroups
 // Warpgroups 0 and 1: the softmax of tiles A and B; warpgroup 2: producer
 // and MMA issuer (warps 10, 11 only complete it).
-constexpr int SM_WARP0 = 0, WARP_PROD = 8, WARP_MMA = 9;
+constexpr int SM_WARP0 = 0, WARP_PROD = 8, WARP_MMA = 9, WARP_WATCH = 10;
 // Register split (setmaxnreg): the kernel is built for 168 registers a thread
 // (384 threads; three warps share each SM sub-partition); the third
 // warpgroup gives part of its share to the softmax warpgroups:
-// 2 x 128 x 208 + 128 x 72 = 62,464 <= 384 x 168 = 64,512.  The host checks
+// 2 x 128 x 208 + 128 x 88 = 64,512 = 384 x 168.  The host checks
 // the built register count against this before it uses the kernel.
-constexpr int REGS_SOFTMAX = 208, REGS_OTHER = 72;
+constexpr int REGS_SOFTMAX = 208, REGS_OTHER = 88;
 constexpr int REGS_NEEDED = (2 * 128 * REGS_SOFTMAX + 128 * REGS_OTHER + THREADS2 - 1) / THREADS2;
 constexpr int UNIT_ROWS = 2 * BM;
 constexpr int UNIT_INTS = 10;   // valid, seq_start, len, unit, h, nA, nB, lse lo/hi
@@ -57,8 +68,13 @@ template <int D>
 struct Cfg2 {
   static constexpr int CHUNKS = D / 64;
   static constexpr uint32_t TILE_BYTES = CHUNKS * CHUNK_BYTES;   // one 128-row Q, K or V tile
-  static constexpr int QB = 2;                                    // Q buffers (two tiles each)
-  static constexpr int STAGES = D == 64 ? 8 : 3;                  // K/V ring slots
+  // Q buffers (two tiles each) and K/V ring slots.  At d = 128 one Q buffer
+  // pair and five ring slots: a K/V tile's load then starts about two key
+  // steps before its first reader (with two Q buffer pairs and three slots,
+  // about one, and the MMAs waited for their operands), at the cost of
+  // loading the next unit's Q only after this unit's last QK.
+  static constexpr int QB = D == 64 ? 2 : 1;
+  static constexpr int STAGES = D == 64 ? 8 : 5;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = 2 * TILE_BYTES * QB;
   static constexpr uint32_t OFF_CTL = OFF_KV + TILE_BYTES * STAGES;
@@ -77,7 +93,7 @@ enum : int {
   T_Q_EMPTY1,
   T_S_FULL0,       // S_X written (commit; also covers PV_X of the previous step), X < 2
   T_S_FULL1,
-  T_P_FULL0,       // P_X written over S_X (the tile's four softmax warps)
+  T_P_FULL0,       // P_X written over S_X (the tile's four softmax warps) and V_j, K_{j+1} landed (watcher)
   T_P_FULL1,
   T_PV_DONE0,      // PV_X completed (commit)
   T_PV_DONE1,
@@ -158,71 +174,90 @@ __device__ __forceinline__ float sum_rounded(const uint32_t (&pk0)[HB / 2],
   return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
-// K/V ring slot of position ps: wait until loaded / release after the MMAs
-// issued so far (by this thread) complete.
+// K/V ring slot of position ps: its full and empty barriers and the parity of
+// the fill that position ps belongs to.
 template <int STAGES>
-__device__ __forceinline__ bool ring_wait(const Ctl2 &ctl, long long ps,
-                                          volatile uint32_t *abort_flag,
-                                          unsigned long long timeout_ns) {
-  return wait_bounded(ctl.bar(T_RING + (int)(ps % STAGES)), (uint32_t)(ps / STAGES) & 1u,
-                      abort_flag, timeout_ns);
+__device__ __forceinline__ uint32_t ring_full(const Ctl2 &ctl, long long ps) {
+  return ctl.bar(T_RING + (int)(ps % STAGES));
 }
 template <int STAGES>
-__device__ __forceinline__ void ring_release(const Ctl2 &ctl, long long ps) {
-  tc_commit(ctl.bar(T_RING + STAGES + (int)(ps % STAGES)));
+__device__ __forceinline__ uint32_t ring_empty(const Ctl2 &ctl, long long ps) {
+  return ctl.bar(T_RING + STAGES + (int)(ps % STAGES));
+}
+template <int STAGES>
+__device__ __forceinline__ uint32_t ring_parity(long long ps) {
+  return (uint32_t)(ps / STAGES) & 1u;
 }
 
 struct IssueState {
   long long npv;   // PV_X issued so far (P_FULL_X phases)
-  int nunits;      // units in which tile X had work (O_FREE_X phases)
+  int nunits;      // units in which tile X had work (O_FREE_X and PV_DONE_X phases)
 };
+
+// Q K_j^T into S (tmem d_tmem), issued by the whole MMA warp (qdesc, kdesc: the
+// 128-row Q and K tiles, K-major, 128-byte swizzle, 64-column chunks).
+template <int D>
+__device__ __forceinline__ void issue_qk_warp(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BN, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t koff = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
+    mma_ss_warp(d_tmem, qdesc + koff, kdesc + koff, IDESC, kk > 0 ? 1u : 0u);
+  }
+}
 
 // Tile X's share of key step j of a unit: PV_X(j) (O_X (+)= P_X(j) V_j; the
 // unit's first overwrites O_X, after the previous epilogue has read it), then
-// QK_X(j+1).  K_j sits at ring position base + 2j, V_j at base + 2j + 1; the
-// first tile to use a slot waits for it (v_ready, k_ready), the last one
-// releases it (tile B whenever it uses the slot).
+// QK_X(j+1).  K_j sits at ring position base + 2j, V_j at base + 2j + 1.
+// Executed by every lane of the MMA warp; each tcgen05 instruction is issued
+// by one elected lane.  One tcgen05.mma costs the issuing warp about 45
+// cycles against the 64 the tensor core takes to run it at N = 128, and the
+// warp runs only a few instructions ahead of the tensor core, so whatever it
+// does between batches beyond ~16 cycles per MMA leaves the tensor core
+// idle.  The warp therefore waits only for P_X(j) (the watcher's arrival in
+// P_FULL_X(j) says that V_j and K_{j+1} have landed), and its commits are
+// S_FULL_X after QK_X(j+1), the release of each ring slot after its last
+// reader, and PV_DONE_X after the tile's last PV (for the epilogue).
+// Descriptor offsets are plain integer additions (the address field cannot
+// carry: shared addresses stay below 256 KB).
 template <int D, int X>
-__device__ __forceinline__ bool pv_then_qk(const Ctl2 &ctl, volatile uint32_t *abort_flag,
-                                           unsigned long long timeout_ns, uint32_t tmem,
-                                           uint64_t kdesc0, uint64_t vdesc0, uint64_t qdesc,
-                                           long long base, int j, int nA, int nB,
-                                           IssueState &st, bool &v_ready, bool &k_ready,
-                                           volatile unsigned *trb) {
+__device__ __forceinline__ bool tile_step(const Ctl2 &ctl, volatile uint32_t *abort_flag,
+                                          unsigned long long timeout_ns, uint32_t tmem,
+                                          uint64_t kdesc0, uint64_t vdesc0, uint64_t qdesc,
+                                          long long base, int j, int nA, int nB,
+                                          IssueState &st, volatile unsigned *trb) {
   using C = Cfg2<D>;
   constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
   (void)trb;
   const int nx = X ? nB : nA;
   if (j >= nx) return true;
-  const long long pv_pos = base + 2 * j + 1, qk_pos = base + 2 * j + 2;
+  const long long v_pos = base + 2 * j + 1, k_pos = base + 2 * j + 2;
+  const bool has_qk = j + 1 < nx;
+  const bool last_user = X == 1 || j >= nB;   // B's MMAs come last in a step
   if (j == 0 && st.nunits > 0 &&
-      !wait_poll(ctl.bar(T_O_FREE0 + X), (uint32_t)(st.nunits - 1) & 1u, abort_flag, timeout_ns))
+      !wait_warp(ctl.bar(T_O_FREE0 + X), (uint32_t)(st.nunits - 1) & 1u, abort_flag, timeout_ns))
     return false;
   ATTN_TRACE_SM(trb, st.npv, 6 + X);
-  if (!wait_poll(ctl.bar(T_P_FULL0 + X), (uint32_t)st.npv & 1u, abort_flag, timeout_ns))
+  if (!wait_warp(ctl.bar(T_P_FULL0 + X), (uint32_t)st.npv & 1u, abort_flag, timeout_ns))
     return false;
   ATTN_TRACE_SM(trb, st.npv, 3 * X);
-  if (!v_ready && !ring_wait<C::STAGES>(ctl, pv_pos, abort_flag, timeout_ns)) return false;
-  v_ready = true;
   tc_fence_after();
-  const uint64_t vdesc = desc_add(vdesc0, (uint32_t)(pv_pos % C::STAGES) * C::TILE_BYTES);
+  const uint64_t vdesc = vdesc0 + (((uint32_t)(v_pos % C::STAGES) * C::TILE_BYTES) >> 4);
   const uint32_t s_x = tmem + 128u * X;
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
-    mma_ts(tmem + C::COL_O + (uint32_t)(D * X), s_x + kk * 8, desc_add(vdesc, kk * 2048),
-           IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-  tc_commit(ctl.bar(T_PV_DONE0 + X));
+    mma_ts_warp(tmem + C::COL_O + (uint32_t)(D * X), s_x + kk * 8, vdesc + (kk * 2048 >> 4),
+                IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+  if (!has_qk) tc_commit_warp(ctl.bar(T_PV_DONE0 + X));   // the tile's last PV: O_X is final
+  if (last_user) tc_commit_warp(ring_empty<C::STAGES>(ctl, v_pos));   // V_j's last use
   ATTN_TRACE_SM(trb, st.npv, 3 * X + 1);
   ++st.npv;
-  if (X == 1 || j >= nB) ring_release<C::STAGES>(ctl, pv_pos);   // V_j's last use
-  if (j + 1 < nx) {   // QK_X(j+1)
-    if (!k_ready && !ring_wait<C::STAGES>(ctl, qk_pos, abort_flag, timeout_ns)) return false;
-    k_ready = true;
-    tc_fence_after();
-    issue_qk<D>(s_x, qdesc, desc_add(kdesc0, (uint32_t)(qk_pos % C::STAGES) * C::TILE_BYTES));
-    tc_commit(ctl.bar(T_S_FULL0 + X));
+  if (has_qk) {   // QK_X(j+1)
+    issue_qk_warp<D>(s_x, qdesc,
+                     kdesc0 + (((uint32_t)(k_pos % C::STAGES) * C::TILE_BYTES) >> 4));
+    tc_commit_warp(ctl.bar(T_S_FULL0 + X));
+    if (last_user) tc_commit_warp(ring_empty<C::STAGES>(ctl, k_pos));   // K_{j+1}'s last use
     ATTN_TRACE_SM(trb, st.npv, 3 * X + 2);
-    if (X == 1 || j + 1 >= nB) ring_release<C::STAGES>(ctl, qk_pos);   // K_{j+1}'s last use
   }
   return true;
 }
@@ -250,7 +285,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
   volatile uint32_t *abort_flag = ctl.words + 1;
   const uint32_t q_s = base_s + C::OFF_Q;
   const uint32_t kv_s = base_s + C::OFF_KV;
-  constexpr uint32_t INFO_CONSUMERS = 1 + 8;   // the MMA issuer, the softmax warps
+  constexpr uint32_t INFO_CONSUMERS = 1 + 8 + 1;   // the MMA issuer, the softmax warps, the watcher
   const int tslot = ATTN_TRACE_SLOT();          // -1 unless built for tracing
 
   if (warp == WARP_MMA) {
@@ -259,7 +294,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
         mbar_init(ctl.bar(T_Q_FULL0 + b), 1);
         mbar_init(ctl.bar(T_Q_EMPTY0 + b), 1);
         mbar_init(ctl.bar(T_S_FULL0 + b), 1);
-        mbar_init(ctl.bar(T_P_FULL0 + b), 4);
+        mbar_init(ctl.bar(T_P_FULL0 + b), 4 + 1);   // the tile's softmax warps, the watcher
         mbar_init(ctl.bar(T_PV_DONE0 + b), 1);
         mbar_init(ctl.bar(T_O_FREE0 + b), 4);
       }
@@ -369,8 +404,8 @@ __global__ void __launch_bounds__(THREADS2, 1)
     }
     __syncwarp();
    } else if (warp == WARP_MMA) {
-    // ---------------- MMA issuer (one thread)
-    if (lane == 0) {
+    // ---------------- MMA issuer (the whole warp; one elected lane issues)
+    {
       const uint64_t kdesc0 = smem_desc_sw128(kv_s, 16, 1024);
       const uint64_t vdesc0 = smem_desc_sw128(kv_s, CHUNK_BYTES, 1024);
       // trace builds: issuer stamps in the spare end of the control block
@@ -381,45 +416,89 @@ __global__ void __launch_bounds__(THREADS2, 1)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         UnitInfo t;
-        if (!(ok = read_unit(ctl, k, t, abort_flag, p.timeout_ns))) break;
-        mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
+        if (!(ok = __all_sync(0xffffffffu, read_unit(ctl, k, t, abort_flag, p.timeout_ns))))
+          break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
         if (!t.valid) break;
         const int qb = k % C::QB;
-        if (!(ok = wait_bounded(ctl.bar(T_Q_FULL0 + qb), (uint32_t)(k / C::QB) & 1u,
-                                abort_flag, p.timeout_ns)))
+        if (!(ok = wait_warp(ctl.bar(T_Q_FULL0 + qb), (uint32_t)(k / C::QB) & 1u, abort_flag,
+                             p.timeout_ns)))
           break;
         const uint64_t qd0 = smem_desc_sw128(q_s + 2 * qb * C::TILE_BYTES, 16, 1024);
         const uint64_t qd1 = smem_desc_sw128(q_s + (2 * qb + 1) * C::TILE_BYTES, 16, 1024);
         const int nA = t.n[0], nB = t.n[1];
         const int n = max(nA, nB);
-        if (!(ok = ring_wait<C::STAGES>(ctl, base, abort_flag, p.timeout_ns))) break;
+        if (!(ok = wait_warp(ring_full<C::STAGES>(ctl, base), ring_parity<C::STAGES>(base),
+                             abort_flag, p.timeout_ns)))
+          break;
         tc_fence_after();
-        const uint64_t kd = desc_add(kdesc0, (uint32_t)(base % C::STAGES) * C::TILE_BYTES);
+        const uint64_t kd = kdesc0 + (((uint32_t)(base % C::STAGES) * C::TILE_BYTES) >> 4);
         if (nA > 0) {
-          issue_qk<D>(tmem, qd0, kd);
-          tc_commit(ctl.bar(T_S_FULL0));
+          issue_qk_warp<D>(tmem, qd0, kd);
+          tc_commit_warp(ctl.bar(T_S_FULL0));
         }
         if (nB > 0) {
-          issue_qk<D>(tmem + 128u, qd1, kd);
-          tc_commit(ctl.bar(T_S_FULL1));
+          issue_qk_warp<D>(tmem + 128u, qd1, kd);
+          tc_commit_warp(ctl.bar(T_S_FULL1));
         }
-        ring_release<C::STAGES>(ctl, base);
+        tc_commit_warp(ring_empty<C::STAGES>(ctl, base));   // K_0 read by both prologue QKs
+        // The Q buffer is free once the unit's last QK has run (the prologue's
+        // when it has one step, else those of step n - 2).
+        if (n == 1) tc_commit_warp(ctl.bar(T_Q_EMPTY0 + qb));
         for (int j = 0; ok && j < n; ++j) {
-          bool v_ready = false, k_ready = false;
-          ok = pv_then_qk<D, 0>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd0, base, j,
-                                nA, nB, st0, v_ready, k_ready, trb) &&
-               pv_then_qk<D, 1>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd1, base, j,
-                                nA, nB, st1, v_ready, k_ready, trb);
+          ok = tile_step<D, 0>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd0, base, j,
+                               nA, nB, st0, trb) &&
+               tile_step<D, 1>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd1, base, j,
+                               nA, nB, st1, trb);
+          if (ok && j == n - 2) tc_commit_warp(ctl.bar(T_Q_EMPTY0 + qb));
         }
         if (!ok) break;
         if (nA > 0) ++st0.nunits;
         if (nB > 0) ++st1.nunits;
-        tc_commit(ctl.bar(T_Q_EMPTY0 + qb));   // Q buffer free once its QKs are done
         base += 2 * n;
       }
-      tc_commit(ctl.bar(T_DRAIN));   // no MMA may be in flight at teardown
+      tc_commit_warp(ctl.bar(T_DRAIN));   // no MMA may be in flight at teardown
       wait_drain(ctl.bar(T_DRAIN), 0, p.timeout_ns);
-      ATTN_TRACE_SM_FLUSH(trb, 0);
+      if (lane == 0) ATTN_TRACE_SM_FLUSH(trb, 0);
+    }
+    __syncwarp();
+   } else if (warp == WARP_WATCH) {
+    // ---------------- K/V watcher (one thread): adds one arrival to P_FULL_X(j)
+    // once V_j and, if tile X computes S(j+1), K_{j+1} have landed, so that
+    // the MMA issuer waits for P_FULL alone.  It arrives for step j only after
+    // the phase of step j - 1 has completed, so that an early arrival never
+    // counts towards the previous phase.
+    if (lane == 0) {
+      long long base = 0;         // ring position of the unit's K_0
+      long long gx[2] = {0, 0};   // P_FULL_X phases arrived at so far
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        UnitInfo t;
+        if (!(ok = read_unit(ctl, k, t, abort_flag, p.timeout_ns))) break;
+        mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
+        if (!t.valid) break;
+        const int n = max(t.n[0], t.n[1]);
+        for (int j = 0; ok && j < n; ++j) {
+          const long long v_pos = base + 2 * j + 1, k_pos = v_pos + 1;
+          ok = wait_bounded(ring_full<C::STAGES>(ctl, v_pos), ring_parity<C::STAGES>(v_pos),
+                            abort_flag, p.timeout_ns);
+          for (int x = 0; ok && x < 2; ++x) {
+            if (j >= t.n[x]) continue;
+            if (j + 1 < t.n[x])
+              ok = wait_bounded(ring_full<C::STAGES>(ctl, k_pos), ring_parity<C::STAGES>(k_pos),
+                                abort_flag, p.timeout_ns);
+            if (ok && gx[x] > 0)
+              ok = wait_bounded(ctl.bar(T_P_FULL0 + x), (uint32_t)(gx[x] - 1) & 1u, abort_flag,
+                                p.timeout_ns);
+            if (ok) {
+              mbar_arrive(ctl.bar(T_P_FULL0 + x));
+              ++gx[x];
+            }
+          }
+        }
+        base += 2 * n;
+      }
     }
     __syncwarp();
    }
@@ -433,7 +512,8 @@ __global__ void __launch_bounds__(THREADS2, 1)
     const uint32_t s_t = tmem + lane_off + 128u * (uint32_t)x;
     const uint32_t o_t = tmem + lane_off + C::COL_O + (uint32_t)(D * x);
     const float c = p.scale_log2;
-    long long g = 0;   // key steps of tile x so far (S_FULL, P_FULL, PV_DONE phases)
+    long long g = 0;   // key steps of tile x so far (S_FULL and P_FULL phases)
+    int units_x = 0;   // units in which tile x had work (PV_DONE phases)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       UnitInfo t;
@@ -522,8 +602,9 @@ __global__ void __launch_bounds__(THREADS2, 1)
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE; then O_x is free for the next unit
-      ok = wait_warp(ctl.bar(T_PV_DONE0 + x), (uint32_t)(g - 1) & 1u, abort_flag, p.timeout_ns);
+      ok = wait_warp(ctl.bar(T_PV_DONE0 + x), (uint32_t)units_x & 1u, abort_flag, p.timeout_ns);
       if (!ok) break;
+      ++units_x;
       tc_fence_after();
       const bool live = q_idx < t.len;
       const float m_use = (m == -INFINITY) ? 0.f : m;

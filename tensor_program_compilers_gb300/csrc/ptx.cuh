@@ -63,6 +63,28 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of three mbarrier phases in one shared-memory round trip
+// (the three tests issue back to back, before any result is consumed): bit i
+// of the result is set when barrier i has completed the phase of parity pi.
+__device__ __forceinline__ uint32_t mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1,
+                                               uint32_t p1, uint32_t b2, uint32_t p2) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t.reg .b32 t0, t1, t2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "selp.b32 t0, 1, 0, q0;\n\t"
+      "selp.b32 t1, 2, 0, q1;\n\t"
+      "selp.b32 t2, 4, 0, q2;\n\t"
+      "or.b32 t0, t0, t1;\n\t"
+      "or.b32 %0, t0, t2;\n\t}\n"
+      : "=r"(r)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return r;
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled bulk-tensor load into shared memory, completing on `bar`.
 // Coordinates are in elements, innermost first.
@@ -144,6 +166,40 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective forms of the three: every lane of a converged warp executes
+// them with the same operands and one elected lane issues the instruction.
+// An issuing thread that shares its sub-partition with busy warps keeps its
+// issue rate this way (its operand arithmetic is warp-uniform), where a lone
+// lane of a diverged warp was measured to fall far behind the tensor core.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          bar)
       : "memory");
 }
 
