@@ -224,14 +224,13 @@ template <int D, int X>
 __device__ __forceinline__ bool tile_step(const Ctl2 &ctl, volatile uint32_t *abort_flag,
                                           unsigned long long timeout_ns, uint32_t tmem,
                                           uint64_t kdesc0, uint64_t vdesc0, uint64_t qdesc,
-                                          long long base, int j, int nA, int nB,
+                                          int v_slot, int k_slot, int j, int nA, int nB,
                                           IssueState &st, volatile unsigned *trb) {
   using C = Cfg2<D>;
   constexpr uint32_t IDESC_PV = idesc_bf16_f32(D, 1);
   (void)trb;
   const int nx = X ? nB : nA;
   if (j >= nx) return true;
-  const long long v_pos = base + 2 * j + 1, k_pos = base + 2 * j + 2;
   const bool has_qk = j + 1 < nx;
   const bool last_user = X == 1 || j >= nB;   // B's MMAs come last in a step
   if (j == 0 && st.nunits > 0 &&
@@ -242,21 +241,20 @@ __device__ __forceinline__ bool tile_step(const Ctl2 &ctl, volatile uint32_t *ab
     return false;
   ATTN_TRACE_SM(trb, st.npv, 3 * X);
   tc_fence_after();
-  const uint64_t vdesc = vdesc0 + (((uint32_t)(v_pos % C::STAGES) * C::TILE_BYTES) >> 4);
+  const uint64_t vdesc = vdesc0 + (((uint32_t)v_slot * C::TILE_BYTES) >> 4);
   const uint32_t s_x = tmem + 128u * X;
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
     mma_ts_warp(tmem + C::COL_O + (uint32_t)(D * X), s_x + kk * 8, vdesc + (kk * 2048 >> 4),
                 IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
   if (!has_qk) tc_commit_warp(ctl.bar(T_PV_DONE0 + X));   // the tile's last PV: O_X is final
-  if (last_user) tc_commit_warp(ring_empty<C::STAGES>(ctl, v_pos));   // V_j's last use
+  if (last_user) tc_commit_warp(ctl.bar(T_RING + C::STAGES + v_slot));   // V_j's last use
   ATTN_TRACE_SM(trb, st.npv, 3 * X + 1);
   ++st.npv;
   if (has_qk) {   // QK_X(j+1)
-    issue_qk_warp<D>(s_x, qdesc,
-                     kdesc0 + (((uint32_t)(k_pos % C::STAGES) * C::TILE_BYTES) >> 4));
+    issue_qk_warp<D>(s_x, qdesc, kdesc0 + (((uint32_t)k_slot * C::TILE_BYTES) >> 4));
     tc_commit_warp(ctl.bar(T_S_FULL0 + X));
-    if (last_user) tc_commit_warp(ring_empty<C::STAGES>(ctl, k_pos));   // K_{j+1}'s last use
+    if (last_user) tc_commit_warp(ctl.bar(T_RING + C::STAGES + k_slot));   // K_{j+1}'s last use
     ATTN_TRACE_SM(trb, st.npv, 3 * X + 2);
   }
   return true;
@@ -446,12 +444,17 @@ __global__ void __launch_bounds__(THREADS2, 1)
         // The Q buffer is free once the unit's last QK has run (the prologue's
         // when it has one step, else those of step n - 2).
         if (n == 1) tc_commit_warp(ctl.bar(T_Q_EMPTY0 + qb));
+        // ring slots of V_j and K_{j+1} (positions base + 2j + 1, + 2), kept
+        // as 32-bit counters rather than recomputed from 64-bit positions
+        int v_slot = (int)((base + 1) % C::STAGES);
         for (int j = 0; ok && j < n; ++j) {
-          ok = tile_step<D, 0>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd0, base, j,
-                               nA, nB, st0, trb) &&
-               tile_step<D, 1>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd1, base, j,
-                               nA, nB, st1, trb);
+          const int k_slot = v_slot + 1 == C::STAGES ? 0 : v_slot + 1;
+          ok = tile_step<D, 0>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd0, v_slot,
+                               k_slot, j, nA, nB, st0, trb) &&
+               tile_step<D, 1>(ctl, abort_flag, p.timeout_ns, tmem, kdesc0, vdesc0, qd1, v_slot,
+                               k_slot, j, nA, nB, st1, trb);
           if (ok && j == n - 2) tc_commit_warp(ctl.bar(T_Q_EMPTY0 + qb));
+          v_slot = k_slot + 1 == C::STAGES ? 0 : k_slot + 1;
         }
         if (!ok) break;
         if (nA > 0) ++st0.nunits;
