@@ -160,6 +160,28 @@ __device__ __forceinline__ float exp_row(const float (&h0)[HB], const float (&h1
   return sum_acc(acc);
 }
 
+// The row's 128 scores (TMEM columns col..col+127 of this thread's lane):
+// four loads, one wait.
+__device__ __forceinline__ void load_row(uint32_t taddr, float (&h0)[HB], float (&h1)[HB]) {
+  uint32_t a[32], b[32], c[32], d[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld32(taddr + 64, c);
+  tmem_ld32(taddr + 96, d);
+  tmem_wait_ld();
+  reg_fence32(a);
+  reg_fence32(b);
+  reg_fence32(c);
+  reg_fence32(d);
+#pragma unroll
+  for (int x = 0; x < 32; ++x) {
+    h0[x] = __uint_as_float(a[x]);
+    h0[32 + x] = __uint_as_float(b[x]);
+    h1[x] = __uint_as_float(c[x]);
+    h1[32 + x] = __uint_as_float(d[x]);
+  }
+}
+
 // Sum of the row's 128 bf16 weights exactly as P.V uses them.
 __device__ __forceinline__ float sum_rounded(const uint32_t (&pk0)[HB / 2],
                                              const uint32_t (&pk1)[HB / 2]) {
@@ -473,8 +495,17 @@ __global__ void __launch_bounds__(THREADS2, 1)
     // the phase of step j - 1 has completed, so that an early arrival never
     // counts towards the previous phase.
     if (lane == 0) {
-      long long base = 0;         // ring position of the unit's K_0
-      long long gx[2] = {0, 0};   // P_FULL_X phases arrived at so far
+      // ring position of the next load as (slot, fill parity), advanced one
+      // position at a time
+      int slot = 0;
+      uint32_t par = 0;
+      const auto advance = [&]() {
+        if (++slot == C::STAGES) {
+          slot = 0;
+          par ^= 1u;
+        }
+      };
+      uint32_t gx[2] = {0, 0};   // P_FULL_X phases arrived at so far
       bool ok = true;
       for (int k = 0; ok; ++k) {
         UnitInfo t;
@@ -482,25 +513,27 @@ __global__ void __launch_bounds__(THREADS2, 1)
         mbar_arrive(ctl.bar(T_INFO_EMPTY0 + k % INFO_SLOTS));
         if (!t.valid) break;
         const int n = max(t.n[0], t.n[1]);
+        advance();   // K_0
         for (int j = 0; ok && j < n; ++j) {
-          const long long v_pos = base + 2 * j + 1, k_pos = v_pos + 1;
-          ok = wait_bounded(ring_full<C::STAGES>(ctl, v_pos), ring_parity<C::STAGES>(v_pos),
-                            abort_flag, p.timeout_ns);
+          // V_j at (slot, par); K_{j+1} at the next position
+          const int v_slot = slot, k_slot = slot + 1 == C::STAGES ? 0 : slot + 1;
+          const uint32_t v_par = par, k_par = k_slot == 0 ? par ^ 1u : par;
+          ok = wait_bounded(ctl.bar(T_RING + v_slot), v_par, abort_flag, p.timeout_ns);
           for (int x = 0; ok && x < 2; ++x) {
             if (j >= t.n[x]) continue;
             if (j + 1 < t.n[x])
-              ok = wait_bounded(ring_full<C::STAGES>(ctl, k_pos), ring_parity<C::STAGES>(k_pos),
-                                abort_flag, p.timeout_ns);
+              ok = wait_bounded(ctl.bar(T_RING + k_slot), k_par, abort_flag, p.timeout_ns);
             if (ok && gx[x] > 0)
-              ok = wait_bounded(ctl.bar(T_P_FULL0 + x), (uint32_t)(gx[x] - 1) & 1u, abort_flag,
+              ok = wait_bounded(ctl.bar(T_P_FULL0 + x), (gx[x] - 1u) & 1u, abort_flag,
                                 p.timeout_ns);
             if (ok) {
               mbar_arrive(ctl.bar(T_P_FULL0 + x));
               ++gx[x];
             }
           }
+          advance();   // V_j
+          if (j + 1 < n) advance();   // K_{j+1}
         }
-        base += 2 * n;
       }
     }
     __syncwarp();
@@ -545,8 +578,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
         const int kb = j * BN;
         const bool masked = kb + BN > t.len || (p.causal && kb + BN - 1 > r0);
         float h0[HB], h1[HB];
-        load_half(s_t, h0);
-        load_half(s_t + HB, h1);
+        load_row(s_t, h0, h1);
         if (masked) {
           mask_half(h0, kb, 0, lim);
           mask_half(h1, kb + HB, 0, lim);
@@ -576,8 +608,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
           if (again || !__any_sync(0xffffffffu, need)) break;
           again = true;
           want = need;
-          load_half(s_t, h0);
-          load_half(s_t + HB, h1);
+          load_row(s_t, h0, h1);
           if (masked) {
             mask_half(h0, kb, 0, lim);
             mask_half(h1, kb + HB, 0, lim);
