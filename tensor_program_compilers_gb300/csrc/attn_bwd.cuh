@@ -251,6 +251,18 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
            (accumulate || h > 0 || kk > 0) ? 1u : 0u);
 }
 
+// issue_pv_half for an issuing warp (every lane, one elected lane issues).
+template <int D>
+__device__ __forceinline__ void issue_pv_half_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint64_t bdesc, int h, bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(D, 1);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts_warp(d_tmem, a_tmem + 64u * (uint32_t)h + 8u * (uint32_t)kk,
+                bdesc + (uint64_t)(((4 * h + kk) * 2048) >> 4), IDESC,
+                (accumulate || h > 0 || kk > 0) ? 1u : 0u);
+}
+
 // Epilogue of one accumulator row: NCOLS fp32 columns * mul -> bf16, 16-byte
 // stores (if live).
 template <int NCOLS>
@@ -362,10 +374,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    // MMA issuer: the whole warp runs the loop, one elected lane issues each
+    // tcgen05 instruction (a lone lane sharing its sub-partition with two
+    // softmax warps issues far more slowly)
+    {
       const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
       const uint64_t vdesc = smem_desc_sw128(v_s, 16, 1024);
-      bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      bool ok = wait_warp(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
       // Per step s: S^T(s) and dP^T(s) in full; dV += P^T(s) dO once the
       // softmax warps have written P^T; then S^T(s+1) (S^T's columns are
       // free once dV(s) has read P^T: one thread's MMAs run in issue order)
@@ -373,12 +388,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // dP^T(s+1).  So the next scores are computed while dS is formed.
       const uint32_t ring = base + C::A_OFF_RING;
       if (ok && steps > 0 &&
-          (ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+          (ok = wait_warp(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
         tc_fence_after();
-        issue_qk<D>(tmem + COL_ST, kdesc, smem_desc_sw128(ring, 16, 1024));
-        tc_commit(ctl.bar(B_ST_FULL));
-        issue_qk<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(ring + C::TILE, 16, 1024));
-        tc_commit(ctl.bar(B_DPT_FULL));
+        issue_qk_warp<D>(tmem + COL_ST, kdesc, smem_desc_sw128(ring, 16, 1024));
+        tc_commit_warp(ctl.bar(B_ST_FULL));
+        issue_qk_warp<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(ring + C::TILE, 16, 1024));
+        tc_commit_warp(ctl.bar(B_DPT_FULL));
       }
       for (int s = 0; ok && s < steps; ++s) {
         const int slot = s & 1;
@@ -386,33 +401,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t q_n = ring + (slot ^ 1) * C::A_SLOT;   // the next step's slot
         const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
         const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
-        if (!(ok = wait_bounded(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        if (!(ok = wait_warp(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
-        issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
-        issue_pv_half<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
         const bool more = s + 1 < steps;
         if (more) {
-          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
+          if (!(ok = wait_warp(ctl.bar(B_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
                                   abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_qk<D>(tmem + COL_ST, kdesc, smem_desc_sw128(q_n, 16, 1024));
-          tc_commit(ctl.bar(B_ST_FULL));
+          issue_qk_warp<D>(tmem + COL_ST, kdesc, smem_desc_sw128(q_n, 16, 1024));
+          tc_commit_warp(ctl.bar(B_ST_FULL));
         }
-        if (!(ok = wait_bounded(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        if (!(ok = wait_warp(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
-        issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, s > 0);
-        issue_pv_half<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 1, s > 0);
-        tc_commit(ctl.bar(B_EMPTY0 + slot));   // Q(s), dO(s) and their rows are read
+        issue_pv_half_warp<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 1, s > 0);
+        tc_commit_warp(ctl.bar(B_EMPTY0 + slot));   // Q(s), dO(s) and their rows are read
         if (more) {
-          issue_qk<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(q_n + C::TILE, 16, 1024));
-          tc_commit(ctl.bar(B_DPT_FULL));
+          issue_qk_warp<D>(tmem + COL_DPT, vdesc, smem_desc_sw128(q_n + C::TILE, 16, 1024));
+          tc_commit_warp(ctl.bar(B_DPT_FULL));
         }
       }
-      if (ok) tc_commit(ctl.bar(B_DONE));
-      tc_commit(ctl.bar(B_DRAIN));
+      if (ok) tc_commit_warp(ctl.bar(B_DONE));
+      tc_commit_warp(ctl.bar(B_DRAIN));
       wait_drain(ctl.bar(B_DRAIN), 0, p.timeout_ns);
     }
     __syncwarp();
@@ -621,10 +636,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    // MMA issuer: the whole warp, one elected lane issues (as in the dK/dV kernel)
+    {
       const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
       const uint64_t dodesc = smem_desc_sw128(do_s, 16, 1024);
-      bool ok = wait_bounded(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
+      bool ok = wait_warp(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
       // Per step s: S(s) and dP(s) in full; S(s+1) as soon as the softmax
       // warps have read S(s) (P is no operand here); dQ += dS(s) K once they
       // have written dS over dP(s); then dP(s+1) (dP's columns are free once
@@ -632,49 +648,49 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // is released when its dP product is done, a K slot after dQ.
       const uint32_t kring = base + C::B_OFF_K, vring = base + C::B_OFF_V;
       if (ok && steps > 0 &&
-          (ok = wait_bounded(ctl.bar(B_KFULL0), 0, abort_flag, p.timeout_ns))) {
+          (ok = wait_warp(ctl.bar(B_KFULL0), 0, abort_flag, p.timeout_ns))) {
         tc_fence_after();
-        issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring, 16, 1024));
-        tc_commit(ctl.bar(B_ST_FULL));
-        if ((ok = wait_bounded(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
+        issue_qk_warp<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring, 16, 1024));
+        tc_commit_warp(ctl.bar(B_ST_FULL));
+        if ((ok = wait_warp(ctl.bar(B_FULL0), 0, abort_flag, p.timeout_ns))) {
           tc_fence_after();
-          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring, 16, 1024));
-          tc_commit(ctl.bar(B_DPT_FULL));
-          tc_commit(ctl.bar(B_EMPTY0));   // V(0) is read
+          issue_qk_warp<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring, 16, 1024));
+          tc_commit_warp(ctl.bar(B_DPT_FULL));
+          tc_commit_warp(ctl.bar(B_EMPTY0));   // V(0) is read
         }
       }
       for (int s = 0; ok && s < steps; ++s) {
         const int ks = s % C::K_STAGES, kn = (s + 1) % C::K_STAGES, vn = (s + 1) % C::V_STAGES;
         const bool more = s + 1 < steps;
-        if (!(ok = wait_bounded(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        if (!(ok = wait_warp(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         if (more) {
-          if (!(ok = wait_bounded(ctl.bar(B_KFULL0 + kn), (uint32_t)((s + 1) / C::K_STAGES) & 1u,
+          if (!(ok = wait_warp(ctl.bar(B_KFULL0 + kn), (uint32_t)((s + 1) / C::K_STAGES) & 1u,
                                   abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_qk<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring + kn * C::TILE, 16, 1024));
-          tc_commit(ctl.bar(B_ST_FULL));
+          issue_qk_warp<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring + kn * C::TILE, 16, 1024));
+          tc_commit_warp(ctl.bar(B_ST_FULL));
         }
-        if (!(ok = wait_bounded(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        if (!(ok = wait_warp(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
         const uint64_t k_mn = smem_desc_sw128(kring + ks * C::TILE, CHUNK_BYTES, 1024);
-        issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 0, s > 0);
-        issue_pv_half<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 1, s > 0);
-        tc_commit(ctl.bar(B_KEMPTY0 + ks));   // K(s) is read
+        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 0, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 1, s > 0);
+        tc_commit_warp(ctl.bar(B_KEMPTY0 + ks));   // K(s) is read
         if (more) {
-          if (!(ok = wait_bounded(ctl.bar(B_FULL0 + vn), (uint32_t)((s + 1) / C::V_STAGES) & 1u,
+          if (!(ok = wait_warp(ctl.bar(B_FULL0 + vn), (uint32_t)((s + 1) / C::V_STAGES) & 1u,
                                   abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
-          issue_qk<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
-          tc_commit(ctl.bar(B_DPT_FULL));
-          tc_commit(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
+          issue_qk_warp<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
+          tc_commit_warp(ctl.bar(B_DPT_FULL));
+          tc_commit_warp(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
         }
       }
-      if (ok) tc_commit(ctl.bar(B_DONE));
-      tc_commit(ctl.bar(B_DRAIN));
+      if (ok) tc_commit_warp(ctl.bar(B_DONE));
+      tc_commit_warp(ctl.bar(B_DRAIN));
       wait_drain(ctl.bar(B_DRAIN), 0, p.timeout_ns);
     }
     __syncwarp();

@@ -829,6 +829,20 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qdesc, uint64
   }
 }
 
+// issue_qk for an issuing warp: every lane runs it with the same operands and
+// one elected lane issues each MMA (descriptor offsets as plain integer
+// additions: the 14-bit address field cannot carry, shared addresses stay
+// below 256 KB).
+template <int D>
+__device__ __forceinline__ void issue_qk_warp(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BN, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t koff = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
+    mma_ss_warp(d_tmem, qdesc + koff, kdesc + koff, IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+
 // O (+)= P V_j: A = P from TMEM (bf16 pairs), B = V tile (vdesc) with keys as
 // K and the head dim as N (N contiguous: 64-wide swizzle atoms CHUNK_BYTES
 // apart, 8-key groups 1024 bytes apart, 16 keys = 2048 bytes per step).

@@ -216,18 +216,6 @@ struct IssueState {
   int nunits;      // units in which tile X had work (O_FREE_X and PV_DONE_X phases)
 };
 
-// Q K_j^T into S (tmem d_tmem), issued by the whole MMA warp (qdesc, kdesc: the
-// 128-row Q and K tiles, K-major, 128-byte swizzle, 64-column chunks).
-template <int D>
-__device__ __forceinline__ void issue_qk_warp(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
-  constexpr uint32_t IDESC = idesc_bf16_f32(BN, 0);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t koff = ((kk >> 2) * CHUNK_BYTES + (kk & 3) * 32) >> 4;
-    mma_ss_warp(d_tmem, qdesc + koff, kdesc + koff, IDESC, kk > 0 ? 1u : 0u);
-  }
-}
-
 // Tile X's share of key step j of a unit: PV_X(j) (O_X (+)= P_X(j) V_j; the
 // unit's first overwrites O_X, after the previous epilogue has read it), then
 // QK_X(j+1).  K_j sits at ring position base + 2j, V_j at base + 2j + 1.
