@@ -264,20 +264,56 @@ def launch_floor_us(dev, flush):
     return round(statistics.median(ts), 2)
 
 
-def secondary_rooflines(wl, rr, ms, hbm_gbs, floor_us):
+def dram_latency_us(pkg, dev, hops=20000, reps=3):
+    """Latency of one load that misses the L2, from a one-thread pointer chase
+    over a 512 MiB chain (tang, section 9.2: the latency term of the time
+    floor); median of `reps` chases."""
+    import torch
+    scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    result = torch.zeros(2, dtype=torch.int64, device=dev)
+    ns = []
+    for _ in range(reps):
+        pkg.attn_probe_dram_latency(scratch, scratch.numel(), hops, result)
+        torch.cuda.synchronize(dev)
+        ns.append(int(result[0].item()) / hops)
+    del scratch
+    return round(statistics.median(ns) / 1e3, 4)
+
+
+def work_units(wl, lens):
+    """Work units (256 query rows of one sequence and head) a forward launch
+    of this workload schedules: the W of the time floor's wave term."""
+    return sum((L + 255) // 256 for L in lens) * wl.Hq
+
+
+def secondary_rooflines(wl, rr, ms, hbm_gbs, floor_us, lat_us=None, peak=None, sms=152):
     """The bounds that matter for the short workloads: the minimum HBM bytes
     (Q, K, V read once, O and LSE written once) against the copy bandwidth,
     the exponentials (one per visible score, FLOPs / 4d) against the MUFU
-    rate, and the time against the launch floor."""
+    rate, the time against the launch floor, and the time floor of tang,
+    section 9.2, read as
+        T >= t_launch + max(t_lat + bytes / BW, flops / peak, ceil(W / W_res) t_lat)
+    with W the launch's work units and W_res one per SM."""
     inp = rr["inp"]
     rows = inp.total_rows
     nbytes = rows * (2 * wl.Hq + 2 * wl.Hkv) * wl.d * 2 + rows * wl.Hq * 4
     gbs = nbytes / (ms / 1e3) / 1e9
     ex2 = rr["flops"] / (4 * wl.d) / (ms / 1e3)
-    return {"us": round(ms * 1e3, 2), "launch_floor_us": floor_us, "min_bytes": nbytes,
-            "hbm_gbs": round(gbs, 1),
-            "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
-            "exp2_per_s": float(f"{ex2:.4g}"), "frac_of_mufu": round(ex2 / MUFU_EX2_PER_S, 4)}
+    out = {"us": round(ms * 1e3, 2), "launch_floor_us": floor_us, "min_bytes": nbytes,
+           "hbm_gbs": round(gbs, 1),
+           "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None,
+           "exp2_per_s": float(f"{ex2:.4g}"), "frac_of_mufu": round(ex2 / MUFU_EX2_PER_S, 4)}
+    if lat_us is not None and hbm_gbs and peak:
+        waves = -(-work_units(wl, inp.lens) // sms)
+        terms = {"lat_plus_bytes": lat_us + nbytes / (hbm_gbs * 1e9) * 1e6,
+                 "flops": rr["flops"] / (peak * 1e12) * 1e6,
+                 "waves_lat": waves * lat_us}
+        floor = floor_us + max(terms.values())
+        out.update({"dram_latency_us": lat_us, "waves": waves,
+                    "time_floor_us": round(floor, 2),
+                    "time_floor_terms_us": {k: round(v, 3) for k, v in terms.items()},
+                    "x_floor": round(ms * 1e3 / floor, 2)})
+    return out
 
 
 def time_steps(step, steps, warmup, flush, stream):
@@ -456,6 +492,75 @@ def run_e2e(pkg, W, wl, inp, dev, steps):
     return dict(ms=ms, steps=steps, flops=flops, h2d=h2d, d2h=d2h)
 
 
+def run_e2e_pipelined(pkg, W, wl, inp, dev, steps):
+    """The e2e measurement with step i+1's host-to-device copies and step i-1's
+    device-to-host read overlapping step i's forward: two sets of device
+    buffers and pinned host outputs, one stream each for the copies in, the
+    forward and the copies out, ordered by events (a set is refilled only
+    after its forward ran, an output set rewritten only after it was read
+    back).  Every step still copies its own Q, K, V in and its O, LSE out;
+    the interval runs from the first copy in to the last copy out."""
+    import torch
+    qh, kh, vh = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    lse_shape = (wl.Hq, inp.n_arg) if wl.varlen else (wl.B, wl.Hq, wl.N)
+    sets = []
+    for _ in range(2):
+        q, k, v = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+        sets.append(dict(q=q, k=k, v=v, o=torch.empty_like(q),
+                         lse=torch.empty(lse_shape, dtype=torch.float32, device=dev),
+                         oh=torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                         lh=torch.empty(lse_shape, dtype=torch.float32).pin_memory()))
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    ran = [None, None]     # forward of the set's last step done (inputs free)
+    read = [None, None]    # read-back of the set's last step done (outputs free)
+
+    def step(i):
+        b = sets[i & 1]
+        with torch.cuda.stream(s_in):
+            if ran[i & 1] is not None:
+                s_in.wait_event(ran[i & 1])
+            b["q"].copy_(qh, non_blocking=True)
+            b["k"].copy_(kh, non_blocking=True)
+            b["v"].copy_(vh, non_blocking=True)
+            loaded = ev()
+            loaded.record(s_in)
+        s_run.wait_event(loaded)
+        if read[i & 1] is not None:
+            s_run.wait_event(read[i & 1])
+        pkg.attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], wl.B, wl.Hq, wl.Hkv, inp.n_arg,
+                     wl.d, wl.scale, wl.causal, cu, stream=s_run.cuda_stream)
+        done = ev()
+        done.record(s_run)
+        ran[i & 1] = done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            b["oh"].copy_(b["o"], non_blocking=True)
+            b["lh"].copy_(b["lse"], non_blocking=True)
+            back = ev()
+            back.record(s_out)
+        read[i & 1] = back
+
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(s_in)
+    for i in range(steps):
+        step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    flops = W.causal_flops(wl, inp.lens)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = sets[0]["oh"].numel() * 2 + sets[0]["lh"].numel() * 4
+    return dict(ms=ms, steps=steps, flops=flops, h2d=h2d, d2h=d2h)
+
+
 def cpu_baseline(W, wl, inp, target_s=12.0):
     """The fp64 oracle, as it stands, on a bounded seeded row sample of the
     same workload, timed on this host's cores."""
@@ -522,16 +627,26 @@ def native(args):
 
     e2e = None
     if not args.no_e2e:
-        r = run_e2e(pkg, W, wl, res["inp"], dev, args.e2e_steps)
+        r = run_e2e_pipelined(pkg, W, wl, res["inp"], dev, args.e2e_steps)
         e_max = reduce_max(r["ms"] / 1e3, dev)
         e_flops = reduce_sum(r["flops"] * r["steps"], dev)
+        rs = run_e2e(pkg, W, wl, res["inp"], dev, args.e2e_steps)
+        s_max = reduce_max(rs["ms"] / 1e3, dev)
         e2e = {"value": whole_job_rate(e_flops, e_max) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-               "steps": r["steps"], "ms_per_step": e_max * 1e3 / r["steps"]}
+               "steps": r["steps"], "ms_per_step": e_max * 1e3 / r["steps"],
+               "how": "copies in of step i+1 and out of step i-1 overlap the forward of "
+                      "step i (three streams, two buffer sets)",
+               "serial": {"value": whole_job_rate(reduce_sum(rs["flops"] * rs["steps"], dev),
+                                                  s_max) / 1e12,
+                          "ms_per_step": s_max * 1e3 / rs["steps"],
+                          "how": "copy in, forward, copy out in order on one stream"}}
 
     per_workload = {}
     if not args.no_per_workload:
         floor_us = launch_floor_us(dev, flush)
+        lat_us = dram_latency_us(pkg, dev)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
         for key, other in W.BY_KEY.items():
             if key == args.workload:
                 continue
@@ -540,8 +655,10 @@ def native(args):
             tf = rr["flops"] / (ms / 1e3) / 1e12
             per_workload[key] = {"workload": other.name, "tflops": round(tf, 2),
                                  "ms_per_step": round(ms, 5), "frac_of_peak": round(tf / peak, 4),
+                                 "median_ms": round(statistics.median(rr["per_ms"]), 5),
+                                 "min_ms": round(min(rr["per_ms"]), 5),
                                  **secondary_rooflines(other, rr, ms, peaks.get("hbm_gbs"),
-                                                       floor_us)}
+                                                       floor_us, lat_us, peak, sms)}
             del rr
         per_workload["window"] = run_window(pkg, dev, flush, min(args.steps, 20))
         per_workload["decode"] = run_decode(pkg, dev, flush, min(args.steps, 20),
@@ -629,7 +746,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=["ragged", "gqa", "d256", "block", "tiny"],
                     default="ragged")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -290,6 +290,24 @@ const char *attn_status_string(attn_status s);
  */
 attn_status attn_selftest_timeout(int timeout_us, cudaStream_t stream);
 
+/*
+ * attn_probe_dram_latency -- the DRAM-latency term of the time floor under
+ * a short launch (tang, section 9.2 "the time floor": launch overhead plus
+ * memory latency plus bytes over bandwidth, latency taken from a one-thread
+ * pointer chase).  Writes a chain of 8-byte indices into `scratch` (device,
+ * caller-owned, `bytes` long, 16-byte aligned; bytes >= 64 MiB so that the
+ * chain's start has left the L2 by the time it is chased) whose successive
+ * entries lie 4,160 bytes apart, then follows `hops` (1..1,000,000) of them
+ * with one thread, each load cached in L2 only, and writes to
+ * `result[0]` (device, caller-owned, two 8-byte words) the nanoseconds the
+ * chase took by the GPU's global timer and to result[1] the final index (so
+ * the loads cannot be elided).  Asynchronous on `stream`; scratch's contents
+ * are overwritten.  Errors: ATTN_ERR_INVALID_ARG for null pointers, bad
+ * sizes or hop counts, ATTN_ERR_ALIGNMENT, ATTN_ERR_CUDA for a failed launch.
+ */
+attn_status attn_probe_dram_latency(void *scratch, size_t bytes, int hops,
+                                    unsigned long long *result, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,7 +43,7 @@ EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace
             "attn_fwd_decode_paged", "attn_decode_paged_workspace_bytes",
             "attn_fwd_decode_static", "attn_bwd", "attn_bwd_workspace_bytes",
             "attn_get_status", "attn_status_string", "attn_selftest_timeout",
-            "attn_debug_one_tile"]
+            "attn_debug_one_tile", "attn_probe_dram_latency"]
 
 
 class AttnVariant(ctypes.Structure):
@@ -119,6 +119,8 @@ def _load():
         lib.attn_selftest_timeout.argtypes = [i, vp]
         lib.attn_debug_one_tile.restype = i
         lib.attn_debug_one_tile.argtypes = [i]
+        lib.attn_probe_dram_latency.restype = i
+        lib.attn_probe_dram_latency.argtypes = [vp, ctypes.c_size_t, i, vp, vp]
         _lib = lib
     return _lib
 
@@ -326,6 +328,18 @@ def attn_get_status(stream=None) -> int:
 
 def attn_selftest_timeout(timeout_us: int = 1000, stream=None) -> int:
     return _load().attn_selftest_timeout(int(timeout_us), _stream(stream))
+
+
+def attn_probe_dram_latency(scratch, nbytes: int, hops: int, result, stream=None,
+                            check=True) -> int:
+    """Call the C ``attn_probe_dram_latency``: chase ``hops`` links of a chain
+    written into ``scratch`` (device, ``nbytes``); ``result`` (device, two
+    uint64 words) receives the chase's nanoseconds and the final index."""
+    rc = _load().attn_probe_dram_latency(_ptr(scratch), int(nbytes), int(hops), _ptr(result),
+                                         _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_probe_dram_latency")
+    return rc
 
 
 def attn_debug_one_tile(on: bool) -> bool:

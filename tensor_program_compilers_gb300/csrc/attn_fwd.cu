@@ -1897,6 +1897,45 @@ extern "C" const char *attn_status_string(attn_status s) {
   return "ATTN_UNKNOWN_STATUS";
 }
 
+namespace attn {
+// Pointer chase for the latency term of the time floor: entry i holds the
+// index of the entry `stride` further on (mod n).
+__global__ void probe_init_kernel(unsigned long long *buf, unsigned long long n,
+                                  unsigned long long stride) {
+  for (unsigned long long i = blockIdx.x * (unsigned long long)blockDim.x + threadIdx.x; i < n;
+       i += (unsigned long long)gridDim.x * blockDim.x)
+    buf[i] = (i + stride) % n;
+}
+__global__ void probe_chase_kernel(const unsigned long long *buf, int hops,
+                                   unsigned long long *result) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  unsigned long long idx = 0;
+  const uint64_t t0 = globaltimer_ns();
+  for (int h = 0; h < hops; ++h) {
+    unsigned long long nxt;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(nxt) : "l"(buf + idx) : "memory");
+    idx = nxt;
+  }
+  const uint64_t t1 = globaltimer_ns();
+  result[0] = t1 - t0;
+  result[1] = idx;
+}
+}  // namespace attn
+
+extern "C" attn_status attn_probe_dram_latency(void *scratch, size_t bytes, int hops,
+                                               unsigned long long *result, cudaStream_t stream) {
+  if (!scratch || !result || hops < 1 || hops > 1000000 || bytes < (64ull << 20))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scratch) & 15u) || (reinterpret_cast<uintptr_t>(result) & 7u))
+    return ATTN_ERR_ALIGNMENT;
+  const unsigned long long n = bytes / 8, stride = 4160 / 8;
+  attn::probe_init_kernel<<<1024, 256, 0, stream>>>(static_cast<unsigned long long *>(scratch), n,
+                                                    stride);
+  attn::probe_chase_kernel<<<1, 32, 0, stream>>>(
+      static_cast<const unsigned long long *>(scratch), hops, result);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 extern "C" attn_status attn_selftest_timeout(int timeout_us, cudaStream_t stream) {
   if (timeout_us < 1 || timeout_us > 1000000) return ATTN_ERR_INVALID_ARG;
   int dev = 0;

@@ -74,6 +74,21 @@ def test_selftest_rejects_bad_limit(lib):
     assert pkg.attn_selftest_timeout(2_000_000, stream=0) == pkg.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("kw", [dict(scratch=None), dict(result=None), dict(hops=0),
+                                dict(hops=2_000_000), dict(nbytes=1 << 20)])
+def test_latency_probe_rejects_bad_arguments(lib, kw):
+    args = dict(scratch=0x10000, nbytes=512 << 20, hops=100, result=0x20000, stream=0)
+    args.update(kw)
+    assert pkg.attn_probe_dram_latency(check=False, **args) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_latency_probe_rejects_misaligned_buffers(lib):
+    assert pkg.attn_probe_dram_latency(0x10008, 512 << 20, 100, 0x20000, stream=0,
+                                       check=False) == pkg.ATTN_ERR_ALIGNMENT
+    assert pkg.attn_probe_dram_latency(0x10000, 512 << 20, 100, 0x20004, stream=0,
+                                       check=False) == pkg.ATTN_ERR_ALIGNMENT
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "absent.so"))
     monkeypatch.setattr(pkg, "_lib", None)

@@ -363,6 +363,22 @@ def _workload_check(wl, rows_per_head=None, heads=None):
     return compare(og, lg, oo, lo, wl.name + f" ({len(rows)} sampled rows)")
 
 
+@pytest.mark.gpu
+def test_dram_latency_probe_follows_the_chain():
+    """The probe walks `hops` links of a chain whose entry i points at
+    i + 520 (mod n): the final index is hops * 520 mod n, and a load that
+    misses the L2 takes between 100 ns and 5 us."""
+    n = (256 << 20) // 8
+    scratch = torch.empty(n * 8, dtype=torch.uint8, device="cuda")
+    result = torch.zeros(2, dtype=torch.int64, device="cuda")
+    hops = 5000
+    pkg.attn_probe_dram_latency(scratch, scratch.numel(), hops, result)
+    torch.cuda.synchronize()
+    assert pkg.attn_get_status() == pkg.ATTN_OK
+    assert int(result[1].item()) == (hops * 520) % n
+    assert 100 <= int(result[0].item()) / hops <= 5000
+
+
 def test_workload_tiny_full():
     print(_workload_check(W.TINY))
 
