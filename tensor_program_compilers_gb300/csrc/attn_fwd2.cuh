@@ -296,8 +296,17 @@ __global__ void __launch_bounds__(THREADS2, 1)
   constexpr uint32_t INFO_CONSUMERS = 1 + 8 + 1;   // the MMA issuer, the softmax warps, the watcher
   const int tslot = ATTN_TRACE_SLOT();          // -1 unless built for tracing
 
-  if (warp == WARP_MMA) {
+  // The producer sets up the barriers and sends its first unit's loads before
+  // the set-up barrier, so that their DRAM latency overlaps the TMEM
+  // allocation and the barrier (in a short launch after the L2 was flushed,
+  // the parameters, tensor maps and inputs all come from DRAM).
+  int primed = 0;           // producer lane 0: ring items of its first unit already issued
+  bool q_primed = false;    // producer lane 0: the first unit's Q already issued
+  if (warp == WARP_PROD) {
     if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
       for (int b = 0; b < 2; ++b) {
         mbar_init(ctl.bar(T_Q_FULL0 + b), 1);
         mbar_init(ctl.bar(T_Q_EMPTY0 + b), 1);
@@ -319,12 +328,30 @@ __global__ void __launch_bounds__(THREADS2, 1)
       mbar_init_fence();
     }
     __syncwarp();
+    const Tile t = decode_tile(p, blockIdx.x, false);   // the first unit (round 0)
+    if (t.valid && lane == 0) {
+      int nA = 0, nB = 0;
+      unit_steps(p.causal, t.unit, t.len, nA, nB);
+      const int kvh = t.h / p.group;
+      const int row0 = t.seq_start + UNIT_ROWS * t.unit;
+      const int tiles = nB > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(ctl.bar(T_Q_FULL0), C::TILE_BYTES * tiles);
+      for (int x = 0; x < tiles; ++x)
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(q_s + x * C::TILE_BYTES + c * CHUNK_BYTES, &tm_q, ctl.bar(T_Q_FULL0), c * 64,
+                      t.h, row0 + BM * x);
+      q_primed = true;
+      primed = min(2 * max(nA, nB), C::STAGES);   // ring slots start empty
+      for (int item = 0; item < primed; ++item) {
+        mbar_arrive_expect_tx(ctl.bar(T_RING + item), C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_3d(kv_s + item * C::TILE_BYTES + c * CHUNK_BYTES, (item & 1) ? &tm_v : &tm_k,
+                      ctl.bar(T_RING + item), c * 64, kvh, t.seq_start + (item >> 1) * BN);
+      }
+    }
+  } else if (warp == WARP_MMA) {
     tmem_alloc(smem_u32(ctl.words), TMEM_COLS);
     tmem_relinquish();
-  } else if (warp == WARP_PROD && lane == 0) {
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_k);
-    tma_prefetch_map(&tm_v);
   }
   tc_fence_before();
   __syncthreads();
@@ -335,8 +362,8 @@ __global__ void __launch_bounds__(THREADS2, 1)
    setmaxnreg_dec<REGS_OTHER>();
    if (warp == WARP_PROD) {
     // ---------------- producer: decode units, publish them, load Q and K/V
-    long long pos = 0;   // global ring position
-    int q_loads = 0;
+    long long pos = primed;        // global ring position (the primed items are issued)
+    int q_loads = q_primed ? 1 : 0;
     bool ok = true;
     long long round = 0;
     for (int k = 0; ok; ++k) {
@@ -372,7 +399,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
           if (k >= C::QB)
             ok = wait_bounded(ctl.bar(T_Q_EMPTY0 + qb), (uint32_t)(k / C::QB - 1) & 1u,
                               abort_flag, p.timeout_ns);
-          if (ok) {
+          if (ok && !(k == 0 && q_primed)) {
             const int tiles = nB > 0 ? 2 : 1;
             ++q_loads;
             mbar_arrive_expect_tx(ctl.bar(T_Q_FULL0 + qb), C::TILE_BYTES * tiles);
@@ -383,7 +410,7 @@ __global__ void __launch_bounds__(THREADS2, 1)
           }
           // K_0, V_0, K_1, V_1, ...
           const int n = max(nA, nB);
-          for (int item = 0; ok && item < 2 * n; ++item, ++pos) {
+          for (int item = k == 0 ? primed : 0; ok && item < 2 * n; ++item, ++pos) {
             const int slot = (int)(pos % C::STAGES);
             if (!(ok = wait_bounded(ctl.bar(T_RING + C::STAGES + slot),
                                     ((uint32_t)(pos / C::STAGES) & 1u) ^ 1u, abort_flag,
