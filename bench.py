@@ -421,13 +421,22 @@ def run_decode_paged(pkg, dev, flush, steps, hbm_gbs, page_size=16):
             "frac_of_hbm": round(gbs / hbm_gbs, 4) if hbm_gbs else None}
 
 
-def run_backward(pkg, dev, flush, steps):
-    """Backward of the GQA prefill workload (B2 Hq32 Hkv8 N4096 d128 causal):
-    dQ, dK, dV from the forward's O and LSE.  TFLOP/s under the usual
-    convention of 2.5x the forward's FLOPs (five products of the forward's
-    size; the kernels here compute seven, recomputing S and dP in both)."""
+BWD_SHAPES = {
+    # the GQA prefill workload's shape; the kernels compute seven products of
+    # the forward's size (S and dP recomputed in both kernels)
+    "backward": (2, 32, 8, 4096, 128),
+    # the long head-dim-256 prefill shape; three kernels (dV, dK, dQ) compute
+    # sixteen products of the forward's per-block size
+    "backward256": (1, 16, 2, 16384, 256),
+}
+
+
+def run_backward(pkg, dev, flush, steps, shape="backward"):
+    """Backward (dQ, dK, dV from the forward's O and LSE), causal, of one of
+    BWD_SHAPES.  TFLOP/s under the usual convention of 2.5x the forward's
+    FLOPs (five products of the forward's size)."""
     import torch
-    B, Hq, Hkv, N, d = 2, 32, 8, 4096, 128
+    B, Hq, Hkv, N, d = BWD_SHAPES[shape]
     g = torch.Generator().manual_seed(2004)
     q = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16).to(dev)
     k = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
@@ -666,6 +675,8 @@ def native(args):
         per_workload["decode_paged"] = run_decode_paged(pkg, dev, flush, min(args.steps, 20),
                                                         peaks.get("hbm_gbs"))
         per_workload["backward"] = run_backward(pkg, dev, flush, min(args.steps, 20))
+        per_workload["backward256"] = run_backward(pkg, dev, flush, min(args.steps, 10),
+                                                   "backward256")
 
     base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -752,7 +763,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows-per-head", type=int, default=24)
-    ap.add_argument("--extra", choices=["window", "decode", "decode_paged", "backward"],
+    ap.add_argument("--extra", choices=["window", "decode", "decode_paged", "backward",
+                                        "backward256"],
                     default=None,
                     help="time only this extra path (one JSON line; for profiling)")
     a = ap.parse_args(argv)
@@ -772,8 +784,8 @@ def extra_only(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.extra == "window":
         out = run_window(pkg, dev, flush, args.steps)
-    elif args.extra == "backward":
-        out = run_backward(pkg, dev, flush, args.steps)
+    elif args.extra in ("backward", "backward256"):
+        out = run_backward(pkg, dev, flush, args.steps, args.extra)
     elif args.extra == "decode_paged":
         out = run_decode_paged(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
     else:

@@ -238,7 +238,8 @@ attn_status attn_fwd_decode_static(const void *q, const void *k, const void *v, 
  *   lse      : the forward's fp32 LSE in its layout ([B, Hq, N] or [Hq, T]).
  *   N, cu_seqlens: as attn_fwd (packed: N = T, cu_seqlens device int32[B+1];
  *              bad offsets are reported as ATTN_ERR_BAD_SEQLENS).
- *   d        : 64 or 128.
+ *   d        : 64, 128 or 256 (256: dV, dK and dQ in three kernels, the
+ *              scores recomputed in each).
  *   workspace: caller-owned device memory of at least
  *              attn_bwd_workspace_bytes(B, Hq, N, cu_seqlens != NULL) bytes,
  *              16-byte aligned (per-row D and LSE log2(e), sequence

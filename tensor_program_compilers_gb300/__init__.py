@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 INCLUDE_DIR = os.path.join(_ROOT, "include")
 SOURCES = [os.path.join(_CSRC, "attn_fwd.cu")]
 DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(_CSRC, "attn_bwd.cuh"),
-                     os.path.join(_CSRC, "attn_fwd2.cuh"), os.path.join(INCLUDE_DIR, "attn.h")]
+                     os.path.join(_CSRC, "attn_fwd2.cuh"), os.path.join(_CSRC, "attn_bwd256.cuh"),
+                     os.path.join(INCLUDE_DIR, "attn.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

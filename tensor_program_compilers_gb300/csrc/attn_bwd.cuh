@@ -794,6 +794,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }  // namespace bwd
 }  // namespace attn
 
+#include "attn_bwd256.cuh"
+
 // ------------------------------------------------------------------ host
 namespace attn {
 namespace bwd {
@@ -818,7 +820,7 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   using namespace attn;
   using namespace attn::bwd;
   if (B < 0 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
@@ -848,7 +850,10 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
       if (!opt_in_smem(attn_bwd_dkdv_kernel<64>, BCfg<64>::A_SMEM) ||
           !opt_in_smem(attn_bwd_dkdv_kernel<128>, BCfg<128>::A_SMEM) ||
           !opt_in_smem(attn_bwd_dq_kernel<64>, BCfg<64>::B_SMEM) ||
-          !opt_in_smem(attn_bwd_dq_kernel<128>, BCfg<128>::B_SMEM))
+          !opt_in_smem(attn_bwd_dq_kernel<128>, BCfg<128>::B_SMEM) ||
+          !opt_in_smem(attn_bwd_dv256_kernel, B256::V_SMEM) ||
+          !opt_in_smem(attn_bwd_dk256_kernel, B256::K_SMEM) ||
+          !opt_in_smem(attn_bwd_dq256_kernel, B256::Q_SMEM))
         return ATTN_ERR_CUDA;
       ready[dev] = true;
     }
@@ -891,10 +896,15 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     bwd_rows_kernel<64><<<row_blocks, 256, 0, stream>>>(p);
     attn_bwd_dkdv_kernel<64><<<kv_units, BWD_THREADS, BCfg<64>::A_SMEM, stream>>>(mq, mdo, mk, mv, p);
     attn_bwd_dq_kernel<64><<<q_units, BWD_THREADS, BCfg<64>::B_SMEM, stream>>>(mq, mdo, mk, mv, p);
-  } else {
+  } else if (d == 128) {
     bwd_rows_kernel<128><<<row_blocks, 256, 0, stream>>>(p);
     attn_bwd_dkdv_kernel<128><<<kv_units, BWD_THREADS, BCfg<128>::A_SMEM, stream>>>(mq, mdo, mk, mv, p);
     attn_bwd_dq_kernel<128><<<q_units, BWD_THREADS, BCfg<128>::B_SMEM, stream>>>(mq, mdo, mk, mv, p);
+  } else {   // d = 256: dV, dK and dQ in three kernels (attn_bwd256.cuh)
+    bwd_rows_kernel<256><<<row_blocks, 256, 0, stream>>>(p);
+    attn_bwd_dv256_kernel<<<kv_units, BWD_THREADS, B256::V_SMEM, stream>>>(mq, mdo, mk, p);
+    attn_bwd_dk256_kernel<<<kv_units, BWD_THREADS, B256::K_SMEM, stream>>>(mq, mdo, mk, mv, p);
+    attn_bwd_dq256_kernel<<<q_units, BWD_THREADS, B256::Q_SMEM, stream>>>(mq, mdo, mk, mv, p);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -185,7 +185,7 @@ def call_bwd(**kw):
     return pkg.attn_bwd(check=False, **args)
 
 
-@pytest.mark.parametrize("kw", [dict(d=256), dict(d=32), dict(Hq=6, Hkv=4), dict(scale=0.0),
+@pytest.mark.parametrize("kw", [dict(d=512), dict(d=96), dict(d=32), dict(Hq=6, Hkv=4), dict(scale=0.0),
                                 dict(dq=None), dict(lse=None), dict(dout=None),
                                 dict(workspace=None), dict(workspace_bytes=16),
                                 dict(N=1 << 30, B=4)])

@@ -63,7 +63,7 @@ def check(q, k, v, g, causal, what):
         assert err.mean() <= REL_MEAN * max(np.abs(r).mean(), 1e-3), msg
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 77, 128, 300, 513])
 def test_bwd_parity(d, causal, N):
@@ -81,6 +81,15 @@ def test_bwd_gqa_groups(Hq, Hkv):
     q, k, v = rand((B, N, Hq, d), 11), rand((B, N, Hkv, d), 12), rand((B, N, Hkv, d), 13)
     g = rand((B, N, Hq, d), 14)
     check(q, k, v, g, True, f"Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (3, 3)])
+def test_bwd_gqa_groups_d256(Hq, Hkv):
+    """Head dim 256 (three kernels: dV, dK, dQ) with grouped heads."""
+    B, N, d = 1, 384, 256
+    q, k, v = rand((B, N, Hq, d), 15), rand((B, N, Hkv, d), 16), rand((B, N, Hkv, d), 17)
+    g = rand((B, N, Hq, d), 18)
+    check(q, k, v, g, True, f"d=256 Hq={Hq} Hkv={Hkv}")
 
 
 def test_bwd_peaked_scores():
@@ -112,7 +121,7 @@ def test_bwd_small_workspace_rejected():
     assert rc == pkg.ATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_packed(d, causal):
     lens = [1, 127, 128, 129, 300, 0, 513, 5]
@@ -203,24 +212,35 @@ def test_bwd_parity_long_sequences():
             _check_grads(mine, fut.result(), what)
 
 
-def test_bwd_benchmarked_shape_fp32():
-    """The benchmarked backward itself (B2 Hq32 Hkv8 N4096 d128 causal) against
-    the gradient formulas evaluated in fp32 with PyTorch on the GPU, head by
-    head (TF32 off; the reference's own error is far below the tolerance):
-    S = scale Q K^T (masked), P = softmax(S), dP = dO V^T, D = rowsum(P dP),
-    dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO, with
-    dK and dV summed over each kv head's four query heads."""
-    B, Hq, Hkv, N, d = 2, 32, 8, 4096, 128
-    gen = torch.Generator().manual_seed(2004)
-    dev = torch.device("cuda:0")
-    q, k, v, do = (torch.randn(s, generator=gen).to(torch.bfloat16).to(dev)
-                   for s in ((B, N, Hq, d), (B, N, Hkv, d), (B, N, Hkv, d), (B, N, Hq, d)))
-    o, lse = pkg.attention(q, k, v, causal=True)
-    dq, dk, dv = pkg.attention_backward(q, k, v, o, lse, do, True)
-    assert pkg.attn_get_status() == pkg.ATTN_OK
+def test_bwd_d256_long_sequences():
+    """Head dim 256 at 2048 rows (16 query blocks per dK/dV unit and per dQ
+    unit), causal and not, against the fp64 oracle."""
+    from concurrent.futures import ThreadPoolExecutor
+    d, Hq, Hkv, N = 256, 2, 1, 2048
+    cases = []
+    for causal in (True, False):
+        q, k, v = rand((1, N, Hq, d), 81 + causal), rand((1, N, Hkv, d), 82), rand((1, N, Hkv, d), 83)
+        g = rand((1, N, Hq, d), 84)
+        cases.append((f"d=256 N={N} causal={causal}", (q, k, v, g, causal)))
+    with ThreadPoolExecutor(len(cases)) as pool:
+        futs = [_oracle_async(pool, q_, k_, v_, g_, 1, Hq, Hkv, N, d, c_, None)
+                for _, (q_, k_, v_, g_, c_) in cases]
+        mines = [run_bwd(q_, k_, v_, g_, c_) for _, (q_, k_, v_, g_, c_) in cases]
+        for (what, _), mine, fut in zip(cases, mines, futs):
+            _check_grads(mine, fut.result(), what)
+
+
+def fp32_reference_grads(q, k, v, do, causal):
+    """The gradient formulas in fp32 with PyTorch on the GPU, head by head
+    (TF32 off): S = scale Q K^T (masked), P = softmax(S), dP = dO V^T,
+    D = rowsum(P dP), dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q,
+    dV = P^T dO, with dK and dV summed over each kv head's query heads."""
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dev = q.device
     scale = d ** -0.5
     grp = Hq // Hkv
-    mask = torch.ones(N, N, dtype=torch.bool, device=dev).triu(1)
+    mask = torch.ones(N, N, dtype=torch.bool, device=dev).triu(1) if causal else None
     tf32 = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
     try:
@@ -232,7 +252,11 @@ def test_bwd_benchmarked_shape_fp32():
                 kv = h // grp
                 qh, kh, vh, gh = (q[b, :, h].float(), k[b, :, kv].float(), v[b, :, kv].float(),
                                   do[b, :, h].float())
-                p = torch.softmax((qh @ kh.T * scale).masked_fill(mask, float("-inf")), -1)
+                sc = qh @ kh.T * scale
+                if mask is not None:
+                    sc = sc.masked_fill(mask, float("-inf"))
+                p = torch.softmax(sc, -1)
+                del sc
                 dp = gh @ vh.T
                 ds = p * (dp - (p * dp).sum(-1, keepdim=True))
                 rq[b, :, h] = scale * (ds @ kh)
@@ -241,5 +265,36 @@ def test_bwd_benchmarked_shape_fp32():
                 del p, dp, ds
     finally:
         torch.backends.cuda.matmul.allow_tf32 = tf32
+    return [t.cpu().numpy() for t in (rq, rk, rv)]
+
+
+def test_bwd_d256_long_shape_fp32():
+    """The long head-dim-256 configuration's shape (B1 Hq16 Hkv2 N16384 d256
+    causal, the shape of the benchmarked d = 256 backward) against the fp32
+    gradient formulas on the GPU."""
+    B, Hq, Hkv, N, d = 1, 16, 2, 16384, 256
+    gen = torch.Generator().manual_seed(2005)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (torch.randn(s, generator=gen).to(torch.bfloat16).to(dev)
+                   for s in ((B, N, Hq, d), (B, N, Hkv, d), (B, N, Hkv, d), (B, N, Hq, d)))
+    o, lse = pkg.attention(q, k, v, causal=True)
+    dq, dk, dv = pkg.attention_backward(q, k, v, o, lse, do, True)
+    assert pkg.attn_get_status() == pkg.ATTN_OK
     _check_grads([t.float().cpu().numpy() for t in (dq, dk, dv)],
-                 [t.cpu().numpy() for t in (rq, rk, rv)], "B2 Hq32 Hkv8 N4096 d128 causal")
+                 fp32_reference_grads(q, k, v, do, True), "B1 Hq16 Hkv2 N16384 d256 causal")
+
+
+def test_bwd_benchmarked_shape_fp32():
+    """The benchmarked backward itself (B2 Hq32 Hkv8 N4096 d128 causal)
+    against the gradient formulas in fp32 on the GPU (the reference's own
+    error is far below the tolerance)."""
+    B, Hq, Hkv, N, d = 2, 32, 8, 4096, 128
+    gen = torch.Generator().manual_seed(2004)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (torch.randn(s, generator=gen).to(torch.bfloat16).to(dev)
+                   for s in ((B, N, Hq, d), (B, N, Hkv, d), (B, N, Hkv, d), (B, N, Hq, d)))
+    o, lse = pkg.attention(q, k, v, causal=True)
+    dq, dk, dv = pkg.attention_backward(q, k, v, o, lse, do, True)
+    assert pkg.attn_get_status() == pkg.ATTN_OK
+    _check_grads([t.float().cpu().numpy() for t in (dq, dk, dv)],
+                 fp32_reference_grads(q, k, v, do, True), "B2 Hq32 Hkv8 N4096 d128 causal")
