@@ -902,8 +902,9 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     attn_bwd_dq_kernel<128><<<q_units, BWD_THREADS, BCfg<128>::B_SMEM, stream>>>(mq, mdo, mk, mv, p);
   } else {   // d = 256: dV, dK and dQ in three kernels (attn_bwd256.cuh)
     bwd_rows_kernel<256><<<row_blocks, 256, 0, stream>>>(p);
-    attn_bwd_dv256_kernel<<<kv_units, BWD_THREADS, B256::V_SMEM, stream>>>(mq, mdo, mk, p);
-    attn_bwd_dk256_kernel<<<kv_units, BWD_THREADS, B256::K_SMEM, stream>>>(mq, mdo, mk, mv, p);
+    // two-CTA clusters: a unit's steps split over the pair
+    attn_bwd_dv256_kernel<<<2 * kv_units, BWD_THREADS, B256::V_SMEM, stream>>>(mq, mdo, mk, p);
+    attn_bwd_dk256_kernel<<<2 * kv_units, BWD_THREADS, B256::K_SMEM, stream>>>(mq, mdo, mk, mv, p);
     attn_bwd_dq256_kernel<<<q_units, BWD_THREADS, B256::Q_SMEM, stream>>>(mq, mdo, mk, mv, p);
   }
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

@@ -23,6 +23,14 @@
 // a single pass (the scores are formed three times, dP twice).  Warp roles as
 // in attn_bwd.cuh: warp 0 producer, warp 1 MMA issue loop (one elected lane
 // issues), warps 2-9 softmax (two per TMEM lane quarter, 64 columns each).
+//
+// A dV or dK unit (one kv head's 128-key block) walks group x blocks steps,
+// up to 8 x 128 at 16k rows with 8 query heads per kv head -- longer than a
+// whole SM's fair share when there are few kv heads.  So each unit runs on
+// a two-CTA cluster: rank 0 takes the first half of the steps, rank 1 the
+// second, and at the end rank 1 adds its fp32 partial accumulator into rank
+// 0's shared memory (distributed shared memory), which rank 0 sums into its
+// own before the bf16 store.
 
 namespace attn {
 namespace bwd {
@@ -129,8 +137,75 @@ __device__ __forceinline__ void load64(uint32_t taddr, uint32_t (&u0)[32], uint3
   reg_fence32(u1);
 }
 
+// Pair exchange area: 128 rows x 256 fp32 (1 KB a row), the 16-byte pieces
+// of a row XOR-swizzled by row % 8 so that a warp's 32 rows spread over
+// every bank.
+__device__ __forceinline__ uint32_t xch_addr(uint32_t area, int row, int piece) {
+  return area + (uint32_t)row * 1024u + ((uint32_t)(piece ^ (row & 7)) << 4);
+}
+
+// Rank 1: this thread's 128 accumulator columns (half hf of the row) into
+// the peer's exchange area.
+__device__ __forceinline__ void pair_send(uint32_t taddr, uint32_t peer_area, int row, int hf) {
+#pragma unroll 1
+  for (int cc = 0; cc < 128; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+      st_cluster_v4(xch_addr(peer_area, row, (hf * 128 + cc) / 4 + x),
+                    make_uint4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]));
+  }
+}
+
+// Rank 0: (own accumulator + the peer's partial, if it has one) * mul as
+// bf16, 16-byte stores (if live).
+__device__ __forceinline__ void pair_store(uint32_t taddr, uint32_t area, bool peer, int row,
+                                           int hf, float mul, __nv_bfloat16 *dst, bool live) {
+#pragma unroll 1
+  for (int cc = 0; cc < 128; cc += 32) {
+    uint32_t o[32];
+    tmem_ld32(taddr + cc, o);
+    tmem_wait_ld();
+    reg_fence32(o);
+    float f[32];
+#pragma unroll
+    for (int x = 0; x < 32; ++x) f[x] = __uint_as_float(o[x]);
+    if (peer) {
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint4 w = ld_shared_v4(xch_addr(area, row, (hf * 128 + cc) / 4 + x));
+        f[4 * x] += __uint_as_float(w.x);
+        f[4 * x + 1] += __uint_as_float(w.y);
+        f[4 * x + 2] += __uint_as_float(w.z);
+        f[4 * x + 3] += __uint_as_float(w.w);
+      }
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) w[x] = pack_bf16x2(f[2 * x] * mul, f[2 * x + 1] * mul);
+    if (live) {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc);
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+        d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+    }
+  }
+}
+
+// The pair's share of a unit's steps: rank 0 [0, half), rank 1 [half, n).
+struct PairSteps {
+  int s0, n, peer_n;
+};
+__device__ __forceinline__ PairSteps pair_steps(int total, uint32_t rank) {
+  const int half = (total + 1) >> 1;
+  return rank ? PairSteps{half, total - half, half} : PairSteps{0, half, total - half};
+}
+
 // ------------------------------------------------------------------ dV
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_k, const BwdParams p) {
@@ -145,13 +220,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::V_OFF_CTL + 8 * X_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const BUnit un = bwd_unit(p, blockIdx.x, p.Hkv, false);
-  if (!un.valid) return;   // uniform over the CTA, before any set-up
+  const uint32_t rank = cluster_ctarank();
+  const BUnit un = bwd_unit(p, blockIdx.x >> 1, p.Hkv, false);
+  if (!un.valid) return;   // uniform over the cluster, before any set-up
   const int jb = un.blk, kvh = un.head, b = un.seq;
   const int nblk = un.nblk, row0 = un.start, len = un.len;
   const int i0 = p.causal ? jb : 0;
-  const int steps = p.group * (nblk - i0);
+  const PairSteps ps = pair_steps(p.group * (nblk - i0), rank);
+  const int steps = ps.n;   // this CTA's steps t = 0 .. steps-1 are unit steps s0 + t
   const uint32_t k_s = base + C::V_OFF_K, q_s = base + C::V_OFF_Q, do_s = base + C::V_OFF_DO;
+  bool have = false;   // softmax threads: this CTA's accumulator row is final
   constexpr uint32_t COL_ST = 0, COL_DV = 256;
 
   if (warp == 1) {
@@ -172,15 +250,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   if (warp == 0) {
     // producer: K once; per step Q(s) with its lse2 row (row slot s & 1) once
     // S^T(s-1) has read Q(s-1), and dO(s) once dV(s-1) has read dO(s-1)
-    if (lane == 0) {
+    if (lane == 0 && steps > 0) {
       int issued_a = 0, issued_do = 0;
       bool ok = true;
       mbar_arrive_expect_tx(ctl.bar(X_STATIC), C::TILE);
       for (int c = 0; c < 4; ++c)
         tma_load_3d(k_s + c * CHUNK_BYTES, &tm_k, ctl.bar(X_STATIC), c * 64, kvh, row0 + jb * BM);
       for (int s = 0; ok && s < steps; ++s) {
-        const int h = kvh * p.group + s / (nblk - i0);
-        const int ib = i0 + s % (nblk - i0);
+        const int h = kvh * p.group + (ps.s0 + s) / (nblk - i0);
+        const int ib = i0 + (ps.s0 + s) % (nblk - i0);
         if (s > 0 && !(ok = wait_bounded(ctl.bar(X_A_EMPTY), (uint32_t)(s - 1) & 1u, abort_flag,
                                          p.timeout_ns)))
           break;
@@ -219,25 +297,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
     const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
     const uint64_t do_mn = smem_desc_sw128(do_s, CHUNK_BYTES, 1024);
-    bool ok = wait_warp(ctl.bar(X_STATIC), 0, abort_flag, p.timeout_ns);
-    for (int s = 0; ok && s < steps; ++s) {
-      const uint32_t par = (uint32_t)s & 1u;
-      if (!(ok = wait_warp(ctl.bar(X_A_FULL), par, abort_flag, p.timeout_ns))) break;
-      tc_fence_after();
-      issue_qk_warp<D>(tmem + COL_ST, kdesc, qdesc);
-      tc_commit_warp(ctl.bar(X_ST_FULL));
-      tc_commit_warp(ctl.bar(X_A_EMPTY));   // Q(s) is read
-      if (!(ok = wait_warp(ctl.bar(X_PT_FULL), par, abort_flag, p.timeout_ns)) ||
-          !(ok = wait_warp(ctl.bar(X_DO_FULL), par, abort_flag, p.timeout_ns)))
-        break;
-      tc_fence_after();
-      issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
-      issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
-      tc_commit_warp(ctl.bar(X_DO_EMPTY));   // dO(s) and P^T(s) are read
+    if (steps > 0) {
+      bool ok = wait_warp(ctl.bar(X_STATIC), 0, abort_flag, p.timeout_ns);
+      for (int s = 0; ok && s < steps; ++s) {
+        const uint32_t par = (uint32_t)s & 1u;
+        if (!(ok = wait_warp(ctl.bar(X_A_FULL), par, abort_flag, p.timeout_ns))) break;
+        tc_fence_after();
+        issue_qk_warp<D>(tmem + COL_ST, kdesc, qdesc);
+        tc_commit_warp(ctl.bar(X_ST_FULL));
+        tc_commit_warp(ctl.bar(X_A_EMPTY));   // Q(s) is read
+        if (!(ok = wait_warp(ctl.bar(X_PT_FULL), par, abort_flag, p.timeout_ns)) ||
+            !(ok = wait_warp(ctl.bar(X_DO_FULL), par, abort_flag, p.timeout_ns)))
+          break;
+        tc_fence_after();
+        issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
+        tc_commit_warp(ctl.bar(X_DO_EMPTY));   // dO(s) and P^T(s) are read
+      }
+      if (ok) tc_commit_warp(ctl.bar(X_DONE));
+      tc_commit_warp(ctl.bar(X_DRAIN));
+      wait_drain(ctl.bar(X_DRAIN), 0, p.timeout_ns);
     }
-    if (ok) tc_commit_warp(ctl.bar(X_DONE));
-    tc_commit_warp(ctl.bar(X_DRAIN));
-    wait_drain(ctl.bar(X_DRAIN), 0, p.timeout_ns);
     __syncwarp();
   } else {
     // softmax warps: thread = key row jb*128 + row, query columns 64 hf .. +63
@@ -247,7 +327,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int key = jb * BM + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float c = p.scale_log2;
-    bool ok = true;
+    bool ok = steps > 0;
     for (int s = 0; ok && s < steps; ++s) {
       const uint32_t par = (uint32_t)s & 1u;
       // the step's lse2 row (slot s & 1), then S^T(s)
@@ -256,7 +336,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           !(ok = wait_warp(ctl.bar(X_ST_FULL), par, abort_flag, p.timeout_ns)))
         break;
       tc_fence_after();
-      const int ib = i0 + s % (nblk - i0);
+      const int ib = i0 + (ps.s0 + s) % (nblk - i0);
       const float *lse2 = reinterpret_cast<const float *>(smem + C::V_OFF_ROWS + (s & 1) * 512);
       uint32_t us0[32], us1[32], pw[2][16];
       load64(tmem + lane_off + COL_ST + 64 * hf, us0, us1);
@@ -268,11 +348,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       warp_arrive(ctl.bar(X_PT_FULL));
     }
-    if (ok && (ok = wait_warp(ctl.bar(X_DONE), 0, abort_flag, p.timeout_ns))) {
+    if (ok && wait_warp(ctl.bar(X_DONE), 0, abort_flag, p.timeout_ns)) {
       tc_fence_after();
-      const long long off = ((long long)(row0 + key) * p.Hkv + kvh) * D + hf * (D / 2);
-      store_row_bf16<D / 2>(tmem + lane_off + COL_DV + hf * (D / 2), 1.f, p.dv + off, key < len);
+      have = true;
     }
+  }
+  // every product of both CTAs is complete: rank 0's Q and dO tiles are free
+  cluster_sync_all();
+  if (warp >= 2) {
+    const int row = (warp & 3) * 32 + lane, hf = (warp - 2) >> 2;
+    const uint32_t acc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + COL_DV + hf * (D / 2);
+    if (rank == 1 && have) pair_send(acc, mapa_shared(q_s, 0), row, hf);
+    cluster_sync_all();   // rank 1's partial is in rank 0's exchange area
+    if (rank == 0 && have) {
+      const long long off = ((long long)(row0 + jb * BM + row) * p.Hkv + kvh) * D + hf * (D / 2);
+      pair_store(acc, q_s, ps.peer_n > 0, row, hf, 1.f, p.dv + off, jb * BM + row < len);
+    }
+  } else {
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -283,7 +376,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ dK
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dk256_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -299,13 +392,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   ctl.words = reinterpret_cast<uint32_t *>(smem + C::K_OFF_CTL + 8 * X_COUNT);
   volatile uint32_t *abort_flag = ctl.words + 1;
 
-  const BUnit un = bwd_unit(p, blockIdx.x, p.Hkv, false);
-  if (!un.valid) return;
+  const uint32_t rank = cluster_ctarank();
+  const BUnit un = bwd_unit(p, blockIdx.x >> 1, p.Hkv, false);
+  if (!un.valid) return;   // uniform over the cluster
   const int jb = un.blk, kvh = un.head, b = un.seq;
   const int nblk = un.nblk, row0 = un.start, len = un.len;
   const int i0 = p.causal ? jb : 0;
-  const int steps = p.group * (nblk - i0);
+  const PairSteps ps = pair_steps(p.group * (nblk - i0), rank);
+  const int steps = ps.n;
   const uint32_t k_s = base + C::K_OFF_K, v_s = base + C::K_OFF_V, q_s = base + C::K_OFF_Q;
+  bool have = false;
   const uint32_t ring = base + C::K_OFF_RING;
   constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DK = 256;
 
@@ -329,7 +425,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // producer: K, V once; per step the first two dO(s) chunks, Q(s) with its
     // rows once dK(s-1) has read Q(s-1), then the last two dO chunks (dO
     // chunk position 4 s + c goes to ring slot (4 s + c) % 2)
-    if (lane == 0) {
+    if (lane == 0 && steps > 0) {
       int issued = 0, cpos = 0;
       bool ok = true;
       mbar_arrive_expect_tx(ctl.bar(X_STATIC), 2 * C::TILE);
@@ -338,8 +434,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tma_load_3d(v_s + c * CHUNK_BYTES, &tm_v, ctl.bar(X_STATIC), c * 64, kvh, row0 + jb * BM);
       }
       for (int s = 0; ok && s < steps; ++s) {
-        const int h = kvh * p.group + s / (nblk - i0);
-        const int ib = i0 + s % (nblk - i0);
+        const int h = kvh * p.group + (ps.s0 + s) / (nblk - i0);
+        const int ib = i0 + (ps.s0 + s) % (nblk - i0);
         for (int c = 0; ok && c < 4; ++c, ++cpos) {
           if (c == 2) {   // Q(s) and the step's rows
             if (s > 0 && !(ok = wait_bounded(ctl.bar(X_A_EMPTY), (uint32_t)(s - 1) & 1u,
@@ -383,7 +479,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
     const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
     const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
-    bool ok = wait_warp(ctl.bar(X_STATIC), 0, abort_flag, p.timeout_ns);
+    bool ok = steps > 0 && wait_warp(ctl.bar(X_STATIC), 0, abort_flag, p.timeout_ns);
     int cpos = 0;
     for (int s = 0; ok && s < steps; ++s) {
       const uint32_t par = (uint32_t)s & 1u;
@@ -409,9 +505,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       issue_pv_half_warp<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 1, s > 0);
       tc_commit_warp(ctl.bar(X_A_EMPTY));   // Q(s) and the rows are read
     }
-    if (ok) tc_commit_warp(ctl.bar(X_DONE));
-    tc_commit_warp(ctl.bar(X_DRAIN));
-    wait_drain(ctl.bar(X_DRAIN), 0, p.timeout_ns);
+    if (steps > 0) {
+      if (ok) tc_commit_warp(ctl.bar(X_DONE));
+      tc_commit_warp(ctl.bar(X_DRAIN));
+      wait_drain(ctl.bar(X_DRAIN), 0, p.timeout_ns);
+    }
     __syncwarp();
   } else {
     const int wq = warp & 3;
@@ -422,14 +520,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const float c = p.scale_log2;
     const float *lse2 = reinterpret_cast<const float *>(smem + C::K_OFF_ROWS);
     const float *dsum = lse2 + 128;
-    bool ok = true;
+    bool ok = steps > 0;
     for (int s = 0; ok && s < steps; ++s) {
       const uint32_t par = (uint32_t)s & 1u;
       if (!(ok = wait_warp(ctl.bar(X_A_FULL), par, abort_flag, p.timeout_ns)) ||
           !(ok = wait_warp(ctl.bar(X_ST_FULL), par, abort_flag, p.timeout_ns)))
         break;
       tc_fence_after();
-      const int ib = i0 + s % (nblk - i0);
+      const int ib = i0 + (ps.s0 + s) % (nblk - i0);
       // phase 1: P^T in registers (no product reads it here)
       uint32_t us0[32], us1[32], pw[2][16];
       load64(tmem + lane_off + COL_ST + 64 * hf, us0, us1);
@@ -467,12 +565,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       warp_arrive(ctl.bar(X_DST_FULL));
     }
-    if (ok && (ok = wait_warp(ctl.bar(X_DONE), 0, abort_flag, p.timeout_ns))) {
+    if (ok && wait_warp(ctl.bar(X_DONE), 0, abort_flag, p.timeout_ns)) {
       tc_fence_after();
-      const long long off = ((long long)(row0 + key) * p.Hkv + kvh) * D + hf * (D / 2);
-      store_row_bf16<D / 2>(tmem + lane_off + COL_DK + hf * (D / 2), p.scale, p.dk + off,
-                            key < len);
+      have = true;
     }
+  }
+  // every product of both CTAs is complete: rank 0's V and Q tiles are free
+  cluster_sync_all();
+  if (warp >= 2) {
+    const int row = (warp & 3) * 32 + lane, hf = (warp - 2) >> 2;
+    const uint32_t acc = tmem + ((uint32_t)((warp & 3) * 32) << 16) + COL_DK + hf * (D / 2);
+    if (rank == 1 && have) pair_send(acc, mapa_shared(v_s, 0), row, hf);
+    cluster_sync_all();   // rank 1's partial is in rank 0's exchange area
+    if (rank == 0 && have) {
+      const long long off = ((long long)(row0 + jb * BM + row) * p.Hkv + kvh) * D + hf * (D / 2);
+      pair_store(acc, v_s, ps.peer_n > 0, row, hf, p.scale, p.dk + off, jb * BM + row < len);
+    }
+  } else {
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
