@@ -161,7 +161,9 @@ enum : int {
   B_DST_FULL,          // all softmax warps: dS^T (dS) written over dP^T (dP)
   B_KFULL0,            // dQ kernel: K ring slot s loaded, s < 3 (B_FULL0/1 and
   B_KEMPTY0 = B_KFULL0 + 3,   // B_EMPTY0/1 serve its V ring); K slot s consumed
-  B_COUNT = B_KEMPTY0 + 3
+  B_DP1 = B_KEMPTY0 + 3,      // dQ kernel: dP in TMEM buffer 1 (B_DPT_FULL: buffer 0)
+  B_DS1,                      // dQ kernel: dS written over buffer 1 (B_DST_FULL: 0)
+  B_COUNT
 };
 
 // ------------------------------------------------------------------ row pass
@@ -228,6 +230,8 @@ __device__ __forceinline__ void bwd_init_barriers(const BCtl &c) {
   mbar_init(c.bar(B_DPT_FULL), 1);
   mbar_init(c.bar(B_PT_FULL), BWD_SM_WARPS);
   mbar_init(c.bar(B_DST_FULL), BWD_SM_WARPS);
+  mbar_init(c.bar(B_DP1), 1);
+  mbar_init(c.bar(B_DS1), BWD_SM_WARPS);
   for (int s = 0; s < 3; ++s) {
     mbar_init(c.bar(B_KFULL0 + s), 1);
     mbar_init(c.bar(B_KEMPTY0 + s), 1);
@@ -585,7 +589,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl.words[0];
-  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+  // S, two dP buffers (step s in buffer s & 1), dQ
+  constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 384;
+  static_assert(COL_DQ + D <= TMEM_COLS, "tensor memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -641,11 +647,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint64_t qdesc = smem_desc_sw128(q_s, 16, 1024);
       const uint64_t dodesc = smem_desc_sw128(do_s, 16, 1024);
       bool ok = wait_warp(ctl.bar(B_STATIC_FULL), 0, abort_flag, p.timeout_ns);
-      // Per step s: S(s) and dP(s) in full; S(s+1) as soon as the softmax
-      // warps have read S(s) (P is no operand here); dQ += dS(s) K once they
-      // have written dS over dP(s); then dP(s+1) (dP's columns are free once
-      // dQ(s) has read dS: one thread's MMAs run in issue order).  A V slot
-      // is released when its dP product is done, a K slot after dQ.
+      // Per step s: S(s+1) and dP(s+1) as soon as the softmax warps have read
+      // S(s) (P is no operand here; dP(s+1) goes to the other dP buffer,
+      // whose dS(s-1) the dQ product issued before has read: one thread's
+      // MMAs run in issue order), then dQ += dS(s) K once they have written
+      // dS over dP(s).  So the softmax warps never wait for a product of
+      // their own step's chain.  A V slot is released when its dP product is
+      // done, a K slot after dQ.
       const uint32_t kring = base + C::B_OFF_K, vring = base + C::B_OFF_V;
       if (ok && steps > 0 &&
           (ok = wait_warp(ctl.bar(B_KFULL0), 0, abort_flag, p.timeout_ns))) {
@@ -661,33 +669,36 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       for (int s = 0; ok && s < steps; ++s) {
         const int ks = s % C::K_STAGES, kn = (s + 1) % C::K_STAGES, vn = (s + 1) % C::V_STAGES;
+        const uint32_t bn = (uint32_t)(s + 1) & 1u, bs = (uint32_t)s & 1u;
         const bool more = s + 1 < steps;
         if (!(ok = wait_warp(ctl.bar(B_PT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
           break;
         if (more) {
           if (!(ok = wait_warp(ctl.bar(B_KFULL0 + kn), (uint32_t)((s + 1) / C::K_STAGES) & 1u,
-                                  abort_flag, p.timeout_ns)))
+                               abort_flag, p.timeout_ns)))
             break;
           tc_fence_after();
           issue_qk_warp<D>(tmem + COL_S, qdesc, smem_desc_sw128(kring + kn * C::TILE, 16, 1024));
           tc_commit_warp(ctl.bar(B_ST_FULL));
+          if (!(ok = wait_warp(ctl.bar(B_FULL0 + vn), (uint32_t)((s + 1) / C::V_STAGES) & 1u,
+                               abort_flag, p.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_qk_warp<D>(tmem + COL_DP + 128u * bn, dodesc,
+                           smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
+          tc_commit_warp(ctl.bar(bn ? B_DP1 : B_DPT_FULL));
+          tc_commit_warp(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
         }
-        if (!(ok = wait_warp(ctl.bar(B_DST_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+        // dS(s) over buffer s & 1 (one barrier per buffer: the softmax warps
+        // may finish step s + 1 before this wait returns)
+        if (!(ok = wait_warp(ctl.bar(bs ? B_DS1 : B_DST_FULL), (uint32_t)(s >> 1) & 1u,
+                             abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
         const uint64_t k_mn = smem_desc_sw128(kring + ks * C::TILE, CHUNK_BYTES, 1024);
-        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 0, s > 0);
-        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP, k_mn, 1, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP + 128u * bs, k_mn, 0, s > 0);
+        issue_pv_half_warp<D>(tmem + COL_DQ, tmem + COL_DP + 128u * bs, k_mn, 1, s > 0);
         tc_commit_warp(ctl.bar(B_KEMPTY0 + ks));   // K(s) is read
-        if (more) {
-          if (!(ok = wait_warp(ctl.bar(B_FULL0 + vn), (uint32_t)((s + 1) / C::V_STAGES) & 1u,
-                                  abort_flag, p.timeout_ns)))
-            break;
-          tc_fence_after();
-          issue_qk_warp<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
-          tc_commit_warp(ctl.bar(B_DPT_FULL));
-          tc_commit_warp(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
-        }
       }
       if (ok) tc_commit_warp(ctl.bar(B_DONE));
       tc_commit_warp(ctl.bar(B_DRAIN));
@@ -750,14 +761,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
       }
       // phase 2: dS = P o (dP - D), bf16 over the first 32 of the 64 columns
-      if (!(ok = wait_warp(ctl.bar(B_DPT_FULL), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
+      // of dP buffer s & 1
+      const uint32_t bs = (uint32_t)s & 1u, col_dp = COL_DP + 128u * bs;
+      if (!(ok = wait_warp(ctl.bar(bs ? B_DP1 : B_DPT_FULL), (uint32_t)(s >> 1) & 1u, abort_flag,
+                           p.timeout_ns)))
         break;
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int c0 = 64 * hf + 32 * ch;
         uint32_t ud[32];
-        tmem_ld32(tmem + lane_off + COL_DP + c0, ud);
+        tmem_ld32(tmem + lane_off + col_dp + c0, ud);
         tmem_wait_ld();
         reg_fence32(ud);
         uint32_t dw[16];
@@ -770,11 +784,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     a0, a1);
           dw[x >> 1] = pack_bf16x2(a0, a1);
         }
-        tmem_st16(tmem + lane_off + COL_DP + 64 * hf + 16 * ch, dw);
+        tmem_st16(tmem + lane_off + col_dp + 64 * hf + 16 * ch, dw);
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(ctl.bar(B_DST_FULL));
+      warp_arrive(ctl.bar(bs ? B_DS1 : B_DST_FULL));
     }
     if (ok && (ok = wait_warp(ctl.bar(B_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
