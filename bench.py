@@ -99,10 +99,14 @@ def measured_peaks() -> dict:
         return {}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(forward_only: bool = False) -> str:
+    """Hash of the kernel sources (forward_only: without the backward's
+    headers, which define no forward kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_program_compilers_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if forward_only and name.startswith("attn_bwd"):
+            continue
         if name.endswith((".cu", ".cuh")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
@@ -118,7 +122,7 @@ def recorded_traffic(workload_key: str):
     except (OSError, ValueError):
         return None
     ent = rec.get(workload_key)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash(forward_only=True):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -431,12 +435,14 @@ BWD_SHAPES = {
 }
 
 
-def run_backward(pkg, dev, flush, steps, shape="backward"):
+def run_backward(pkg, dev, flush, steps, shape="backward", seqlen=None):
     """Backward (dQ, dK, dV from the forward's O and LSE), causal, of one of
-    BWD_SHAPES.  TFLOP/s under the usual convention of 2.5x the forward's
-    FLOPs (five products of the forward's size)."""
+    BWD_SHAPES (seqlen: another sequence length, for small profiling runs).
+    TFLOP/s under the usual convention of 2.5x the forward's FLOPs (five
+    products of the forward's size)."""
     import torch
     B, Hq, Hkv, N, d = BWD_SHAPES[shape]
+    N = seqlen or N
     g = torch.Generator().manual_seed(2004)
     q = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16).to(dev)
     k = torch.randn((B, N, Hkv, d), generator=g).to(torch.bfloat16).to(dev)
@@ -759,6 +765,8 @@ def parse_args(argv=None):
                     default="ragged")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bwd-seqlen", type=int, default=None,
+                    help="with --extra backward*: another sequence length (profiling)")
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -785,7 +793,7 @@ def extra_only(args):
     if args.extra == "window":
         out = run_window(pkg, dev, flush, args.steps)
     elif args.extra in ("backward", "backward256"):
-        out = run_backward(pkg, dev, flush, args.steps, args.extra)
+        out = run_backward(pkg, dev, flush, args.steps, args.extra, args.bwd_seqlen)
     elif args.extra == "decode_paged":
         out = run_decode_paged(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))
     else:
