@@ -22,6 +22,7 @@ INCLUDE_DIR = os.path.join(_ROOT, "include")
 SOURCES = [os.path.join(_CSRC, "attn_fwd.cu")]
 DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(_CSRC, "attn_bwd.cuh"),
                      os.path.join(_CSRC, "attn_fwd2.cuh"), os.path.join(_CSRC, "attn_bwd256.cuh"),
+                     os.path.join(_CSRC, "attn_decode_cc.cuh"),
                      os.path.join(INCLUDE_DIR, "attn.h")]
 
 NVCC_FLAGS = [

@@ -210,6 +210,9 @@ struct Params {
   // j / page_size]; dk_n = max_blocks * page_size
   const int *block_table;
   int max_blocks, page_size, num_pages;
+  int page_shift;   // log2(page_size) for a power of two, else -1
+  // decode on the CUDA cores: the caches' rows, read with plain loads
+  const __nv_bfloat16 *kc, *vc;
   float *ws_o;          // splits > 1: partial O / l [B, Hq, dq_n, splits, d]
   float *ws_lse;        // and partial LSE [B, Hq, dq_n, splits]
   int unit_rows;        // query rows per CTA work unit (one tile)
@@ -1560,6 +1563,8 @@ static unsigned long long wait_timeout_ns() {
 
 }  // namespace attn
 
+#include "attn_decode_cc.cuh"
+
 extern "C" attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                                 const int *cu_seqlens, cudaStream_t stream) {
@@ -1666,6 +1671,32 @@ extern "C" attn_status attn_fwd_ex(const void *q, const void *k, const void *v, 
 
 namespace attn {
 // Key splits of a decode launch: at most one unit per SM, whole key tiles.
+// Few query rows per (sequence, kv head) -- the group's heads x the new
+// positions -- go to the CUDA-core decode kernel (dcc), more to the tile path.
+static bool decode_on_cores(int Hq, int Hkv, int Nq, int d) {
+  return (long long)(Hq / Hkv) * Nq <= 8 && (d == 64 || d == 128 || d == 256);
+}
+
+static int decode_cc_rows(int Hq, int Hkv, int Nq) {
+  const long long rows = (long long)(Hq / Hkv) * Nq;
+  return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+}
+
+// CUDA-core decode (one CTA of 8-16 warps per SM): whole (sequence, kv head)
+// pairs once they fill half of the SMs -- a split costs a merge pass, which
+// measured more than the idle SMs (B 16, Hkv 8 on 152 SMs: 0.103 ms with one
+// split, 0.117 with two) -- else as many key splits (of at least 128 keys) as
+// fit one round.
+static void decode_splits_cc(int B, int Hkv, int Nk, int sms, int &splits, int &chunk) {
+  const long long per = (long long)B * Hkv;
+  long long want = 2 * per >= sms ? 1 : sms / per;
+  const long long tiles = ((long long)Nk + BN - 1) / BN;
+  if (want > tiles) want = tiles;
+  if (want < 1) want = 1;
+  chunk = (int)(((tiles + want - 1) / want) * BN);
+  splits = (int)(((long long)Nk + chunk - 1) / chunk);
+}
+
 static void decode_splits(int B, int Hkv, int Nk, int sms, int &splits, int &chunk) {
   // At most one round of units: as many splits as keep every (sequence, kv
   // head) on whole SMs.  Measured (B 16, Hkv 8, Nk 8192 on 152 SMs): one
@@ -1692,11 +1723,54 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Nq, in
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || prepare_device(dev) != ATTN_OK) return 0;
   int splits, chunk;
-  decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  if (decode_on_cores(Hq, Hkv, Nq, d))
+    decode_splits_cc(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  else
+    decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
   return decode_ws_bytes(B, Hq, Nq, d, splits);
 }
 
 namespace attn {
+template <int D, int RP, bool PAGED>
+static bool launch_dcc_kernel(unsigned grid, const Params &p, cudaStream_t stream) {
+  static std::atomic<bool> opted[MAX_DEVICES];   // its ring exceeds the default 48 KB
+  constexpr int bytes = dcc::ring_bytes(RP);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return false;
+  if (!opted[dev].load()) {
+    if (cudaFuncSetAttribute(dcc::attn_decode_cc_kernel<D, RP, PAGED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return false;
+    opted[dev].store(true);
+  }
+  dcc::attn_decode_cc_kernel<D, RP, PAGED>
+      <<<grid, dcc::warps_for(RP) * 32, bytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess;
+}
+template <int D, int RP>
+static bool launch_dcc(bool paged, unsigned grid, const Params &p, cudaStream_t stream) {
+  return paged ? launch_dcc_kernel<D, RP, true>(grid, p, stream)
+               : launch_dcc_kernel<D, RP, false>(grid, p, stream);
+}
+template <int D>
+static bool launch_dcc_rows(int rp, bool paged, unsigned grid, const Params &p,
+                            cudaStream_t stream) {
+  switch (rp) {
+    case 1: return launch_dcc<D, 1>(paged, grid, p, stream);
+    case 2: return launch_dcc<D, 2>(paged, grid, p, stream);
+    case 4: return launch_dcc<D, 4>(paged, grid, p, stream);
+    default: return launch_dcc<D, 8>(paged, grid, p, stream);
+  }
+}
+static bool launch_decode_cc(int d, int rp, bool paged, unsigned grid, const Params &p,
+                             cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_dcc_rows<64>(rp, paged, grid, p, stream);
+    case 128: return launch_dcc_rows<128>(rp, paged, grid, p, stream);
+    default: return launch_dcc_rows<256>(rp, paged, grid, p, stream);
+  }
+}
+
 // The decode call; with use_static the workspace is the fixed device array.
 struct PagedArgs {
   const int *block_table;
@@ -1729,21 +1803,27 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   attn_status st = prepare_device(dev);
   if (st != ATTN_OK) return st;
+  const bool cores = decode_on_cores(Hq, Hkv, Nq, d);
   int splits, chunk;
-  decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  if (cores)
+    decode_splits_cc(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
+  else
+    decode_splits(B, Hkv, Nk, g_sm_count[dev], splits, chunk);
   const size_t need = decode_ws_bytes(B, Hq, Nq, d, splits);
   if (use_static) {
     workspace = g_scratch_ptr[dev];
     workspace_bytes = DECODE_SCRATCH_BYTES;
   }
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return ATTN_ERR_CUDA;
   CUtensorMap mk, mv;
-  const int box_rows = pg ? std::min(pg->page_size, BN) : BM;
-  if (!make_map(enc, &mk, k, Hkv, krows, d, box_rows) ||
-      !make_map(enc, &mv, v, Hkv, krows, d, box_rows))
-    return ATTN_ERR_INVALID_ARG;
+  if (!cores) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return ATTN_ERR_CUDA;
+    const int box_rows = pg ? std::min(pg->page_size, BN) : BM;
+    if (!make_map(enc, &mk, k, Hkv, krows, d, box_rows) ||
+        !make_map(enc, &mv, v, Hkv, krows, d, box_rows))
+      return ATTN_ERR_INVALID_ARG;
+  }
 
   Params p{};
   p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
@@ -1765,6 +1845,7 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
     p.max_blocks = pg->max_blocks;
     p.page_size = pg->page_size;
     p.num_pages = pg->num_pages;
+    p.page_shift = (pg->page_size & (pg->page_size - 1)) == 0 ? __builtin_ctz(pg->page_size) : -1;
   }
   p.ws_o = reinterpret_cast<float *>(workspace);
   p.ws_lse = need > 0 ? p.ws_o + (size_t)B * Hq * Nq * splits * d : nullptr;
@@ -1772,8 +1853,16 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
+  p.kc = reinterpret_cast<const __nv_bfloat16 *>(k);
+  p.vc = reinterpret_cast<const __nv_bfloat16 *>(v);
 
   const long long units = (long long)B * Hkv * splits;
+  if (cores) {
+    if (units > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
+    if (!launch_decode_cc(d, decode_cc_rows(Hq, Hkv, Nq), pg != nullptr, (unsigned)units, p,
+                          stream))
+      return ATTN_ERR_CUDA;
+  } else {
   const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
   const unsigned gr = (unsigned)grid;
   switch (d * 2 + (pg ? 1 : 0)) {   // no Q tensor map: decode gathers its query rows
@@ -1783,6 +1872,7 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
     case 257: attn_fwd_kernel<128, 3><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
     case 512: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
     default: attn_fwd_kernel<256, 3><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+  }
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   if (splits > 1) {
