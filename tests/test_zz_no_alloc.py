@@ -89,3 +89,42 @@ def test_static_single_split_needs_no_scratch():
     assert pkg.attn_get_status() == pkg.ATTN_OK
     assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
     assert torch.equal(lse, l_ref)
+
+
+@pytest.mark.parametrize("Nq,Hq", [(1, 16), (4, 16)])
+def test_static_decode_replays_in_a_cuda_graph(Nq, Hq):
+    """The entry point's purpose: after one call outside capture it needs no
+    allocation and no host lookup, so it can be captured in a CUDA graph.
+    Two replays give the workspace entry point's bits (group 4 x Nq 1: the
+    CUDA-core kernel with key splits and the merge; Nq 4: the tile kernel)."""
+    B, Hkv, Nk, d = 3, 4, 3000, 128
+    lens = [3000, 1500, Nq]
+    q, k, v, sl = problem(B, Nq, Hq, Hkv, Nk, d, 90 + Nq, lens)
+    n = pkg.attn_decode_workspace_bytes(B, Hq, Hkv, Nq, Nk, d)
+    assert 0 < n <= pkg.DECODE_STATIC_SCRATCH_BYTES
+    ws = torch.empty(((n + 15) // 16 * 4,), dtype=torch.float32, device="cuda:0")
+    o_ref = torch.full_like(q, float("nan"))
+    l_ref = torch.full((B, Hq, Nq), float("nan"), dtype=torch.float32, device="cuda:0")
+    pkg.attn_fwd_decode(q, k, v, o_ref, l_ref, B, Hq, Hkv, Nq, Nk, d, d ** -0.5, True, sl, ws)
+    assert pkg.attn_get_status() == pkg.ATTN_OK
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq, Nq), float("nan"), dtype=torch.float32, device="cuda:0")
+    call = lambda: pkg.attn_fwd_decode_static(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, d ** -0.5,
+                                              True, sl)
+    call()   # the first call outside capture (device set-up)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert pkg.attn_get_status() == pkg.ATTN_OK
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, l_ref)
