@@ -74,6 +74,35 @@ def test_decode_group_shapes(Hq, Hkv, Nq):
     compare(o, lse, oo, lo, f"decode Hq={Hq} Hkv={Hkv} Nq={Nq}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv,Nq", [(8, 4, 4), (4, 2, 2), (6, 2, 1), (3, 1, 2), (8, 8, 1)])
+def test_decode_few_rows_per_kv_head(d, Hq, Hkv, Nq):
+    """Group x Nq <= 8 rows per kv head (the CUDA-core kernel), causal, with
+    several new positions and row counts that are not powers of two (the
+    kernel pads to 1, 2, 4 or 8 rows); lengths that split the keys and
+    lengths that do not."""
+    B, Nk = 3, 2100
+    lens = [2100, Nq, 777]
+    q = rand((B, Nq, Hq, d), 101 + Hq + Nq + d, 2.0)
+    k, v = caches(B, Nk, Hkv, d, lens, 102 + d)
+    o, lse, _ = run_decode(q, k, v, lens, True, d ** -0.5)
+    oo, lo = oracle.attn_decode_oracle(q, k, v, lens, True, d ** -0.5)
+    compare(o, lse, oo, lo, f"decode d={d} Hq={Hq} Hkv={Hkv} Nq={Nq}")
+
+
+def test_decode_few_rows_many_sequences():
+    """Enough (sequence, kv head) pairs for one unit per CTA (no split),
+    causal with two new positions, varied lengths."""
+    B, Nq, Hq, Hkv, Nk, d = 48, 2, 8, 4, 700, 128
+    lens = [Nq + (b * 37) % 690 for b in range(B)]
+    q = rand((B, Nq, Hq, d), 111, 2.0)
+    k, v = caches(B, Nk, Hkv, d, lens, 112)
+    o, lse, n = run_decode(q, k, v, lens, True, d ** -0.5)
+    assert n == 0
+    oo, lo = oracle.attn_decode_oracle(q, k, v, lens, True, d ** -0.5)
+    compare(o, lse, oo, lo, "decode few rows, many sequences")
+
+
 def test_decode_single_split_writes_directly():
     """Enough (sequence, kv head) pairs for every SM: one split, no merge
     kernel and no workspace."""

@@ -84,6 +84,30 @@ def test_paged_parity_heads_and_queries(d, causal):
     compare(o, lse, oo, lo, f"paged d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("P", [16, 64, 128])
+def test_paged_few_rows_causal(d, P):
+    """The CUDA-core kernel over pages: group 2 x Nq 3 = 6 rows per kv
+    head, causal."""
+    B, Nq, Hq, Hkv = 2, 3, 8, 4
+    lens = [1333, 300]
+    q, kc, vc, table, mb, npg = paged_problem(B, Nq, Hq, Hkv, d, P, lens, 60 + P + d)
+    o, lse, _ = run_paged(q, kc, vc, table, mb, npg, P, lens, True)
+    oo, lo = oracle.attn_decode_paged_oracle(q, kc, vc, lens, table, P, True, d ** -0.5)
+    compare(o, lse, oo, lo, f"paged few rows P={P} d={d}")
+
+
+def test_paged_page_size_not_a_power_of_two():
+    """384-row pages (a multiple of 128, not a power of two: the page index
+    is a division there)."""
+    B, Nq, Hq, Hkv, d, P = 2, 1, 8, 2, 128, 384
+    lens = [2000, 385]
+    q, kc, vc, table, mb, npg = paged_problem(B, Nq, Hq, Hkv, d, P, lens, 77)
+    o, lse, _ = run_paged(q, kc, vc, table, mb, npg, P, lens, False)
+    oo, lo = oracle.attn_decode_paged_oracle(q, kc, vc, lens, table, P, False, d ** -0.5)
+    compare(o, lse, oo, lo, "paged P=384")
+
+
 def test_paged_matches_contiguous_decode():
     """Pages laid out in order are the contiguous caches: the two entry
     points give the same bits."""
