@@ -14,16 +14,19 @@
 // exp2 with log2 e folded into the scale) and P V stay in fp32 registers.
 //
 // A CTA (16 warps; 8 for R > 4, whose registers fill the file at 8) owns
-// one (sequence, kv head, split of the keys).  Per step
-// each warp takes U key slots of KPW keys (one key per lane group).  Its
-// lanes copy their 16-byte pieces of those K and V rows with cp.async into a
-// ring of NST stages in shared memory -- each lane's own 16 bytes per row
-// and slot, which only that lane reads back, so no barrier orders them -- and
-// keep NST - 1 steps of copies in flight while they compute on the oldest:
-// the R scores of each key (a dot product over the lane group), one move of
-// the running max per step, and p V.  Warps keep separate (m, l, o) states,
-// merged through shared memory at the end; the split's state goes to the
-// output (one split) or to the workspace for attn_combine_kernel.
+// one (sequence, kv head, split of the keys).  Per step each warp takes U
+// key slots of KPW keys (one key per lane group); one lane per key finds its
+// row (through the page table) and shares it by shuffle.  The lanes copy
+// their 16-byte pieces of the K and V rows with cp.async into a ring of NST
+// stages in shared memory -- each lane's own 16 bytes per row and slot,
+// which only that lane reads back, so no barrier orders them -- and keep
+// NST - 1 steps of copies in flight while they compute on the oldest: the R
+// partial dot products of each key in f32 pairs, reduced over the lane group
+// by a transposed butterfly that leaves each lane one row's score (so a lane
+// exponentiates once per key and keeps one running max and sum), then p V
+// for every row.  Warps keep separate (m, l, o) states, merged through
+// shared memory at the end; the split's state goes to the output (one
+// split) or to the workspace for attn_combine_kernel.
 
 namespace attn {
 namespace dcc {
@@ -35,16 +38,6 @@ constexpr int STAGE_BYTES = U * 2 * 32 * 16;
 // thread) and its ring in shared memory (NST x 4 KB)
 __host__ __device__ constexpr int warps_for(int rp) { return rp <= 4 ? 16 : 8; }
 __host__ __device__ constexpr int ring_bytes(int rp) { return warps_for(rp) * NST * STAGE_BYTES; }
-
-// 8 bf16 (a 16-byte load) widened to fp32.
-__device__ __forceinline__ void widen8(const uint4 w, float (&f)[8]) {
-  const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(x[i] << 16);
-    f[2 * i + 1] = __uint_as_float(x[i] & 0xFFFF0000u);
-  }
-}
 
 // 16 bytes global -> shared, bypassing L1; src_bytes 0 writes zeros and
 // reads nothing.

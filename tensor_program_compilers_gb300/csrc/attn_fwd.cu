@@ -1863,18 +1863,18 @@ static attn_status decode_impl(const void *q, const void *k, const void *v, void
                           stream))
       return ATTN_ERR_CUDA;
   } else {
-  const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
-  const unsigned gr = (unsigned)grid;
-  switch (d * 2 + (pg ? 1 : 0)) {   // no Q tensor map: decode gathers its query rows
-    case 128: attn_fwd_kernel<64, 2><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    case 129: attn_fwd_kernel<64, 3><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    case 256: attn_fwd_kernel<128, 2><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    case 257: attn_fwd_kernel<128, 3><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    case 512: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
-    default: attn_fwd_kernel<256, 3><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    const long long grid = units <= 2LL * g_sm_count[dev] ? units : (long long)g_sm_count[dev];
+    const unsigned gr = (unsigned)grid;
+    switch (d * 2 + (pg ? 1 : 0)) {   // no Q tensor map: decode gathers its query rows
+      case 128: attn_fwd_kernel<64, 2><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+      case 129: attn_fwd_kernel<64, 3><<<gr, THREADS, Cfg<64>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+      case 256: attn_fwd_kernel<128, 2><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+      case 257: attn_fwd_kernel<128, 3><<<gr, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+      case 512: attn_fwd_kernel<256, 2><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+      default: attn_fwd_kernel<256, 3><<<gr, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(mk, mk, mv, p); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
-  }
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   if (splits > 1) {
     const unsigned cg = (unsigned)(((long long)B * Hq * Nq + 7) / 8);
     switch (d) {
