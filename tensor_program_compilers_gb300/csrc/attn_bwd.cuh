@@ -617,9 +617,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tma_load_3d(kdst + c * CHUNK_BYTES, &tm_k, ctl.bar(B_KFULL0 + ks), c * 64, kvh,
                       row0 + s * BM);
         ++issued;
+        // V slot vs held V(s - 2), read by dP(s - 2), whose buffer (s - 2) & 1 = vs
+        // completes its barrier: that completion frees the slot (no commit of
+        // its own; the barrier cannot run ahead, dP(s) needing V(s))
+        static_assert(C::V_STAGES == 2, "V slots pair with the two dP buffers");
         if (s >= C::V_STAGES &&
-            !(ok = wait_bounded(ctl.bar(B_EMPTY0 + vs), (uint32_t)(s / C::V_STAGES - 1) & 1u,
-                                abort_flag, p.timeout_ns)))
+            !(ok = wait_bounded(ctl.bar(vs ? B_DP1 : B_DPT_FULL),
+                                (uint32_t)(s / C::V_STAGES - 1) & 1u, abort_flag, p.timeout_ns)))
           break;
         const uint32_t vdst = base + C::B_OFF_V + vs * C::TILE;
         mbar_arrive_expect_tx(ctl.bar(B_FULL0 + vs), C::TILE);
@@ -664,7 +668,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tc_fence_after();
           issue_qk_warp<D>(tmem + COL_DP, dodesc, smem_desc_sw128(vring, 16, 1024));
           tc_commit_warp(ctl.bar(B_DPT_FULL));
-          tc_commit_warp(ctl.bar(B_EMPTY0));   // V(0) is read
         }
       }
       for (int s = 0; ok && s < steps; ++s) {
@@ -687,7 +690,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           issue_qk_warp<D>(tmem + COL_DP + 128u * bn, dodesc,
                            smem_desc_sw128(vring + vn * C::TILE, 16, 1024));
           tc_commit_warp(ctl.bar(bn ? B_DP1 : B_DPT_FULL));
-          tc_commit_warp(ctl.bar(B_EMPTY0 + vn));   // V(s+1) is read once dP is done
         }
         // dS(s) over buffer s & 1 (one barrier per buffer: the softmax warps
         // may finish step s + 1 before this wait returns)
