@@ -100,12 +100,12 @@ def measured_peaks() -> dict:
 
 
 def kernel_source_hash(forward_only: bool = False) -> str:
-    """Hash of the kernel sources (forward_only: without the backward's
-    headers, which define no forward kernel)."""
+    """Hash of the kernel sources (forward_only: without the backward's and
+    the CUDA-core decode's headers, which define no forward kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_program_compilers_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if forward_only and name.startswith("attn_bwd"):
+        if forward_only and name.startswith(("attn_bwd", "attn_decode_cc")):
             continue
         if name.endswith((".cu", ".cuh")):
             with open(os.path.join(csrc, name), "rb") as f:
