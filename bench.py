@@ -432,7 +432,12 @@ BWD_SHAPES = {
     # the long head-dim-256 prefill shape; three kernels (dV, dK, dQ) compute
     # sixteen products of the forward's per-block size
     "backward256": (1, 16, 2, 16384, 256),
+    # the GQA prefill shape at head dim 64, through the two-kernel path and
+    # through the single pass (five products; dQ by bulk reduce-adds)
+    "backward64": (2, 32, 8, 4096, 64),
+    "backward64_single": (2, 32, 8, 4096, 64),
 }
+BWD_SINGLE_PASS = {"backward64_single"}
 
 
 def run_backward(pkg, dev, flush, steps, shape="backward", seqlen=None):
@@ -450,17 +455,21 @@ def run_backward(pkg, dev, flush, steps, shape="backward", seqlen=None):
     do = torch.randn((B, N, Hq, d), generator=g).to(torch.bfloat16).to(dev)
     o, lse = pkg.attention(q, k, v, causal=True)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    n = pkg.attn_bwd_workspace_bytes(B, Hq, N)
+    single = shape in BWD_SINGLE_PASS
+    n = (pkg.attn_bwd_single_pass_workspace_bytes if single else pkg.attn_bwd_workspace_bytes)(
+        B, Hq, N)
     ws = torch.empty(((n + 15) // 16 * 4,), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    step = lambda: pkg.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
-                                True, workspace=ws, stream=stream.cuda_stream)
+    run = pkg.attn_bwd_single_pass if single else pkg.attn_bwd
+    step = lambda: run(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5, True,
+                       workspace=ws, stream=stream.cuda_stream)
     t = statistics.median(time_steps(step, steps, 3, flush, stream))
     st = pkg.attn_get_status(stream.cuda_stream)
     if st != pkg.ATTN_OK:
         raise RuntimeError(f"backward run: {pkg.attn_status_string(st)}")
     fwd_flops = 4.0 * B * Hq * N * N * d / 2
-    return {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} causal",
+    return {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} causal"
+                        + (", single pass" if single else ""),
             "tflops": round(2.5 * fwd_flops / (t / 1e3) / 1e12, 2), "ms_per_step": round(t, 5),
             "flop_convention": "2.5 x forward"}
 
@@ -683,6 +692,8 @@ def native(args):
         per_workload["backward"] = run_backward(pkg, dev, flush, min(args.steps, 20))
         per_workload["backward256"] = run_backward(pkg, dev, flush, min(args.steps, 10),
                                                    "backward256")
+        for key in ("backward64", "backward64_single"):
+            per_workload[key] = run_backward(pkg, dev, flush, min(args.steps, 20), key)
 
     base = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -771,8 +782,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-rows-per-head", type=int, default=24)
-    ap.add_argument("--extra", choices=["window", "decode", "decode_paged", "backward",
-                                        "backward256"],
+    ap.add_argument("--extra", choices=["window", "decode", "decode_paged", *BWD_SHAPES],
                     default=None,
                     help="time only this extra path (one JSON line; for profiling)")
     a = ap.parse_args(argv)
@@ -792,7 +802,7 @@ def extra_only(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.extra == "window":
         out = run_window(pkg, dev, flush, args.steps)
-    elif args.extra in ("backward", "backward256"):
+    elif args.extra in BWD_SHAPES:
         out = run_backward(pkg, dev, flush, args.steps, args.extra, args.bwd_seqlen)
     elif args.extra == "decode_paged":
         out = run_decode_paged(pkg, dev, flush, args.steps, measured_peaks().get("hbm_gbs"))

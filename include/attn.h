@@ -255,6 +255,31 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      cudaStream_t stream);
 
 /*
+ * attn_bwd_single_pass -- the same gradients as attn_bwd, for d = 64, in one
+ * kernel per (kv head, 128-key block) (tang, section 8.3 "Attention backward
+ * on Hopper": one kernel per key block, dK and dV held on chip, dQ added
+ * with bulk asynchronous reductions).  Each key block adds its share of dQ,
+ * dS K, into an fp32 buffer in the workspace with bulk tensor reduce-adds;
+ * a last pass writes dq = scale x that buffer in bf16.  Five matrix products
+ * per (key block, query block) pair instead of attn_bwd's seven.
+ *
+ * Arguments, layouts, ownership and errors as attn_bwd, except:
+ *   d        : 64 only (anything else is ATTN_ERR_INVALID_ARG);
+ *   workspace: at least attn_bwd_single_pass_workspace_bytes(B, Hq, N,
+ *              cu_seqlens != NULL) bytes, 16-byte aligned: the fp32 dQ
+ *              buffer (Hq x padded rows x 64) followed by attn_bwd's.
+ * dk and dv are bitwise those of attn_bwd.  dq is not bitwise reproducible:
+ * the key blocks' fp32 shares are added in the order they arrive, so its
+ * rounding can differ between runs (its accuracy does not).
+ */
+size_t attn_bwd_single_pass_workspace_bytes(int B, int Hq, int N, int packed);
+attn_status attn_bwd_single_pass(const void *q, const void *k, const void *v, const void *o,
+                                 const void *dout, const float *lse, void *dq, void *dk,
+                                 void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                                 int causal, const int *cu_seqlens, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * attn_get_status -- takes and clears the current device's status word (the
  * first device-side error recorded since the last read) in one atomic
  * exchange, ordered on `stream` after the work already queued there, then

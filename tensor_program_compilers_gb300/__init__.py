@@ -23,6 +23,7 @@ SOURCES = [os.path.join(_CSRC, "attn_fwd.cu")]
 DEPENDS = SOURCES + [os.path.join(_CSRC, "ptx.cuh"), os.path.join(_CSRC, "attn_bwd.cuh"),
                      os.path.join(_CSRC, "attn_fwd2.cuh"), os.path.join(_CSRC, "attn_bwd256.cuh"),
                      os.path.join(_CSRC, "attn_decode_cc.cuh"),
+                     os.path.join(_CSRC, "attn_bwd_fused.cuh"),
                      os.path.join(INCLUDE_DIR, "attn.h")]
 
 NVCC_FLAGS = [
@@ -44,6 +45,7 @@ ATTN_ERR_BAD_PAGE_TABLE = 7
 EXPORTED = ["attn_fwd", "attn_fwd_ex", "attn_fwd_decode", "attn_decode_workspace_bytes",
             "attn_fwd_decode_paged", "attn_decode_paged_workspace_bytes",
             "attn_fwd_decode_static", "attn_bwd", "attn_bwd_workspace_bytes",
+            "attn_bwd_single_pass", "attn_bwd_single_pass_workspace_bytes",
             "attn_get_status", "attn_status_string", "attn_selftest_timeout",
             "attn_debug_one_tile", "attn_probe_dram_latency"]
 
@@ -111,6 +113,10 @@ def _load():
                                  ctypes.c_float, i, vp, vp, ctypes.c_size_t, vp]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.attn_bwd_single_pass.restype = i
+        lib.attn_bwd_single_pass.argtypes = lib.attn_bwd.argtypes
+        lib.attn_bwd_single_pass_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_single_pass_workspace_bytes.argtypes = [i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
         lib.attn_get_status.restype = i
@@ -262,11 +268,35 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
     return rc
 
 
+def attn_bwd_single_pass_workspace_bytes(B, Hq, N, packed=False) -> int:
+    """Workspace bytes ``attn_bwd_single_pass`` needs (the fp32 dQ buffer,
+    then ``attn_bwd``'s)."""
+    return int(_load().attn_bwd_single_pass_workspace_bytes(int(B), int(Hq), int(N),
+                                                            int(bool(packed))))
+
+
+def attn_bwd_single_pass(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+                         cu_seqlens=None, workspace=None, workspace_bytes=None, stream=None,
+                         check=True) -> int:
+    """Call the C ``attn_bwd_single_pass`` (d = 64): arguments as ``attn_bwd``."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    rc = _load().attn_bwd_single_pass(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        int(B), int(Hq), int(Hkv), int(N), int(d), float(scale), int(bool(causal)),
+        _ptr(cu_seqlens), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if check and rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_single_pass")
+    return rc
+
+
 def attention_backward(q, k, v, o, lse, dout, causal: bool, scale: Optional[float] = None,
-                       cu_seqlens=None, stream=None):
+                       cu_seqlens=None, stream=None, single_pass: bool = False):
     """Allocate dq, dk, dv and the workspace (torch, on q's device) and run
-    ``attn_bwd``: fixed batch q [B, N, Hq, d], k/v [B, N, Hkv, d], or packed
-    q [T, Hq, d], k/v [T, Hkv, d] with cu_seqlens (int32 [B+1], device)."""
+    ``attn_bwd`` (or, single_pass and d = 64, ``attn_bwd_single_pass``):
+    fixed batch q [B, N, Hq, d], k/v [B, N, Hkv, d], or packed q [T, Hq, d],
+    k/v [T, Hkv, d] with cu_seqlens (int32 [B+1], device)."""
     import torch
     d = q.shape[-1]
     if cu_seqlens is None:
@@ -278,10 +308,12 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool, scale: Optional[floa
         B = cu_seqlens.numel() - 1
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    n = attn_bwd_workspace_bytes(B, Hq, N, packed=cu_seqlens is not None)
+    size = attn_bwd_single_pass_workspace_bytes if single_pass else attn_bwd_workspace_bytes
+    n = size(B, Hq, N, packed=cu_seqlens is not None)
     ws = torch.empty(((max(n, 16) + 15) // 16 * 4,), dtype=torch.float32, device=q.device)
-    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, ws,
-             stream=stream)
+    run = attn_bwd_single_pass if single_pass else attn_bwd
+    run(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, ws,
+        stream=stream)
     return dq, dk, dv
 
 

@@ -42,6 +42,7 @@ struct BwdParams {
   int *pstart;           // [B+1] padded start of each sequence (set-up pass)
   float *lse2;           // [Hq, rows_pad]: LSE log2(e); +inf on padding rows
   float *dsum;           // [Hq, rows_pad]: D = rowsum(dO o O); 0 on padding rows
+  float *dq_acc;         // single pass, d = 64: [Hq, rows_pad, 64] fp32 dS K sums
   int B, Hq, Hkv, N, T, nb_max, group, causal;
   float scale, scale_log2;
   unsigned long long timeout_ns;
@@ -169,8 +170,9 @@ enum : int {
 // ------------------------------------------------------------------ row pass
 // Eight lanes per (head, padded row), 16-byte loads: D = sum_c dO o O and
 // LSE log2(e); padding rows of a sequence get D = 0 and +inf, which zeroes
-// their P in the kernels.
-template <int D>
+// their P in the kernels.  ZERO_ACC (single pass, d = 64): the row of the
+// fp32 dQ buffer is zeroed as well.
+template <int D, bool ZERO_ACC = false>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31, seg = lane & 7;
   const long long row = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);   // h rows_pad + r
@@ -181,6 +183,11 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   const int b = live ? seq_of_padded_row(p, r) : 0;
   const int i = r - p.pstart[b];
   const bool pad = live && i >= p.seq_len(b);
+  if (ZERO_ACC && live) {
+    float4 *z = reinterpret_cast<float4 *>(p.dq_acc + row * 64 + seg * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   live = live && !pad;
   constexpr int PER = D / 8;   // elements per lane: PER / 8 loads of 16 bytes
   float acc = 0.f;
@@ -811,6 +818,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }  // namespace attn
 
 #include "attn_bwd256.cuh"
+#include "attn_bwd_fused.cuh"
 
 // ------------------------------------------------------------------ host
 namespace attn {
@@ -818,27 +826,44 @@ namespace bwd {
 // Padded 128-row blocks of all sequences: B ceil(N / 128) for a fixed batch
 // is at most ceil(rows / 128) + B, which also bounds a packed batch.
 static long long bwd_nb_max(int B, long long rows) { return (rows + BM - 1) / BM + B; }
-}  // namespace bwd
-}  // namespace attn
 
-extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int packed) {
-  if (B < 1 || Hq < 1 || N < 1) return 0;
+// Bytes of the fp32 dQ buffer of the single pass (d = 64), 0 otherwise.
+static size_t bwd_acc_bytes(int B, int Hq, int N, int packed) {
   const long long rows = packed ? (long long)N : (long long)B * N;
-  const size_t rows_pad = (size_t)attn::bwd::bwd_nb_max(B, rows) * attn::BM;
-  return 2 * (size_t)Hq * rows_pad * sizeof(float) + ((size_t)B + 1) * sizeof(int);
+  return (size_t)Hq * (size_t)bwd_nb_max(B, rows) * BM * 64 * sizeof(float);
 }
 
-extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                                const void *dout, const float *lse, void *dq, void *dk,
-                                void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
-                                int causal, const int *cu_seqlens, void *workspace,
-                                size_t workspace_bytes, cudaStream_t stream) {
-  using namespace attn;
-  using namespace attn::bwd;
+// fp32 [rows, 64] buffer seen as 32 x 32 boxes, 128-byte swizzle: the
+// target of the single pass's reduce-adds.
+static bool make_acc_map(EncodeTiledFn enc, CUtensorMap *m, float *base, long long rows) {
+  cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {64 * sizeof(float)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// Argument checks, the per-device shared-memory opt-in, the tensor maps of
+// Q, dO, K, V and the parameters, shared by both backward entry points.
+// single: the single pass (d = 64, the fp32 dQ buffer at the workspace's
+// start).  Returns ATTN_OK with *empty set when there is nothing to do.
+static attn_status bwd_prepare(const void *q, const void *k, const void *v, const void *o,
+                               const void *dout, const float *lse, void *dq, void *dk,
+                               void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                               int causal, const int *cu_seqlens, void *workspace,
+                               size_t workspace_bytes, bool single, CUtensorMap (&maps)[5],
+                               BwdParams &p, bool *empty) {
+  *empty = false;
   if (B < 0 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
+  if (single ? d != 64 : (d != 64 && d != 128 && d != 256)) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || N == 0) return ATTN_OK;
+  if (B == 0 || N == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   auto misaligned = [](const void *ptr, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
@@ -851,7 +876,9 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   if (rows > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
   const long long nb_max = bwd_nb_max(B, rows);
   if (nb_max * BM * (long long)Hq > 0x7FFFFFFFLL) return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_workspace_bytes(B, Hq, N, cu_seqlens ? 1 : 0);
+  const int packed = cu_seqlens ? 1 : 0;
+  const size_t acc = single ? bwd_acc_bytes(B, Hq, N, packed) : 0;
+  const size_t need = acc + attn_bwd_workspace_bytes(B, Hq, N, packed);
   if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -869,19 +896,19 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
           !opt_in_smem(attn_bwd_dq_kernel<128>, BCfg<128>::B_SMEM) ||
           !opt_in_smem(attn_bwd_dv256_kernel, B256::V_SMEM) ||
           !opt_in_smem(attn_bwd_dk256_kernel, B256::K_SMEM) ||
-          !opt_in_smem(attn_bwd_dq256_kernel, B256::Q_SMEM))
+          !opt_in_smem(attn_bwd_dq256_kernel, B256::Q_SMEM) ||
+          !opt_in_smem(attn_bwd_fused_kernel, FCfg::SMEM))
         return ATTN_ERR_CUDA;
       ready[dev] = true;
     }
   }
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return ATTN_ERR_CUDA;
-  CUtensorMap mq, mdo, mk, mv;
-  if (!make_map(enc, &mq, q, Hq, rows, d) || !make_map(enc, &mdo, dout, Hq, rows, d) ||
-      !make_map(enc, &mk, k, Hkv, rows, d) || !make_map(enc, &mv, v, Hkv, rows, d))
+  if (!make_map(enc, &maps[0], q, Hq, rows, d) || !make_map(enc, &maps[1], dout, Hq, rows, d) ||
+      !make_map(enc, &maps[2], k, Hkv, rows, d) || !make_map(enc, &maps[3], v, Hkv, rows, d))
     return ATTN_ERR_INVALID_ARG;
 
-  BwdParams p{};
+  p = BwdParams{};
   p.dq = reinterpret_cast<__nv_bfloat16 *>(dq);
   p.dk = reinterpret_cast<__nv_bfloat16 *>(dk);
   p.dv = reinterpret_cast<__nv_bfloat16 *>(dv);
@@ -890,7 +917,8 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   p.lse = lse;
   p.cu = cu_seqlens;
   p.nb_max = (int)nb_max;
-  p.lse2 = reinterpret_cast<float *>(workspace);
+  p.dq_acc = single ? reinterpret_cast<float *>(workspace) : nullptr;
+  p.lse2 = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + acc);
   p.dsum = p.lse2 + (size_t)Hq * nb_max * BM;
   p.pstart = reinterpret_cast<int *>(p.dsum + (size_t)Hq * nb_max * BM);
   p.B = B;
@@ -903,10 +931,38 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
+  if (single && !make_acc_map(enc, &maps[4], p.dq_acc, (long long)Hq * nb_max * BM))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+}  // namespace bwd
+}  // namespace attn
 
-  const unsigned row_blocks = (unsigned)(((long long)Hq * nb_max * BM + 31) / 32);
-  const unsigned kv_units = (unsigned)((long long)Hkv * nb_max);
-  const unsigned q_units = (unsigned)((long long)Hq * nb_max);
+extern "C" size_t attn_bwd_workspace_bytes(int B, int Hq, int N, int packed) {
+  if (B < 1 || Hq < 1 || N < 1) return 0;
+  const long long rows = packed ? (long long)N : (long long)B * N;
+  const size_t rows_pad = (size_t)attn::bwd::bwd_nb_max(B, rows) * attn::BM;
+  return 2 * (size_t)Hq * rows_pad * sizeof(float) + ((size_t)B + 1) * sizeof(int);
+}
+
+extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                                const void *dout, const float *lse, void *dq, void *dk,
+                                void *dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                                int causal, const int *cu_seqlens, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  using namespace attn;
+  using namespace attn::bwd;
+  CUtensorMap maps[5];
+  BwdParams p;
+  bool empty = false;
+  const attn_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
+                                     causal, cu_seqlens, workspace, workspace_bytes, false, maps,
+                                     p, &empty);
+  if (st != ATTN_OK || empty) return st;
+  const CUtensorMap &mq = maps[0], &mdo = maps[1], &mk = maps[2], &mv = maps[3];
+  const unsigned row_blocks = (unsigned)(((long long)Hq * p.nb_max * BM + 31) / 32);
+  const unsigned kv_units = (unsigned)((long long)Hkv * p.nb_max);
+  const unsigned q_units = (unsigned)((long long)Hq * p.nb_max);
   bwd_setup_kernel<<<1, 32, 0, stream>>>(p);
   if (d == 64) {
     bwd_rows_kernel<64><<<row_blocks, 256, 0, stream>>>(p);
@@ -923,5 +979,35 @@ extern "C" attn_status attn_bwd(const void *q, const void *k, const void *v, con
     attn_bwd_dk256_kernel<<<2 * kv_units, BWD_THREADS, B256::K_SMEM, stream>>>(mq, mdo, mk, mv, p);
     attn_bwd_dq256_kernel<<<q_units, BWD_THREADS, B256::Q_SMEM, stream>>>(mq, mdo, mk, mv, p);
   }
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" size_t attn_bwd_single_pass_workspace_bytes(int B, int Hq, int N, int packed) {
+  if (B < 1 || Hq < 1 || N < 1) return 0;
+  return attn::bwd::bwd_acc_bytes(B, Hq, N, packed) + attn_bwd_workspace_bytes(B, Hq, N, packed);
+}
+
+extern "C" attn_status attn_bwd_single_pass(const void *q, const void *k, const void *v,
+                                            const void *o, const void *dout, const float *lse,
+                                            void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                                            int N, int d, float scale, int causal,
+                                            const int *cu_seqlens, void *workspace,
+                                            size_t workspace_bytes, cudaStream_t stream) {
+  using namespace attn;
+  using namespace attn::bwd;
+  CUtensorMap maps[5];
+  BwdParams p;
+  bool empty = false;
+  const attn_status st = bwd_prepare(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
+                                     causal, cu_seqlens, workspace, workspace_bytes, true, maps,
+                                     p, &empty);
+  if (st != ATTN_OK || empty) return st;
+  const unsigned row_blocks = (unsigned)(((long long)Hq * p.nb_max * BM + 31) / 32);
+  const unsigned kv_units = (unsigned)((long long)Hkv * p.nb_max);
+  bwd_setup_kernel<<<1, 32, 0, stream>>>(p);
+  bwd_rows_kernel<64, true><<<row_blocks, 256, 0, stream>>>(p);
+  attn_bwd_fused_kernel<<<kv_units, BWD_THREADS, FCfg::SMEM, stream>>>(maps[0], maps[1], maps[2],
+                                                                        maps[3], maps[4], p);
+  bwd_dq_convert_kernel<<<row_blocks, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
