@@ -833,15 +833,15 @@ static size_t bwd_acc_bytes(int B, int Hq, int N, int packed) {
   return (size_t)Hq * (size_t)bwd_nb_max(B, rows) * BM * 64 * sizeof(float);
 }
 
-// fp32 [rows, 64] buffer seen as 32 x 32 boxes, 128-byte swizzle: the
-// target of the single pass's reduce-adds.
+// fp32 [rows, 64] buffer seen as boxes of 32 rows x 16 columns, 64-byte
+// swizzle: the target of the single pass's reduce-adds.
 static bool make_acc_map(EncodeTiledFn enc, CUtensorMap *m, float *base, long long rows) {
   cuuint64_t dims[2] = {64, (cuuint64_t)rows};
   cuuint64_t strides[1] = {64 * sizeof(float)};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {16, 32};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
@@ -1006,8 +1006,8 @@ extern "C" attn_status attn_bwd_single_pass(const void *q, const void *k, const 
   const unsigned kv_units = (unsigned)((long long)Hkv * p.nb_max);
   bwd_setup_kernel<<<1, 32, 0, stream>>>(p);
   bwd_rows_kernel<64, true><<<row_blocks, 256, 0, stream>>>(p);
-  attn_bwd_fused_kernel<<<kv_units, BWD_THREADS, FCfg::SMEM, stream>>>(maps[0], maps[1], maps[2],
-                                                                        maps[3], maps[4], p);
+  attn_bwd_fused_kernel<<<kv_units, F_THREADS, FCfg::SMEM, stream>>>(maps[0], maps[1], maps[2],
+                                                                      maps[3], maps[4], p);
   bwd_dq_convert_kernel<<<row_blocks, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -16,15 +16,23 @@
 // them, so dq's fp32 rounding (not its value within the tolerance) varies
 // from run to run.
 //
-// Tensor memory: S^T [0,128) (P^T bf16 over its first 64 columns), dP^T
-// [128,256) (dS^T over its first 64), dV [256,320), dK [320,384), the dQ
-// share [384,448).  The dQ product takes dS from shared memory: the softmax
-// warps write their dS^T rows there as well, in the 128-byte-swizzled
-// layout with the query index contiguous (an M-major A operand), and K
-// serves both as the K-major A of S^T and as the N-major B of dS K.
+// Tensor memory: S^T [0,128) (P^T bf16 over the first 16 of each 32
+// columns), dP^T [128,256), dV [256,320), dK [320,384), the dQ share
+// [384,448), dS^T in bf16 [448,512) (the A operand of dK).  The dQ product
+// takes dS from shared memory: the softmax warps also write their dS^T rows
+// there (one 128-byte swizzled line per key, the query index contiguous: an
+// M-major A operand), and K serves both as the K-major A of S^T and as the
+// N-major B of dS K.
 
 namespace attn {
 namespace bwd {
+
+// producer, MMA issuer, 16 softmax warps (four per TMEM lane quarter, one per
+// 32 of the 128 columns of a score tile: four warps per sub-partition hide
+// one another's TMEM and shared-memory latencies), and four dQ warps (one
+// per lane quarter) that move the dQ share out, off the softmax warps' path
+constexpr int F_SM_WARPS = 16, F_DQ_WARPS = 4;
+constexpr int F_THREADS = 64 + 32 * (F_SM_WARPS + F_DQ_WARPS);
 
 struct FCfg {
   static constexpr int D = 64;
@@ -32,9 +40,9 @@ struct FCfg {
   static constexpr uint32_t SLOT = 2 * TILE + 1024;              // Q, dO, lse2 row, dsum row
   static constexpr uint32_t OFF_RING = 2 * TILE;                 // after K, V
   static constexpr uint32_t OFF_DS = OFF_RING + 2 * SLOT;        // dS, 128 queries x 128 keys
-  static constexpr uint32_t OFF_STG = OFF_DS + 2 * TILE;         // 8 warps x 32 rows x 32 fp32
-  static constexpr uint32_t STG_WARP = 32 * 128;
-  static constexpr uint32_t OFF_CTL = OFF_STG + BWD_SM_WARPS * STG_WARP;
+  static constexpr uint32_t OFF_STG = OFF_DS + 2 * TILE;         // 4 dQ warps x 32 rows x 64 fp32
+  static constexpr uint32_t STG_WARP = 32 * 256;                 // four boxes of 16 columns
+  static constexpr uint32_t OFF_CTL = OFF_STG + F_DQ_WARPS * STG_WARP;
   static constexpr uint32_t CTL_BYTES = 256;
   static constexpr uint32_t SMEM = OFF_CTL + CTL_BYTES + 1024;
   static_assert(OFF_DS % 1024 == 0 && OFF_STG % 1024 == 0, "swizzle atoms");
@@ -52,8 +60,9 @@ enum : int {
   F_ST,           // S^T of the step in TMEM
   F_DPT,          // dP^T of the step in TMEM
   F_PT,           // softmax warps: P^T written
-  F_DST,          // softmax warps: dS^T written (TMEM and shared memory), dQ share read
+  F_DST,          // softmax warps: dS^T written (TMEM and shared memory)
   F_DQ,           // the step's dQ share in TMEM
+  F_DQ_READ,      // dQ warps: the share loaded (its columns are free)
   F_COUNT
 };
 static_assert(8 * F_COUNT + 8 <= (int)FCfg::CTL_BYTES, "control block");
@@ -81,38 +90,96 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns: thread t gets lane (base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// A (K = 128 queries, bf16 pairs in TMEM) times B (N-major shared-memory
+// tile, 64 columns), accumulated into d_tmem (overwritten unless
+// accumulate).  Each softmax warp packs its 32 query columns into the first
+// 16 of the 32 TMEM columns it read itself (so no warp writes columns that
+// another still reads): queries 16 kk .. 16 kk + 15 sit at columns
+// 32 (kk / 2) + 8 (kk % 2).
+__device__ __forceinline__ void issue_pv_quarters_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                       uint64_t bdesc, bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(64, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_warp(d_tmem, a_tmem + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1),
+                bdesc + (uint64_t)((kk * 2048) >> 4), IDESC, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dK += dS^T Q: A = dS^T in TMEM (bf16 pairs, queries 16 kk .. 16 kk + 15 at
+// column 8 kk), B = Q (queries x head dim, N-major, 16 queries = 2048 bytes
+// per step).  (With A read from shared memory instead, an N = 64 product
+// needs more shared-memory bandwidth per cycle than the SM has.)
+__device__ __forceinline__ void issue_dk_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t q_mn,
+                                              bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(64, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_warp(d_tmem, a_tmem + 8u * (uint32_t)kk, q_mn + (uint64_t)((kk * 2048) >> 4), IDESC,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // Instruction descriptor for dS K: A (dS) and B (K) both stored with the
 // M / N index contiguous.
 constexpr uint32_t IDESC_DQ = idesc_bf16_f32(64, 1) | (1u << 15);
 
-// One warp's share of the dQ product: rows 32 wq .. 32 wq + 31 of the query
-// block, columns 32 hf .. 32 hf + 31, from TMEM into the warp's staging box
-// (128-byte swizzle, one 128-byte line per row) and reduce-added into the
-// buffer at (column c0, buffer row c1).  Lane 0 first waits until the
-// warp's previous reduce-add has read the box (issued a step earlier).
-__device__ __forceinline__ void dq_share_out(uint32_t taddr, uint32_t stg,
-                                             const CUtensorMap *map, int c0, int c1) {
+// A dQ warp's part of the share: rows 32 wq .. 32 wq + 31 of the query block,
+// all 64 columns, loaded from TMEM (then released on F_DQ_READ), written to
+// the warp's staging area as four boxes of 16 columns (64-byte swizzle: one
+// 64-byte line per row, its 16-byte pieces permuted by bits 1-2 of the row)
+// and reduce-added into the buffer at buffer row c1.  Lane 0 first waits
+// until the warp's previous reduce-adds have read the area.
+__device__ __forceinline__ void dq_share_out(uint32_t taddr, uint32_t stg, uint32_t read_bar,
+                                             const CUtensorMap *map, int c1) {
   const int lane = threadIdx.x & 31;
-  uint32_t u[32];
-  tmem_ld32(taddr, u);
+  uint32_t u0[32], u1[32];
+  tmem_ld32(taddr, u0);
+  tmem_ld32(taddr + 32, u1);
   tmem_wait_ld();
-  reg_fence32(u);
+  reg_fence32(u0);
+  reg_fence32(u1);
+  tc_fence_before();
+  warp_arrive(read_bar);
   if (lane == 0) bulk_wait_read_all();
   __syncwarp();
-  const uint32_t line = stg + (uint32_t)lane * 128u;
+  const uint32_t line = stg + (uint32_t)lane * 64u;
+  const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    st_shared_v4(line + ((uint32_t)(j ^ (lane & 7)) << 4),
-                 make_uint4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]));
+  for (int j = 0; j < 4; ++j) {
+    st_shared_v4(line + ((j ^ sw) << 4), make_uint4(u0[4 * j], u0[4 * j + 1], u0[4 * j + 2], u0[4 * j + 3]));
+    st_shared_v4(line + 2048 + ((j ^ sw) << 4),
+                 make_uint4(u0[16 + 4 * j], u0[17 + 4 * j], u0[18 + 4 * j], u0[19 + 4 * j]));
+    st_shared_v4(line + 4096 + ((j ^ sw) << 4),
+                 make_uint4(u1[4 * j], u1[4 * j + 1], u1[4 * j + 2], u1[4 * j + 3]));
+    st_shared_v4(line + 6144 + ((j ^ sw) << 4),
+                 make_uint4(u1[16 + 4 * j], u1[17 + 4 * j], u1[18 + 4 * j], u1[19 + 4 * j]));
+  }
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_reduce_add_2d(map, c0, c1, stg);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_reduce_add_2d(map, 16 * q, c1, stg + 2048u * q);
     bulk_commit_group();
   }
 }
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(F_THREADS, 1)
     attn_bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_do,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -149,9 +216,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(bar(F_DRAIN), 1);
       mbar_init(bar(F_ST), 1);
       mbar_init(bar(F_DPT), 1);
-      mbar_init(bar(F_PT), BWD_SM_WARPS);
-      mbar_init(bar(F_DST), BWD_SM_WARPS);
+      mbar_init(bar(F_PT), F_SM_WARPS);
+      mbar_init(bar(F_DST), F_SM_WARPS);
       mbar_init(bar(F_DQ), 1);
+      mbar_init(bar(F_DQ_READ), F_DQ_WARPS);
       words[1] = 0u;
       mbar_init_fence();
     }
@@ -169,7 +237,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = words[0];
-  constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384;
+  constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384,
+                     COL_DS = 448;
 
   if (warp == 0) {
     // producer: K, V once, then Q(s), dO(s) and the two rows of each step
@@ -209,10 +278,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // MMA issuer (whole warp, one elected lane issues).  Per step s: dV +=
     // P^T(s) dO(s) once P^T is written; S^T(s+1) (its columns are free once
     // dV(s) has read P^T: one thread's MMAs run in issue order); then, once
-    // dS is written, dK += dS^T(s) Q(s), dQ share = dS(s) K, and dP^T(s+1).
-    // dQ(s) overwrites the share that the softmax warps read before
-    // writing dS(s); the softmax warps rewrite the shared dS tile only after
-    // dP^T(s+1), which follows dQ(s), has completed.
+    // dS(s) is written, dK += dS^T(s) Q(s), the dQ share dS(s) K, and
+    // dP^T(s+1).  dQ(s) overwrites the share once the dQ warps have loaded
+    // the previous one; the softmax warps rewrite dS^T (TMEM) and the dS tile
+    // only after dP^T(s+1), which follows dQ(s), has completed.  (Issuing
+    // dP^T(s+1) before dK(s) and dQ(s), as soon as dP^T(s) is loaded, was
+    // measured slower: the next step's dQ share then waits longer.)
     const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
     const uint64_t vdesc = smem_desc_sw128(v_s, 16, 1024);
     const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
@@ -234,8 +305,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
       if (!(ok = wait_warp(bar(F_PT), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
       tc_fence_after();
-      issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 0, s > 0);
-      issue_pv_half_warp<D>(tmem + COL_DV, tmem + COL_ST, do_mn, 1, s > 0);
+      issue_pv_quarters_warp(tmem + COL_DV, tmem + COL_ST, do_mn, s > 0);
       const bool more = s + 1 < steps;
       if (more) {
         if (!(ok = wait_warp(bar(F_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
@@ -247,9 +317,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!(ok = wait_warp(bar(F_DST), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
       tc_fence_after();
-      issue_pv_half_warp<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 0, s > 0);
-      issue_pv_half_warp<D>(tmem + COL_DK, tmem + COL_DPT, q_mn, 1, s > 0);
+      issue_dk_warp(tmem + COL_DK, tmem + COL_DS, q_mn, s > 0);
       tc_commit_warp(bar(F_EMPTY0 + slot));   // Q(s), dO(s) and their rows are read
+      if (s > 0 && !(ok = wait_warp(bar(F_DQ_READ), (uint32_t)(s - 1) & 1u, abort_flag,
+                                    p.timeout_ns)))
+        break;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)   // 16 keys per MMA: two 8-row groups of both operands
         mma_ss_warp(tmem + COL_DQ, ds_mn + (uint64_t)((kk * 2048) >> 4),
@@ -264,25 +336,36 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tc_commit_warp(bar(F_DRAIN));
     wait_drain(bar(F_DRAIN), 0, p.timeout_ns);
     __syncwarp();
+  } else if (warp >= 2 + F_SM_WARPS) {
+    // dQ warps: query rows 32 (warp%4) .. + 31 of each step's block
+    const int wq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t stg = base + C::OFF_STG + (uint32_t)(warp - 2 - F_SM_WARPS) * C::STG_WARP;
+    const long long hrow = (long long)p.pstart[b] + 32 * wq;   // + h rows_pad + ib 128
+    bool ok = true;
+    for (int s = 0; ok && s < steps; ++s) {
+      if (!(ok = wait_warp(bar(F_DQ), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
+      tc_fence_after();
+      const int h = kvh * p.group + s / nq;
+      dq_share_out(tmem + lane_off + COL_DQ, stg, bar(F_DQ_READ), &tm_dqacc,
+                   (int)((long long)h * p.rows_pad() + hrow + (long long)(i0 + s % nq) * BM));
+    }
+    if (lane == 0) bulk_wait_all();   // the reduce-adds are done with the staging area
+    __syncwarp();
   } else {
     // softmax warps: thread = key row jb*128 + row of TMEM lane quarter
-    // warp%4, query columns 64 hf .. 64 hf + 63; for the dQ share, query row
-    // 32 (warp%4) + lane of the step's block, columns 32 hf .. 32 hf + 31
+    // warp%4, query columns 32 cq .. 32 cq + 31 (cq = 0..3; in the shared dS
+    // tile, piece ch = cq % 2 of half hf = cq / 2)
     const int wq = warp & 3;
-    const int hf = (warp - 2) >> 2;
+    const int cq = (warp - 2) >> 2;
+    const int hf = cq >> 1, ch = cq & 1;
+    const int c0 = 32 * cq;
     const int row = wq * 32 + lane;
     const int key = jb * BM + row;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t stg = base + C::OFF_STG + (uint32_t)(warp - 2) * C::STG_WARP;
     const uint32_t ds_line = ds_s + (uint32_t)hf * CHUNK_BYTES + (uint32_t)row * 128u;
     const float c = p.scale_log2;
     const bool kdead = key >= len;
-    const long long hrow = (long long)p.pstart[b] + 32 * wq;   // + h rows_pad + ib 128
-    // buffer row of the share of step t: head and query block of t
-    auto share_row = [&](int t) {
-      const int h = kvh * p.group + t / nq;
-      return (int)((long long)h * p.rows_pad() + hrow + (long long)(i0 + t % nq) * BM);
-    };
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
       const int slot = s & 1;
@@ -299,10 +382,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // phase 1: P^T = 2^(S^T c - LSE2), bf16, kept in registers for dS; a
       // key past the end of its sequence gets P = 0 (its dK, dV rows are not
       // stored, but its dS would enter every query's dQ)
-      uint32_t pw[2][16];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * hf + 32 * ch;
+      uint32_t pw[16];
+      {
         uint32_t us[32];
         tmem_ld32(tmem + lane_off + COL_ST + c0, us);
         tmem_wait_ld();
@@ -311,10 +392,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
           for (int x = 0; x < 32; x += 4) {
             const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c0 + x);
-            pw[ch][x >> 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x]) * c - l4.x),
-                                         ex2_approx(__uint_as_float(us[x + 1]) * c - l4.y));
-            pw[ch][(x >> 1) + 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x + 2]) * c - l4.z),
-                                               ex2_approx(__uint_as_float(us[x + 3]) * c - l4.w));
+            pw[x >> 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x]) * c - l4.x),
+                                     ex2_approx(__uint_as_float(us[x + 1]) * c - l4.y));
+            pw[(x >> 1) + 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x + 2]) * c - l4.z),
+                                           ex2_approx(__uint_as_float(us[x + 3]) * c - l4.w));
           }
         } else {
 #pragma unroll
@@ -325,29 +406,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             // query ib*128 + qc sees key iff query >= key
             if (kdead || (diag && ib * BM + qc < key)) p0 = 0.f;
             if (kdead || (diag && ib * BM + qc + 1 < key)) p1 = 0.f;
-            pw[ch][x >> 1] = pack_bf16x2(p0, p1);
+            pw[x >> 1] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st16(tmem + lane_off + COL_ST + 64 * hf + 16 * ch, pw[ch]);
+        tmem_st16(tmem + lane_off + COL_ST + c0, pw);
       }
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(bar(F_PT));
-      // the previous step's dQ share, while dP^T(s) is formed
-      if (s > 0) {
-        if (!(ok = wait_warp(bar(F_DQ), (uint32_t)(s - 1) & 1u, abort_flag, p.timeout_ns)))
-          break;
-        tc_fence_after();
-        dq_share_out(tmem + lane_off + COL_DQ + 32 * hf, stg, &tm_dqacc, 32 * hf,
-                     share_row(s - 1));
-      }
       // phase 2: dS^T = P^T o (dP^T - D), bf16, into TMEM (for dK) and into
       // the shared dS tile (for dQ)
       if (!(ok = wait_warp(bar(F_DPT), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
       tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * hf + 32 * ch;
+      {
         uint32_t ud[32];
         tmem_ld32(tmem + lane_off + COL_DPT + c0, ud);
         tmem_wait_ld();
@@ -356,7 +427,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
           const float4 d4 = *reinterpret_cast<const float4 *>(dsum + c0 + x);
-          const uint32_t w0 = pw[ch][x >> 1], w1 = pw[ch][(x >> 1) + 1];
+          const uint32_t w0 = pw[x >> 1], w1 = pw[(x >> 1) + 1];
           float a0, a1, a2, a3;
           f2_unpack(f2_mul(bf16x2_widen(w0),
                            f2_add(f2_pack(__uint_as_float(ud[x]), __uint_as_float(ud[x + 1])),
@@ -367,9 +438,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           dw[x >> 1] = pack_bf16x2(a0, a1);
           dw[(x >> 1) + 1] = pack_bf16x2(a2, a3);
         }
-        tmem_st16(tmem + lane_off + COL_DPT + 64 * hf + 16 * ch, dw);
-        // queries 32 ch .. 32 ch + 31 of this half: four 16-byte pieces of
-        // the key's 128-byte line
+        tmem_st16(tmem + lane_off + COL_DS + 16 * cq, dw);
+        // queries 32 cq .. 32 cq + 31: four 16-byte pieces of the key's
+        // 128-byte line in half hf of the tile
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           st_shared_v4(ds_line + ((uint32_t)((4 * ch + j) ^ (row & 7)) << 4),
@@ -380,20 +451,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_before();
       warp_arrive(bar(F_DST));
     }
-    if (ok && steps > 0 &&
-        (ok = wait_warp(bar(F_DQ), (uint32_t)(steps - 1) & 1u, abort_flag, p.timeout_ns))) {
-      tc_fence_after();
-      dq_share_out(tmem + lane_off + COL_DQ + 32 * hf, stg, &tm_dqacc, 32 * hf,
-                   share_row(steps - 1));
-    }
-    if (lane == 0) bulk_wait_all();   // the reduce-adds are done with the staging box
-    __syncwarp();
     if (ok && (ok = wait_warp(bar(F_DONE), 0, abort_flag, p.timeout_ns))) {
       tc_fence_after();
-      const bool live = key < len;
-      const long long off = ((long long)(row0 + key) * p.Hkv + kvh) * D + hf * (D / 2);
-      store_row_bf16<D / 2>(tmem + lane_off + COL_DV + hf * (D / 2), 1.f, p.dv + off, live);
-      store_row_bf16<D / 2>(tmem + lane_off + COL_DK + hf * (D / 2), p.scale, p.dk + off, live);
+      // column quarters 0, 1: the two halves of dV; 2, 3: those of dK
+      const bool live = key < len, is_k = cq >= 2;
+      const long long off = ((long long)(row0 + key) * p.Hkv + kvh) * D + ch * (D / 2);
+      store_row_bf16<D / 2>(tmem + lane_off + (is_k ? COL_DK : COL_DV) + ch * (D / 2),
+                            is_k ? p.scale : 1.f, (is_k ? p.dk : p.dv) + off, live);
     }
   }
   tc_fence_before();
