@@ -36,10 +36,13 @@ constexpr int F_THREADS = 64 + 32 * (F_SM_WARPS + F_DQ_WARPS);
 
 struct FCfg {
   static constexpr int D = 64;
+  // ring slots: a step's Q and dO take about a step to arrive, so they are
+  // requested two steps ahead
+  static constexpr int STAGES = 3;
   static constexpr uint32_t TILE = CHUNK_BYTES;                  // 128 x 64 bf16
   static constexpr uint32_t SLOT = 2 * TILE + 1024;              // Q, dO, lse2 row, dsum row
   static constexpr uint32_t OFF_RING = 2 * TILE;                 // after K, V
-  static constexpr uint32_t OFF_DS = OFF_RING + 2 * SLOT;        // dS, 128 queries x 128 keys
+  static constexpr uint32_t OFF_DS = OFF_RING + STAGES * SLOT;   // dS, 128 queries x 128 keys
   static constexpr uint32_t OFF_STG = OFF_DS + 2 * TILE;         // 4 dQ warps x 32 rows x 64 fp32
   static constexpr uint32_t STG_WARP = 32 * 256;                 // four boxes of 16 columns
   static constexpr uint32_t OFF_CTL = OFF_STG + F_DQ_WARPS * STG_WARP;
@@ -51,11 +54,9 @@ struct FCfg {
 
 enum : int {
   F_STATIC = 0,   // K, V loaded
-  F_FULL0,        // ring slot s loaded, s < 2
-  F_FULL1,
-  F_EMPTY0,       // ring slot s consumed
-  F_EMPTY1,
-  F_DONE,         // dK, dV final
+  F_FULL0,        // ring slot s loaded, s < 3
+  F_EMPTY0 = F_FULL0 + FCfg::STAGES,   // ring slot s consumed
+  F_DONE = F_EMPTY0 + FCfg::STAGES,    // dK, dV final
   F_DRAIN,        // abort drain of the MMA issuer
   F_ST,           // S^T of the step in TMEM
   F_DPT,          // dP^T of the step in TMEM
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   if (warp == 1) {
     if (lane == 0) {
       mbar_init(bar(F_STATIC), 1);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < C::STAGES; ++s) {
         mbar_init(bar(F_FULL0 + s), 1);
         mbar_init(bar(F_EMPTY0 + s), 1);
       }
@@ -249,9 +250,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       tma_load_3d(k_s, &tm_k, bar(F_STATIC), 0, kvh, row0 + jb * BM);
       tma_load_3d(v_s, &tm_v, bar(F_STATIC), 0, kvh, row0 + jb * BM);
       for (int s = 0; ok && s < steps; ++s) {
-        const int slot = s & 1;
-        if (s >= 2 && !(ok = wait_bounded(bar(F_EMPTY0 + slot), (uint32_t)((s - 2) >> 1) & 1u,
-                                          abort_flag, p.timeout_ns)))
+        const int slot = s % C::STAGES;
+        if (s >= C::STAGES &&
+            !(ok = wait_bounded(bar(F_EMPTY0 + slot), (uint32_t)(s / C::STAGES - 1) & 1u,
+                                abort_flag, p.timeout_ns)))
           break;
         const int h = kvh * p.group + s / nq;
         const int ib = i0 + s % nq;
@@ -267,9 +269,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       }
       if (*abort_flag) {   // drain: bounded waits for the copies issued
         wait_drain(bar(F_STATIC), 0, p.timeout_ns);
-        for (int s = 0; s < 2 && s < issued; ++s) {
-          const int last = s + 2 * ((issued - 1 - s) / 2);
-          wait_drain(bar(F_FULL0 + s), (uint32_t)(last >> 1) & 1u, p.timeout_ns);
+        for (int s = 0; s < C::STAGES && s < issued; ++s) {
+          const int last = s + C::STAGES * ((issued - 1 - s) / C::STAGES);
+          wait_drain(bar(F_FULL0 + s), (uint32_t)(last / C::STAGES) & 1u, p.timeout_ns);
         }
       }
     }
@@ -298,9 +300,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       tc_commit_warp(bar(F_DPT));
     }
     for (int s = 0; ok && s < steps; ++s) {
-      const int slot = s & 1;
+      const int slot = s % C::STAGES, nslot = (s + 1) % C::STAGES;
       const uint32_t q_s = ring + slot * C::SLOT;
-      const uint32_t q_n = ring + (slot ^ 1) * C::SLOT;
+      const uint32_t q_n = ring + nslot * C::SLOT;
       const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, CHUNK_BYTES, 1024);
       const uint64_t q_mn = smem_desc_sw128(q_s, CHUNK_BYTES, 1024);
       if (!(ok = wait_warp(bar(F_PT), (uint32_t)s & 1u, abort_flag, p.timeout_ns))) break;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       issue_pv_quarters_warp(tmem + COL_DV, tmem + COL_ST, do_mn, s > 0);
       const bool more = s + 1 < steps;
       if (more) {
-        if (!(ok = wait_warp(bar(F_FULL0 + (slot ^ 1)), (uint32_t)((s + 1) >> 1) & 1u,
+        if (!(ok = wait_warp(bar(F_FULL0 + nslot), (uint32_t)((s + 1) / C::STAGES) & 1u,
                              abort_flag, p.timeout_ns)))
           break;
         tc_fence_after();
@@ -368,8 +370,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     const bool kdead = key >= len;
     bool ok = true;
     for (int s = 0; ok && s < steps; ++s) {
-      const int slot = s & 1;
-      if (!(ok = wait_warp(bar(F_FULL0 + slot), (uint32_t)(s >> 1) & 1u, abort_flag,
+      const int slot = s % C::STAGES;
+      if (!(ok = wait_warp(bar(F_FULL0 + slot), (uint32_t)(s / C::STAGES) & 1u, abort_flag,
                            p.timeout_ns)) ||
           !(ok = wait_warp(bar(F_ST), (uint32_t)s & 1u, abort_flag, p.timeout_ns)))
         break;
