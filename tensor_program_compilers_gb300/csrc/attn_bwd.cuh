@@ -42,6 +42,7 @@ struct BwdParams {
   int *pstart;           // [B+1] padded start of each sequence (set-up pass)
   float *lse2;           // [Hq, rows_pad]: LSE log2(e); +inf on padding rows
   float *dsum;           // [Hq, rows_pad]: D = rowsum(dO o O); 0 on padding rows
+                         // (the single pass stores both negated)
   float *dq_acc;         // single pass, d = 64: [Hq, rows_pad, 64] fp32 dS K sums
   int B, Hq, Hkv, N, T, nb_max, group, causal;
   float scale, scale_log2;
@@ -170,9 +171,11 @@ enum : int {
 // ------------------------------------------------------------------ row pass
 // Eight lanes per (head, padded row), 16-byte loads: D = sum_c dO o O and
 // LSE log2(e); padding rows of a sequence get D = 0 and +inf, which zeroes
-// their P in the kernels.  ZERO_ACC (single pass, d = 64): the row of the
-// fp32 dQ buffer is zeroed as well.
-template <int D, bool ZERO_ACC = false>
+// their P in the kernels.  SINGLE (single pass, d = 64): both values are
+// stored negated (the kernel then adds them with packed fp32 instructions,
+// which take no negated operands), and the row of the fp32 dQ buffer is
+// zeroed as well.
+template <int D, bool SINGLE = false>
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31, seg = lane & 7;
   const long long row = (long long)blockIdx.x * 32 + (threadIdx.x >> 3);   // h rows_pad + r
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   const int b = live ? seq_of_padded_row(p, r) : 0;
   const int i = r - p.pstart[b];
   const bool pad = live && i >= p.seq_len(b);
-  if (ZERO_ACC && live) {
+  if (SINGLE && live) {
     float4 *z = reinterpret_cast<float4 *>(p.dq_acc + row * 64 + seg * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -208,12 +211,13 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const BwdParams p) {
   }
   for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (seg == 0) {
+    const float sg = SINGLE ? -1.f : 1.f;
     if (pad) {
-      p.lse2[row] = INFINITY;
+      p.lse2[row] = sg * INFINITY;
       p.dsum[row] = 0.f;
     } else if (live) {
-      p.dsum[row] = acc;
-      p.lse2[row] = p.lse[p.lse_index(b, h, i)] * 1.4426950408889634f;
+      p.dsum[row] = sg * acc;
+      p.lse2[row] = sg * (p.lse[p.lse_index(b, h, i)] * 1.4426950408889634f);
     }
   }
 }

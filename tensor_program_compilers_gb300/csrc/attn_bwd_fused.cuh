@@ -377,9 +377,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         break;
       tc_fence_after();
       const int ib = i0 + s % nq;
-      const float *lse2 =
+      // the step's rows, stored negated by the row pass: -LSE log2(e), -D
+      const float *nlse2 =
           reinterpret_cast<const float *>(smem + C::OFF_RING + slot * C::SLOT + 2 * C::TILE);
-      const float *dsum = lse2 + 128;
+      const float *ndsum = nlse2 + 128;
       const bool diag = p.causal && ib == jb;
       // phase 1: P^T = 2^(S^T c - LSE2), bf16, kept in registers for dS; a
       // key past the end of its sequence gets P = 0 (its dK, dV rows are not
@@ -391,20 +392,24 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         tmem_wait_ld();
         reg_fence32(us);
         if (!diag && !kdead) {
+          const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
           for (int x = 0; x < 32; x += 4) {
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2 + c0 + x);
-            pw[x >> 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x]) * c - l4.x),
-                                     ex2_approx(__uint_as_float(us[x + 1]) * c - l4.y));
-            pw[(x >> 1) + 1] = pack_bf16x2(ex2_approx(__uint_as_float(us[x + 2]) * c - l4.z),
-                                           ex2_approx(__uint_as_float(us[x + 3]) * c - l4.w));
+            const float4 l4 = *reinterpret_cast<const float4 *>(nlse2 + c0 + x);
+            float a0, a1, a2, a3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(us[x]), __uint_as_float(us[x + 1])), c2,
+                             f2_pack(l4.x, l4.y)), a0, a1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(us[x + 2]), __uint_as_float(us[x + 3])), c2,
+                             f2_pack(l4.z, l4.w)), a2, a3);
+            pw[x >> 1] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+            pw[(x >> 1) + 1] = pack_bf16x2(ex2_approx(a2), ex2_approx(a3));
           }
         } else {
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
             const int qc = c0 + x;
-            float p0 = ex2_approx(__uint_as_float(us[x]) * c - lse2[qc]);
-            float p1 = ex2_approx(__uint_as_float(us[x + 1]) * c - lse2[qc + 1]);
+            float p0 = ex2_approx(fmaf(__uint_as_float(us[x]), c, nlse2[qc]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(us[x + 1]), c, nlse2[qc + 1]));
             // query ib*128 + qc sees key iff query >= key
             if (kdead || (diag && ib * BM + qc < key)) p0 = 0.f;
             if (kdead || (diag && ib * BM + qc + 1 < key)) p1 = 0.f;
@@ -428,15 +433,15 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         uint32_t dw[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
-          const float4 d4 = *reinterpret_cast<const float4 *>(dsum + c0 + x);
+          const float4 d4 = *reinterpret_cast<const float4 *>(ndsum + c0 + x);
           const uint32_t w0 = pw[x >> 1], w1 = pw[(x >> 1) + 1];
           float a0, a1, a2, a3;
           f2_unpack(f2_mul(bf16x2_widen(w0),
                            f2_add(f2_pack(__uint_as_float(ud[x]), __uint_as_float(ud[x + 1])),
-                                  f2_pack(-d4.x, -d4.y))), a0, a1);
+                                  f2_pack(d4.x, d4.y))), a0, a1);
           f2_unpack(f2_mul(bf16x2_widen(w1),
                            f2_add(f2_pack(__uint_as_float(ud[x + 2]), __uint_as_float(ud[x + 3])),
-                                  f2_pack(-d4.z, -d4.w))), a2, a3);
+                                  f2_pack(d4.z, d4.w))), a2, a3);
           dw[x >> 1] = pack_bf16x2(a0, a1);
           dw[(x >> 1) + 1] = pack_bf16x2(a2, a3);
         }
