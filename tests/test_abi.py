@@ -203,3 +203,45 @@ def test_bwd_workspace_size():
     # padded blocks: ceil(rows / 128) + B; two fp32 values per (head, padded row); B + 1 ints
     assert pkg.attn_bwd_workspace_bytes(2, 8, 300) == 2 * 8 * (5 + 2) * 128 * 4 + 3 * 4
     assert pkg.attn_bwd_workspace_bytes(3, 4, 1000, packed=True) == 2 * 4 * (8 + 3) * 128 * 4 + 16
+
+
+def call_bwd_single(**kw):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, dout=0x5000, lse=0x6000, dq=0x7000,
+                dk=0x8000, dv=0x9000, B=2, Hq=8, Hkv=2, N=256, d=64, scale=0.125, causal=1,
+                cu_seqlens=None, workspace=0xA000, workspace_bytes=1 << 24, stream=0)
+    args.update(kw)
+    return pkg.attn_bwd_single_pass(check=False, **args)
+
+
+@pytest.mark.parametrize("kw", [dict(d=128), dict(d=256), dict(d=32), dict(Hq=6, Hkv=4),
+                                dict(scale=0.0), dict(dq=None), dict(lse=None),
+                                dict(workspace=None), dict(workspace_bytes=16),
+                                # the two-kernel path's workspace (rows 512: 4 + 2
+                                # padded blocks) is too small here
+                                dict(workspace_bytes=2 * 8 * (4 + 2) * 128 * 4 + 3 * 4),
+                                dict(N=1 << 30, B=4)])
+def test_bwd_single_pass_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert call_bwd_single(**kw) == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(dq=0x7008), dict(dk=0x8004), dict(workspace=0xA008),
+                                dict(lse=0x6002), dict(cu_seqlens=0xB002)])
+def test_bwd_single_pass_misaligned_pointers_rejected(lib, kw):
+    assert call_bwd_single(**kw) == pkg.ATTN_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(N=0)])
+def test_bwd_single_pass_empty_problem_is_a_no_op(lib, kw):
+    assert call_bwd_single(**kw) == pkg.ATTN_OK
+
+
+def test_bwd_single_pass_workspace_size():
+    # the fp32 dQ buffer (Hq x padded rows x 64) ahead of the two-kernel path's workspace
+    for B, Hq, N, packed in ((2, 8, 300, False), (3, 4, 1000, True), (1, 1, 1, False)):
+        rows = N if packed else B * N
+        rows_pad = ((rows + 127) // 128 + B) * 128
+        base = pkg.attn_bwd_workspace_bytes(B, Hq, N, packed=packed)
+        assert pkg.attn_bwd_single_pass_workspace_bytes(B, Hq, N, packed=packed) == \
+            Hq * rows_pad * 64 * 4 + base
+    assert pkg.attn_bwd_single_pass_workspace_bytes(0, 8, 300) == 0
+    assert pkg.attn_bwd_single_pass_workspace_bytes(2, 8, 0) == 0
