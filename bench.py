@@ -468,9 +468,12 @@ def run_backward(pkg, dev, flush, steps, shape="backward", seqlen=None):
     if st != pkg.ATTN_OK:
         raise RuntimeError(f"backward run: {pkg.attn_status_string(st)}")
     fwd_flops = 4.0 * B * Hq * N * N * d / 2
+    tf = 2.5 * fwd_flops / (t / 1e3) / 1e12
+    peak = measured_peaks().get("bf16_tflops")
     return {"workload": f"backward B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} causal"
                         + (", single pass" if single else ""),
-            "tflops": round(2.5 * fwd_flops / (t / 1e3) / 1e12, 2), "ms_per_step": round(t, 5),
+            "tflops": round(tf, 2), "ms_per_step": round(t, 5),
+            "frac_of_peak": round(tf / peak, 4) if peak else None,
             "flop_convention": "2.5 x forward"}
 
 
