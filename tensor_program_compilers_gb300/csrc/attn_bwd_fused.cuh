@@ -125,8 +125,8 @@ __device__ __forceinline__ void issue_pv_quarters_warp(uint32_t d_tmem, uint32_t
 
 // dK += dS^T Q: A = dS^T in TMEM (bf16 pairs, queries 16 kk .. 16 kk + 15 at
 // column 8 kk), B = Q (queries x head dim, N-major, 16 queries = 2048 bytes
-// per step).  (With A read from shared memory instead, an N = 64 product
-// needs more shared-memory bandwidth per cycle than the SM has.)
+// per step).  (A read from the shared dS tile instead, an N = 64 product
+// that fetches 6 KB of operands per 32-cycle MMA, was measured slower.)
 __device__ __forceinline__ void issue_dk_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t q_mn,
                                               bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(64, 1);
@@ -163,7 +163,8 @@ __device__ __forceinline__ void dq_share_out(uint32_t taddr, uint32_t stg, uint3
   const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    st_shared_v4(line + ((j ^ sw) << 4), make_uint4(u0[4 * j], u0[4 * j + 1], u0[4 * j + 2], u0[4 * j + 3]));
+    st_shared_v4(line + ((j ^ sw) << 4),
+                 make_uint4(u0[4 * j], u0[4 * j + 1], u0[4 * j + 2], u0[4 * j + 3]));
     st_shared_v4(line + 2048 + ((j ^ sw) << 4),
                  make_uint4(u0[16 + 4 * j], u0[17 + 4 * j], u0[18 + 4 * j], u0[19 + 4 * j]));
     st_shared_v4(line + 4096 + ((j ^ sw) << 4),
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     // the previous one; the softmax warps rewrite dS^T (TMEM) and the dS tile
     // only after dP^T(s+1), which follows dQ(s), has completed.  (Issuing
     // dP^T(s+1) before dK(s) and dQ(s), as soon as dP^T(s) is loaded, was
-    // measured slower: the next step's dQ share then waits longer.)
+    // measured slower.)
     const uint64_t kdesc = smem_desc_sw128(k_s, 16, 1024);
     const uint64_t vdesc = smem_desc_sw128(v_s, 16, 1024);
     const uint64_t k_mn = smem_desc_sw128(k_s, CHUNK_BYTES, 1024);
