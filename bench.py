@@ -588,6 +588,85 @@ def run_e2e_pipelined(pkg, W, wl, inp, dev, steps):
     return dict(ms=ms, steps=steps, flops=flops, h2d=h2d, d2h=d2h)
 
 
+def run_e2e_one_copy_stream(pkg, W, wl, inp, dev, steps):
+    """The e2e measurement with every copy on one copy stream, in the order
+    in(0), in(1), out(0), in(2), out(1), ...: step i+1's inputs still go in
+    while step i's forward runs, but the two directions never share the host
+    link at the same time (on some hosts copies in and out that overlap each
+    other move less than the two in turn).  Two buffer sets as in
+    run_e2e_pipelined; the interval runs from the first copy in to the last
+    copy out."""
+    import torch
+    qh, kh, vh = (t.pin_memory() for t in (inp.q, inp.k, inp.v))
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    lse_shape = (wl.Hq, inp.n_arg) if wl.varlen else (wl.B, wl.Hq, wl.N)
+    sets = []
+    for _ in range(2):
+        q, k, v = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+        sets.append(dict(q=q, k=k, v=v, o=torch.empty_like(q),
+                         lse=torch.empty(lse_shape, dtype=torch.float32, device=dev),
+                         oh=torch.empty(q.shape, dtype=q.dtype).pin_memory(),
+                         lh=torch.empty(lse_shape, dtype=torch.float32).pin_memory()))
+    s_copy, s_run = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    ran = [None, None]      # forward of the set's last step done (inputs free)
+    loaded = [None, None]   # the set's inputs copied in
+    read = [None, None]     # read-back of the set's last step done (outputs free)
+
+    def copy_in(i):
+        b = sets[i & 1]
+        with torch.cuda.stream(s_copy):
+            if ran[i & 1] is not None:
+                s_copy.wait_event(ran[i & 1])
+            b["q"].copy_(qh, non_blocking=True)
+            b["k"].copy_(kh, non_blocking=True)
+            b["v"].copy_(vh, non_blocking=True)
+            e = ev()
+            e.record(s_copy)
+        loaded[i & 1] = e
+
+    def forward_and_out(i, more):
+        b = sets[i & 1]
+        s_run.wait_event(loaded[i & 1])
+        if read[i & 1] is not None:
+            s_run.wait_event(read[i & 1])
+        pkg.attn_fwd(b["q"], b["k"], b["v"], b["o"], b["lse"], wl.B, wl.Hq, wl.Hkv, inp.n_arg,
+                     wl.d, wl.scale, wl.causal, cu, stream=s_run.cuda_stream)
+        done = ev()
+        done.record(s_run)
+        ran[i & 1] = done
+        if more:
+            copy_in(i + 1)   # ahead of this step's read-back on the copy stream
+        with torch.cuda.stream(s_copy):
+            s_copy.wait_event(done)
+            b["oh"].copy_(b["o"], non_blocking=True)
+            b["lh"].copy_(b["lse"], non_blocking=True)
+            back = ev()
+            back.record(s_copy)
+        read[i & 1] = back
+
+    def run(n):
+        copy_in(0)
+        for i in range(n):
+            forward_and_out(i, i + 1 < n)
+
+    run(2)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(s_copy)
+    run(steps)
+    e1.record(s_copy)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    flops = W.causal_flops(wl, inp.lens)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = sets[0]["oh"].numel() * 2 + sets[0]["lh"].numel() * 4
+    return dict(ms=ms, steps=steps, flops=flops, h2d=h2d, d2h=d2h)
+
+
 def cpu_baseline(W, wl, inp, target_s=12.0):
     """The fp64 oracle, as it stands, on a bounded seeded row sample of the
     same workload, timed on this host's cores."""
@@ -657,17 +736,32 @@ def native(args):
         r = run_e2e_pipelined(pkg, W, wl, res["inp"], dev, args.e2e_steps)
         e_max = reduce_max(r["ms"] / 1e3, dev)
         e_flops = reduce_sum(r["flops"] * r["steps"], dev)
+        r1 = run_e2e_one_copy_stream(pkg, W, wl, res["inp"], dev, args.e2e_steps)
+        o_max = reduce_max(r1["ms"] / 1e3, dev)
         rs = run_e2e(pkg, W, wl, res["inp"], dev, args.e2e_steps)
         s_max = reduce_max(rs["ms"] / 1e3, dev)
-        e2e = {"value": whole_job_rate(e_flops, e_max) / 1e12, "unit": UNIT,
+        # every schedule copies the same bytes in and out each step; the
+        # headline is the fastest of the three measured here, all reported
+        schedules = {
+            "overlapped": {"value": whole_job_rate(e_flops, e_max) / 1e12,
+                           "ms_per_step": e_max * 1e3 / r["steps"],
+                           "how": "copies in of step i+1 and out of step i-1 overlap the "
+                                  "forward of step i (three streams, two buffer sets)"},
+            "one_copy_stream": {"value": whole_job_rate(reduce_sum(r1["flops"] * r1["steps"], dev),
+                                                        o_max) / 1e12,
+                                "ms_per_step": o_max * 1e3 / r1["steps"],
+                                "how": "copies in and out on one copy stream (in of step i+1 "
+                                       "ahead of out of step i), the forward on another"},
+            "serial": {"value": whole_job_rate(reduce_sum(rs["flops"] * rs["steps"], dev),
+                                               s_max) / 1e12,
+                       "ms_per_step": s_max * 1e3 / rs["steps"],
+                       "how": "copy in, forward, copy out in order on one stream"},
+        }
+        best = max(schedules, key=lambda k: schedules[k]["value"])
+        e2e = {"value": schedules[best]["value"], "unit": UNIT,
                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-               "steps": r["steps"], "ms_per_step": e_max * 1e3 / r["steps"],
-               "how": "copies in of step i+1 and out of step i-1 overlap the forward of "
-                      "step i (three streams, two buffer sets)",
-               "serial": {"value": whole_job_rate(reduce_sum(rs["flops"] * rs["steps"], dev),
-                                                  s_max) / 1e12,
-                          "ms_per_step": s_max * 1e3 / rs["steps"],
-                          "how": "copy in, forward, copy out in order on one stream"}}
+               "steps": r["steps"], "ms_per_step": schedules[best]["ms_per_step"],
+               "schedule": best, "how": schedules[best]["how"], "schedules": schedules}
 
     per_workload = {}
     if not args.no_per_workload:
